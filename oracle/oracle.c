@@ -1,0 +1,434 @@
+/*
+ * oracle.c -- plain CPU oracle for paging a hybrid KDA + MLA model's cache
+ * between a paged pool and per-chunk objects.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this file's library. The product library never links,
+ * includes or calls it, and it shares no code with the product.
+ *
+ * Everything here is integer arithmetic and memcpy; there is no floating
+ * point, so "correct" means byte-identical.
+ *
+ * Sources (page title, section):
+ *   [KL]  "Kimi-Linear" (LMCache recipe): chunk size a multiple of N; the
+ *         [N, 2N) scheduler budget; snapshots at block boundaries.
+ *   [K3]  "Kimi K3" (LMCache recipe): --chunk-size is a minimum, negotiated
+ *         to the smallest multiple of N at or above it.
+ *   [VB]  "How vLLM manages the KV cache of hybrid models: Kimi Linear /
+ *         Kimi K3" (blog): §2.1 KDA state shapes, §2.2 grouping by equal
+ *         spec, §3.1 padded shared-tensor layout (path A), §3.2 packed layout
+ *         (path B), §4 the byte buffer and its per-layer views.
+ *   [MC]  "When Prefix Cache Meets KDA" (Mooncake post), section "Flat KV":
+ *         69 KDA layers split into three groups of 23, plus the
+ *         full-attention group, on 24 physical slabs.
+ *   [HM]  "Hybrid Attention Models" (LMCache docs), "Object-group
+ *         separation": one object group per cross-chunk attention window.
+ *
+ * Readings where the pages leave a step open (each is listed in the design
+ * notes): equal-spec layers are split into near-equal runs whose count is
+ * fixed by the smallest per-spec layer count; slab t holds the t-th layer of
+ * every group; objects are layer-major in model order and token-major within
+ * a paged layer; a KDA object holds the snapshot of the chunk's last block;
+ * object offsets must be multiples of 16 bytes.
+ *
+ * Parity status: negotiation and layout sizes are pinned by values and
+ * closed forms from the pages; store/load are pinned by invariants (identity,
+ * untouched bytes) and by an independent per-token brute force. The byte
+ * order inside an object is a reading, not a value from the pages.
+ */
+#include <stdint.h>
+#include <string.h>
+
+#include "oracle.h"
+
+/* ------------------------------------------------------------------ */
+/* Chunk-size negotiation ([K3] "Chunk-Size Negotiation"; [KL], [HM]    */
+/* Step 2 for the strict form).                                         */
+/* ------------------------------------------------------------------ */
+int or_negotiate_chunk(int64_t requested, int64_t N, int strict, int64_t *out)
+{
+    if (out == NULL || N <= 0)
+        return OR_ERR_INVALID_ARG;
+    if (strict) {
+        /* Strict form: the chunk must already be a positive multiple of N. */
+        if (requested <= 0)
+            return OR_ERR_INVALID_ARG;
+        if (requested % N != 0)
+            return OR_ERR_NOT_MULTIPLE;
+        *out = requested;
+        return OR_OK;
+    }
+    /* Smallest multiple of N that is >= requested; a minimum at or below
+     * zero negotiates to N itself. */
+    if (requested <= 0) {
+        *out = N;
+        return OR_OK;
+    }
+    int64_t k = requested / N;
+    if (requested % N != 0)
+        k += 1;
+    if (k > INT64_MAX / N)
+        return OR_ERR_OVERFLOW;
+    *out = k * N;
+    return OR_OK;
+}
+
+/* Scheduler budget rule ([KL] "Why these settings"; [HM] Step 2):
+ * budget in [N, 2N) always; >= 2N only with separate object groups. */
+int or_check_step_budget(int64_t N, int64_t max_batched, int separate_object_groups)
+{
+    if (N <= 0 || max_batched <= 0)
+        return OR_ERR_INVALID_ARG;
+    if (max_batched < N)
+        return OR_ERR_BUDGET;
+    if (max_batched < 2 * N)
+        return OR_OK;
+    return separate_object_groups ? OR_OK : OR_ERR_BUDGET;
+}
+
+/* ------------------------------------------------------------------ */
+/* Layout ([VB] §2.1, §2.2, §3.1, §3.2, §4; [MC] "Flat KV").            */
+/* ------------------------------------------------------------------ */
+
+/* Bytes of one layer's page that hold data. A paged attention layer keeps
+ * one token_bytes entry per token of an N-token block ([VB] §4.2, view
+ * (num_blocks, block_size, latent)). A KDA layer keeps conv_state plus
+ * recurrent_state, independent of sequence length ([VB] §2.1). */
+static int64_t real_page_bytes(const or_layer *l, int64_t N)
+{
+    if (l->kind == OR_KDA)
+        return l->conv_bytes + l->rec_bytes;
+    return N * l->token_bytes;
+}
+
+static int same_spec(const or_layer *a, const or_layer *b)
+{
+    return a->kind == b->kind && a->token_bytes == b->token_bytes &&
+           a->conv_bytes == b->conv_bytes && a->rec_bytes == b->rec_bytes &&
+           a->window == b->window;
+}
+
+/* Object-group class of a layer ([HM] "Object-group separation"): full
+ * attention is one window; KDA (a mamba-like state) is another; each
+ * sliding-window size is its own. */
+static int same_window_class(const or_layer *a, const or_layer *b)
+{
+    if (a->kind != b->kind)
+        return 0;
+    if (a->kind == OR_SWA)
+        return a->window == b->window;
+    return 1;
+}
+
+int or_layout_build(or_layout *L)
+{
+    if (L == NULL)
+        return OR_ERR_INVALID_ARG;
+    int n = L->num_layers;
+    if (n <= 0 || n > OR_MAX_LAYERS || L->N <= 0 || L->mem_bytes < 0)
+        return OR_ERR_INVALID_ARG;
+    for (int i = 0; i < n; i++) {
+        const or_layer *l = &L->layers[i];
+        if (l->kind == OR_KDA) {
+            if (l->conv_bytes < 0 || l->rec_bytes < 0 || l->conv_bytes + l->rec_bytes <= 0)
+                return OR_ERR_INVALID_ARG;
+        } else if (l->kind == OR_MLA || l->kind == OR_SWA) {
+            if (l->token_bytes <= 0)
+                return OR_ERR_INVALID_ARG;
+            if (l->kind == OR_SWA && l->window <= 0)
+                return OR_ERR_INVALID_ARG;
+            if (l->token_bytes > INT64_MAX / L->N)
+                return OR_ERR_OVERFLOW;
+        } else {
+            return OR_ERR_INVALID_ARG;
+        }
+    }
+
+    /* Step 1: bucket layers by equal spec, specs in order of first
+     * appearance ([VB] §2.2: same_type_layers keyed by the spec). */
+    int spec_of[OR_MAX_LAYERS];
+    int spec_first[OR_MAX_LAYERS];
+    int spec_count[OR_MAX_LAYERS];
+    int num_specs = 0;
+    for (int i = 0; i < n; i++) {
+        int s;
+        for (s = 0; s < num_specs; s++)
+            if (same_spec(&L->layers[spec_first[s]], &L->layers[i]))
+                break;
+        if (s == num_specs) {
+            spec_first[s] = i;
+            spec_count[s] = 0;
+            num_specs++;
+        }
+        spec_of[i] = s;
+        spec_count[s]++;
+    }
+
+    /* Step 2: split each spec's layers into consecutive runs. With
+     * split_groups set, the number of runs of a spec is
+     * ceil(count / smallest count) and runs are near-equal, longer first;
+     * for Kimi K3 this gives 3 KDA groups of 23 and one MLA group of 24,
+     * i.e. 24 slabs ([MC] "Flat KV"). Otherwise one group per spec. */
+    int smallest = spec_count[0];
+    for (int s = 1; s < num_specs; s++)
+        if (spec_count[s] < smallest)
+            smallest = spec_count[s];
+    int g = 0;
+    int S = 0;
+    for (int s = 0; s < num_specs; s++) {
+        int cnt = spec_count[s];
+        int runs = 1;
+        if (L->split_groups)
+            runs = (cnt + smallest - 1) / smallest;
+        int base_len = cnt / runs;
+        int extra = cnt % runs;
+        int run = 0;
+        int pos_in_run = 0;
+        int run_len = base_len + (run < extra ? 1 : 0);
+        for (int i = 0; i < n; i++) {
+            if (spec_of[i] != s)
+                continue;
+            if (pos_in_run == run_len) {
+                run++;
+                pos_in_run = 0;
+                run_len = base_len + (run < extra ? 1 : 0);
+            }
+            L->kv_group[i] = g + run;
+            L->slot[i] = pos_in_run;
+            pos_in_run++;
+        }
+        for (int r = 0; r < runs; r++) {
+            int len = base_len + (r < extra ? 1 : 0);
+            L->kv_group_kind[g + r] = L->layers[spec_first[s]].kind;
+            L->kv_group_size[g + r] = len;
+            if (len > S)
+                S = len;
+        }
+        g += runs;
+    }
+    L->num_kv_groups = g;
+    L->num_slabs = S;
+
+    /* Step 3: object groups, one per cross-chunk window class in order of
+     * first appearance, or a single group when separation is off. */
+    int og_first[OR_MAX_LAYERS];
+    int num_og = 0;
+    for (int i = 0; i < n; i++) {
+        if (!L->separate_object_groups) {
+            L->object_group[i] = 0;
+            num_og = 1;
+            continue;
+        }
+        int o;
+        for (o = 0; o < num_og; o++)
+            if (same_window_class(&L->layers[og_first[o]], &L->layers[i]))
+                break;
+        if (o == num_og) {
+            og_first[o] = i;
+            num_og++;
+        }
+        L->object_group[i] = o;
+    }
+    L->num_object_groups = num_og;
+
+    for (int i = 0; i < n; i++)
+        L->real_bytes[i] = real_page_bytes(&L->layers[i], L->N);
+
+    if (!L->packed) {
+        /* Path A ([VB] §3.1): one page size for every layer, the largest
+         * real page; smaller pages are padded up to it. Slab t is one tensor
+         * of page_size * num_blocks bytes shared by the t-th layer of every
+         * group, and block b sits at b * page_size inside it. */
+        int64_t page = 0;
+        for (int i = 0; i < n; i++)
+            if (L->real_bytes[i] > page)
+                page = L->real_bytes[i];
+        if (page > INT64_MAX / S)
+            return OR_ERR_OVERFLOW;
+        int64_t per_block = page * (int64_t)S;
+        int64_t nb = L->mem_bytes / per_block;
+        if (nb <= 0)
+            return OR_ERR_NO_MEMORY;
+        L->page_size = page;
+        L->block_stride = page;
+        L->num_blocks = nb;
+        L->pool_bytes = nb * per_block;
+        for (int i = 0; i < n; i++) {
+            L->page_bytes[i] = page;
+            L->stride[i] = page;
+            L->base[i] = (int64_t)L->slot[i] * page * nb;
+        }
+    } else {
+        /* Path B ([VB] §3.2): within each group, byte offsets accumulate
+         * over its layers' real pages; the block stride is the largest
+         * group total; num_blocks = memory // block_stride; each layer is
+         * the strided view (offset, block_stride) of one backing. */
+        int64_t offset_in_group[OR_MAX_LAYERS];
+        int64_t group_total[OR_MAX_LAYERS];
+        for (int k = 0; k < L->num_kv_groups; k++)
+            group_total[k] = 0;
+        for (int k = 0; k < L->num_kv_groups; k++) {
+            for (int t = 0; t < L->kv_group_size[k]; t++) {
+                for (int i = 0; i < n; i++) {
+                    if (L->kv_group[i] == k && L->slot[i] == t) {
+                        offset_in_group[i] = group_total[k];
+                        group_total[k] += L->real_bytes[i];
+                    }
+                }
+            }
+        }
+        int64_t stride = 0;
+        for (int k = 0; k < L->num_kv_groups; k++)
+            if (group_total[k] > stride)
+                stride = group_total[k];
+        int64_t nb = L->mem_bytes / stride;
+        if (nb <= 0)
+            return OR_ERR_NO_MEMORY;
+        L->page_size = 0;
+        L->block_stride = stride;
+        L->num_blocks = nb;
+        L->pool_bytes = nb * stride;
+        for (int i = 0; i < n; i++) {
+            L->page_bytes[i] = L->real_bytes[i];
+            L->stride[i] = stride;
+            L->base[i] = offset_in_group[i];
+        }
+    }
+    return OR_OK;
+}
+
+/* Bytes of one object of group og for chunk size C: the group's layers in
+ * model order; a paged layer holds the C tokens of the chunk (C/N pages),
+ * a KDA layer holds one state snapshot. */
+int64_t or_object_bytes(const or_layout *L, int64_t C, int og)
+{
+    int64_t m = C / L->N;
+    int64_t total = 0;
+    for (int i = 0; i < L->num_layers; i++) {
+        if (L->object_group[i] != og)
+            continue;
+        if (L->layers[i].kind == OR_KDA)
+            total += L->real_bytes[i];
+        else
+            total += m * L->real_bytes[i];
+    }
+    return total;
+}
+
+/* ------------------------------------------------------------------ */
+/* Store and load.                                                      */
+/* ------------------------------------------------------------------ */
+
+/* One page copy between the pool and an object, in either direction.
+ * Returns the status bits raised (0 when the copy was done). */
+static uint32_t copy_page(const or_layout *L, int layer, int64_t block,
+                          uint8_t *pool, uint8_t *obj_bytes, int to_object,
+                          uint32_t missing_bit)
+{
+    if (block == -1)
+        return missing_bit;
+    if (block < 0 || block >= L->num_blocks)
+        return OR_ST_BLOCK_OOR;
+    uint8_t *page = pool + L->base[layer] + block * L->stride[layer];
+    if (to_object)
+        memcpy(obj_bytes, page, (size_t)L->real_bytes[layer]);
+    else
+        memcpy(page, obj_bytes, (size_t)L->real_bytes[layer]);
+    return 0;
+}
+
+static int check_tables(const or_layout *L, const or_tables *T)
+{
+    if (T == NULL || T->num_kv_groups != L->num_kv_groups || T->num_requests < 0)
+        return OR_ERR_INVALID_ARG;
+    for (int k = 0; k < L->num_kv_groups; k++)
+        if ((T->num_requests > 0 && T->table[k] == NULL) || T->num_cols[k] < 0 ||
+            T->row_stride[k] < T->num_cols[k])
+            return OR_ERR_INVALID_ARG;
+    return OR_OK;
+}
+
+/* Moves every object of every job, in either direction. */
+static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
+                        const or_tables *T, const or_jobs *J,
+                        uint8_t *arena, int64_t arena_bytes, uint32_t *status,
+                        int to_object)
+{
+    if (L == NULL || pool == NULL || J == NULL || status == NULL)
+        return OR_ERR_INVALID_ARG;
+    if (C <= 0 || C % L->N != 0)
+        return OR_ERR_NOT_MULTIPLE;
+    int rc = check_tables(L, T);
+    if (rc != OR_OK)
+        return rc;
+    if (J->num_object_groups != L->num_object_groups)
+        return OR_ERR_INVALID_ARG;
+    int64_t m = C / L->N;
+
+    for (int og = 0; og < L->num_object_groups; og++) {
+        int64_t obj_size = or_object_bytes(L, C, og);
+        for (int64_t q = 0; q < J->num_jobs[og]; q++) {
+            const or_job *job = &J->jobs[og][q];
+            int64_t r = job->request;
+            int64_t c = job->chunk;
+            /* A job must name a request of the batch, a non-negative chunk,
+             * and a 16-byte aligned object that fits the arena. */
+            if (r < 0 || r >= T->num_requests || c < 0 || job->offset < 0 ||
+                job->offset % 16 != 0 || obj_size > arena_bytes ||
+                job->offset > arena_bytes - obj_size) {
+                *status |= OR_ST_BAD_JOB;
+                continue;
+            }
+            uint8_t *obj = arena + job->offset;
+            int64_t cursor = 0;
+            for (int i = 0; i < L->num_layers; i++) {
+                if (L->object_group[i] != og)
+                    continue;
+                int k = L->kv_group[i];
+                const int32_t *row = T->table[k] + r * T->row_stride[k];
+                if (L->layers[i].kind == OR_KDA) {
+                    /* The state a restore resumes from is the snapshot
+                     * taken at the end of the chunk's last block ([KL]
+                     * "Why these settings"; [MC] checkpoint boundaries). */
+                    int64_t pos = (c + 1) * m - 1;
+                    if (pos >= T->num_cols[k])
+                        *status |= OR_ST_BAD_JOB;
+                    else
+                        *status |= copy_page(L, i, row[pos], pool, obj + cursor,
+                                             to_object, OR_ST_NO_SNAPSHOT);
+                    cursor += L->real_bytes[i];
+                } else {
+                    /* The chunk's C tokens are its m consecutive blocks. */
+                    for (int64_t j = 0; j < m; j++) {
+                        int64_t pos = c * m + j;
+                        if (pos >= T->num_cols[k])
+                            *status |= OR_ST_BAD_JOB;
+                        else
+                            *status |= copy_page(L, i, row[pos], pool, obj + cursor,
+                                                 to_object, OR_ST_NO_BLOCK);
+                        cursor += L->real_bytes[i];
+                    }
+                }
+            }
+        }
+    }
+    return OR_OK;
+}
+
+int or_store(const or_layout *L, int64_t C, const uint8_t *pool,
+             const or_tables *T, const or_jobs *J,
+             uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    return move_objects(L, C, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1);
+}
+
+int or_load(const or_layout *L, int64_t C, uint8_t *pool,
+            const or_tables *T, const or_jobs *J,
+            const uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    return move_objects(L, C, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0);
+}

@@ -1,0 +1,393 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each check takes an oracle library handle (the real build, or a mutated copy
+in the mutation tests) and raises AssertionError when the oracle disagrees
+with the pages' printed values, a closed form, an invariant, or the
+independent per-token brute force. Run as a script, it runs every check
+against the library path given on the command line and exits non-zero on
+the first failure.
+"""
+from __future__ import annotations
+
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import oracle  # noqa: E402
+from oracle import brute  # noqa: E402
+import workloads as W  # noqa: E402
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                yield line.split()
+
+
+# ----------------------------------------------------------------------------
+# Negotiation and budget
+# ----------------------------------------------------------------------------
+
+def check_negotiation_golden(lib):
+    for req, N, strict, exp in _rows("negotiation.txt"):
+        try:
+            got = oracle.negotiate_chunk(int(req), int(N), bool(int(strict)), _lib=lib)
+        except oracle.OracleError as e:
+            got = {oracle.ERR_NOT_MULTIPLE: "ERR_NOT_MULTIPLE",
+                   oracle.ERR_INVALID_ARG: "ERR_INVALID_ARG"}.get(e.code, e.code)
+        assert str(got) == exp, (req, N, strict, got, exp)
+
+
+def check_negotiation_bruteforce(lib):
+    # The smallest multiple of N that is >= the request, found by search.
+    for N in range(1, 41):
+        for req in list(range(-3, 300)) + [997, 1000]:
+            k = 1
+            while k * N < req:
+                k += 1
+            assert oracle.negotiate_chunk(req, N, False, _lib=lib) == k * N, (req, N)
+            if req > 0:
+                if req % N == 0:
+                    assert oracle.negotiate_chunk(req, N, True, _lib=lib) == req
+                else:
+                    try:
+                        oracle.negotiate_chunk(req, N, True, _lib=lib)
+                        raise AssertionError("strict accepted a non-multiple")
+                    except oracle.OracleError as e:
+                        assert e.code == oracle.ERR_NOT_MULTIPLE
+
+
+def check_negotiation_edges(lib):
+    for N in (0, -5):
+        try:
+            oracle.negotiate_chunk(100, N, False, _lib=lib)
+            raise AssertionError("N <= 0 accepted")
+        except oracle.OracleError as e:
+            assert e.code == oracle.ERR_INVALID_ARG
+    try:
+        oracle.negotiate_chunk(2**63 - 5, 10, False, _lib=lib)
+        raise AssertionError("overflow not reported")
+    except oracle.OracleError as e:
+        assert e.code == oracle.ERR_OVERFLOW
+    assert oracle.negotiate_chunk(2**62, 2**62, False, _lib=lib) == 2**62
+
+
+def check_budget(lib):
+    for N, B, sep, exp in _rows("step_budget.txt"):
+        rc = oracle.check_step_budget(int(N), int(B), bool(int(sep)), _lib=lib)
+        assert (rc == 0) == (exp == "OK"), (N, B, sep, rc, exp)
+    # Exhaustive on small N: allowed iff N <= B < 2N, or B >= 2N with separation.
+    for N in range(1, 30):
+        for B in range(1, 100):
+            for sep in (0, 1):
+                ok = (N <= B < 2 * N) or (B >= 2 * N and sep == 1)
+                assert (oracle.check_step_budget(N, B, sep, _lib=lib) == 0) == ok, (N, B, sep)
+
+
+# ----------------------------------------------------------------------------
+# Layout
+# ----------------------------------------------------------------------------
+
+def _kimi_linear_state(tp):
+    return W.kda(12288 // tp, 3, 32 // tp, 128)
+
+
+def check_page_formulas(lib):
+    """MLA page = N * token_bytes and KDA page = conv + recurrent bytes, pinned
+    by the Kimi-Linear block sizes (944 at TP 2, 1888 at TP 1): at the page's
+    N the attention page covers the state page, and 16 tokens fewer does not."""
+    for tp, N in _rows("block_size.txt"):
+        tp, N = int(tp), int(N)
+        spec = [_kimi_linear_state(tp), W.mla(1152)]
+        for n in (N, N - 16):
+            L = oracle.layout(spec, n, False, 1 << 40, _lib=lib)
+            kda_page, mla_page = L.real_bytes
+            assert kda_page == (12288 // tp) * 3 * 2 + (32 // tp) * 128 * 128 * 4
+            assert mla_page == n * 1152
+            if n == N:
+                assert mla_page >= kda_page
+                # padded path A: the smaller (KDA) page is padded to the MLA page
+                assert L.page_size == mla_page and L.page_bytes == [mla_page, mla_page]
+            else:
+                assert mla_page < kda_page
+
+
+def check_k3_groups(lib):
+    rows = {r[0]: r[1:] for r in _rows("k3_groups.txt")}
+    L = oracle.layout(W.CONFIGS[3].layers, 768, False, 1 << 50, _lib=lib)
+    kda_sizes = [s for s, k in zip(L.kv_group_size, L.kv_group_kind) if k == "KDA"]
+    mla_sizes = [s for s, k in zip(L.kv_group_size, L.kv_group_kind) if k == "MLA"]
+    assert kda_sizes == [int(x) for x in rows["KDA"]], kda_sizes
+    assert mla_sizes == [int(x) for x in rows["MLA"]], mla_sizes
+    assert L.num_slabs == int(rows["slabs"][0])
+    # each group holds consecutive layers of one kind, in model order
+    for g in range(L.num_kv_groups):
+        members = [i for i in range(93) if L.kv_group[i] == g]
+        assert all(L.kinds[i] == L.kv_group_kind[g] for i in members)
+        assert [L.slot[i] for i in members] == list(range(len(members)))
+
+
+def check_closed_forms(lib):
+    """Padded page_size = the largest page; packed block_stride = the largest
+    group total; num_blocks = memory // (bytes per block)."""
+    layers = W.CONFIGS[1].layers
+    mem = 13_754_695_680 + 12345
+    kda_page = 73_728 + 2_097_152
+    mla_page = 944 * 1152
+    P = oracle.layout(layers, 944, False, mem, _lib=lib)
+    assert P.kv_group_kind == ["KDA", "KDA", "KDA", "MLA"] and P.kv_group_size == [6, 6, 6, 6]
+    assert P.num_slabs == 6 and P.page_size == max(kda_page, mla_page) == kda_page
+    assert P.num_blocks == mem // (6 * kda_page) == 1056
+    assert P.pool_bytes == 1056 * 6 * kda_page
+    assert P.num_object_groups == 2 and P.object_group[:4] == [0, 0, 0, 1]
+    for i in range(24):
+        assert P.base[i] == P.slot[i] * kda_page * P.num_blocks and P.stride[i] == kda_page
+    Q = oracle.layout(layers, 944, True, mem, _lib=lib)
+    assert Q.block_stride == max(6 * kda_page, 6 * mla_page) == 13_025_280
+    assert Q.num_blocks == mem // 13_025_280
+    assert Q.page_size == 0 and Q.page_bytes == Q.real_bytes
+    # The MLA group's pages sit back to back from offset 0 of the block.
+    mla_layers = [i for i in range(24) if Q.kinds[i] == "MLA"]
+    assert [Q.base[i] for i in mla_layers] == [t * mla_page for t in range(6)]
+    # object sizes for chunk C = N
+    assert P.object_bytes(944, 0) == 18 * kda_page
+    assert P.object_bytes(944, 1) == 6 * mla_page
+    assert P.object_bytes(1888, 1) == 12 * mla_page and P.object_bytes(1888, 0) == 18 * kda_page
+    # tiny case: 64 blocks of one 73,728-byte slab
+    T = oracle.layout(W.CONFIGS[0].layers, 64, False, 64 * 73_728, _lib=lib)
+    assert T.num_slabs == 1 and T.num_kv_groups == 4 and T.page_size == 73_728 and T.num_blocks == 64
+    # one group per spec
+    G = oracle.layout(layers, 944, False, mem, split_groups=False, _lib=lib)
+    assert G.kv_group_size == [18, 6] and G.num_slabs == 18
+    # object-group classes: full attention, KDA, and each sliding window
+    spec = [W.kda(64, 3, 2, 16), W.swa(64, 4096), W.mla(64), W.swa(64, 512), W.swa(32, 4096)]
+    O = oracle.layout(spec, 16, True, 1 << 30, _lib=lib)
+    assert O.object_group == [0, 1, 2, 3, 1] and O.num_object_groups == 4
+    O1 = oracle.layout(spec, 16, True, 1 << 30, separate_object_groups=False, _lib=lib)
+    assert O1.object_group == [0] * 5 and O1.num_object_groups == 1
+    # too little memory for one block
+    try:
+        oracle.layout(layers, 944, True, 13_025_279, _lib=lib)
+        raise AssertionError("a pool without one whole block was accepted")
+    except oracle.OracleError as e:
+        assert e.code == oracle.ERR_NO_MEMORY
+
+
+def random_spec(rng, n_layers=None):
+    n = n_layers or int(rng.integers(1, 9))
+    kinds = rng.choice(["MLA", "KDA", "SWA"], size=n)
+    tb = int(rng.choice([16, 32, 48]))
+    conv = int(rng.choice([0, 48, 96]))
+    rec = int(rng.choice([64, 256, 1024]))
+    out = []
+    for k in kinds:
+        if k == "MLA":
+            out.append(W.mla(tb))
+        elif k == "SWA":
+            out.append(W.swa(tb, int(rng.choice([32, 64]))))
+        else:
+            out.append(W.kda(conv // 6, 3, 1, int(np.sqrt(rec // 4)) or 4) if conv else
+                       {"kind": "KDA", "token_bytes": 0, "conv_bytes": 0, "rec_bytes": rec, "window": 0})
+    return out
+
+
+def check_non_overlap(lib, trials=60):
+    """Byte-ownership maps. Pages of different blocks never share a byte;
+    inside one block, the pages of one KV group's layers never share a byte
+    (layers of different groups do alias at the same block id by design: a
+    block belongs to one group at a time, path A's shared tensors and path B's
+    per-group offsets both rely on that). Every page lies inside the pool, and
+    the brute-force layout agrees."""
+    rng = np.random.default_rng(7)
+    for t in range(trials):
+        spec = random_spec(rng)
+        N = int(rng.choice([2, 4, 8]))
+        packed = bool(t % 2)
+        split = bool((t // 2) % 2)
+        mem = int(rng.integers(2000, 40000))
+        try:
+            L = oracle.layout(spec, N, packed, mem, split_groups=split, _lib=lib)
+        except oracle.OracleError as e:
+            assert e.code == oracle.ERR_NO_MEMORY
+            continue
+        B = brute.BruteLayout(spec, N, packed, mem, split)
+        assert L.num_blocks == B.num_blocks and L.pool_bytes == B.pool_bytes
+        assert [L.kv_group[i] for i in range(len(spec))] == [B.kv_group_of[i] for i in range(len(spec))]
+        block_owner = np.full(L.pool_bytes, -1, dtype=np.int64)
+        group_owner = {g: np.zeros(L.pool_bytes, dtype=bool) for g in range(L.num_kv_groups)}
+        for i in range(len(spec)):
+            assert L.base[i] == B.tensor_offset[i] and L.stride[i] == B.layer_stride[i]
+            g = L.kv_group[i]
+            for b in range(L.num_blocks):
+                lo = L.base[i] + b * L.stride[i]
+                hi = lo + L.real_bytes[i]
+                assert 0 <= lo and hi <= L.pool_bytes, (spec, i, b)
+                seen = block_owner[lo:hi]
+                assert ((seen == -1) | (seen == b)).all(), ("two blocks share a byte", spec, i, b)
+                block_owner[lo:hi] = b
+                assert not group_owner[g][lo:hi].any(), ("one group's pages overlap", spec, i, b)
+                group_owner[g][lo:hi] = True
+        if not packed:
+            assert L.page_size == max(L.real_bytes)
+
+
+# ----------------------------------------------------------------------------
+# Store and load
+# ----------------------------------------------------------------------------
+
+def tiny_case(lib, cfg_index=0, spec=None, N=None, req_chunk=None, packed=None, lengths=None,
+              seed=0, snapshot="block", split=True, separate=True):
+    cfg = W.CONFIGS[cfg_index]
+    if spec is not None:
+        cfg = W.Config(99, "random", spec, N, req_chunk, packed, len(lengths), "fixed",
+                       tuple(lengths), snapshot=snapshot, seed=seed)
+    C = oracle.negotiate_chunk(cfg.requested_chunk, cfg.N, _lib=lib)
+    big = oracle.layout(cfg.layers, cfg.N, cfg.packed, 1 << 40, split_groups=split,
+                        separate_object_groups=separate, _lib=lib)
+    lengths = W.request_lengths(cfg)
+    need = W.count_blocks(cfg, big.kv_group_kind, lengths, cfg.N, C)
+    nb = cfg.pool_blocks or need
+    per_block = big.pool_bytes // big.num_blocks
+    L = oracle.layout(cfg.layers, cfg.N, cfg.packed, nb * per_block, split_groups=split,
+                      separate_object_groups=separate, _lib=lib)
+    assert L.num_blocks == nb
+    sizes = [L.object_bytes(C, g) for g in range(L.num_object_groups)]
+    jobs, arena_bytes = W.pack_jobs(W.store_units(lengths, C, L.num_object_groups), sizes)
+    t_src = W.block_tables(cfg, L.kv_group_kind, lengths, cfg.N, C, nb, cfg.seed)
+    t_dst = W.block_tables(cfg, L.kv_group_kind, lengths, cfg.N, C, nb, cfg.seed + 1000)
+    pool = W.fill_normal_np(L.pool_bytes, cfg.seed)
+    return dict(cfg=cfg, C=C, L=L, lengths=lengths, jobs=jobs, arena_bytes=arena_bytes,
+                t_src=t_src, t_dst=t_dst, pool=pool, sizes=sizes, split=split, separate=separate)
+
+
+def _addressed(L, C, tables, jobs):
+    """Byte mask of every pool byte a store/load of `jobs` touches (pure
+    reading of the tables; used for the untouched-bytes invariant)."""
+    mask = np.zeros(L.pool_bytes, dtype=bool)
+    m = C // L.N
+    for og, J in enumerate(jobs):
+        for job in J:
+            r, c = int(job["request"]), int(job["chunk"])
+            for i in range(len(L.kinds)):
+                if L.object_group[i] != og:
+                    continue
+                row = tables[L.kv_group[i]][r]
+                pos = [(c + 1) * m - 1] if L.kinds[i] == "KDA" else range(c * m, (c + 1) * m)
+                for p in pos:
+                    lo = L.base[i] + int(row[p]) * L.stride[i]
+                    mask[lo:lo + L.real_bytes[i]] = True
+    return mask
+
+
+def check_store_load(lib, case):
+    L, C = case["L"], case["C"]
+    pool, jobs = case["pool"], case["jobs"]
+    arena = np.zeros(case["arena_bytes"], dtype=np.uint8)
+    st = oracle.store(L, C, pool, case["t_src"], jobs, arena)
+    assert st == 0, st
+    # 1) the per-token brute force builds the same objects
+    B = brute.BruteLayout(L_spec(case), L.N, L.packed, L.pool_bytes, case["split"])
+    arena_b = np.zeros_like(arena)
+    brute.store(B, C, pool, case["t_src"], jobs, arena_b, case["separate"])
+    assert np.array_equal(arena, arena_b), "store differs from the per-token brute force"
+    # 2) load into a sentinel pool under new tables: addressed bytes restored
+    #    by the brute force as well, and every other byte keeps the sentinel
+    dst = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    assert oracle.load(L, C, dst, case["t_dst"], jobs, arena) == 0
+    dst_b = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    brute.load(B, C, dst_b, case["t_dst"], jobs, arena, case["separate"])
+    assert np.array_equal(dst, dst_b), "load differs from the per-token brute force"
+    mask = _addressed(L, C, case["t_dst"], jobs)
+    assert (dst[~mask] == W.SENTINEL).all(), "load wrote outside its target pages"
+    # 3) re-storing from the loaded pool gives the same objects (identity)
+    arena2 = np.zeros_like(arena)
+    assert oracle.store(L, C, dst, case["t_dst"], jobs, arena2) == 0
+    assert np.array_equal(arena, arena2), "store(load(x)) != x"
+    # 4) every object byte came from the source pool: objects are non-trivial
+    assert arena.any()
+
+
+def L_spec(case):
+    return case["cfg"].layers
+
+
+def check_errors(lib, case):
+    """Bad block ids and bad jobs raise their bits and skip only the page or
+    the object concerned."""
+    L, C = case["L"], case["C"]
+    pool, jobs = case["pool"], case["jobs"]
+    good = np.zeros(case["arena_bytes"], dtype=np.uint8)
+    oracle.store(L, C, pool, case["t_src"], jobs, good)
+    kda_g = L.kv_group_kind.index("KDA")
+    mla_g = L.kv_group_kind.index("MLA")
+    m = C // L.N
+    for what, bit in (("oor", oracle.ST_BLOCK_OOR), ("neg", oracle.ST_BLOCK_OOR),
+                      ("snap", oracle.ST_NO_SNAPSHOT), ("mla", oracle.ST_NO_BLOCK)):
+        tabs = [t.copy() for t in case["t_src"]]
+        if what == "oor":
+            tabs[mla_g][0, 0] = L.num_blocks
+        elif what == "neg":
+            tabs[mla_g][0, 0] = -7
+        elif what == "snap":
+            tabs[kda_g][0, m - 1] = -1
+        else:
+            tabs[mla_g][0, 0] = -1
+        a = np.full(case["arena_bytes"], 0x5A, dtype=np.uint8)
+        st = oracle.store(L, C, pool, tabs, jobs, a)
+        assert st == bit, (what, st)
+        diff = np.flatnonzero(a != good)
+        group = kda_g if what == "snap" else mla_g
+        skipped = L.real_bytes[L.kv_group.index(group)]  # one page of that group
+        assert (a[diff] == 0x5A).all()
+        assert diff.size <= skipped and diff.size > 0, (what, diff.size, skipped)
+    # bad jobs: request out of range, misaligned offset, offset past the arena,
+    # chunk past the table
+    for bad in ("req", "align", "end", "chunk"):
+        J = [j.copy() for j in jobs]
+        if bad == "req":
+            J[0][0]["request"] = len(case["lengths"])
+        elif bad == "align":
+            J[0][0]["offset"] += 8
+        elif bad == "end":
+            J[0][0]["offset"] = case["arena_bytes"]
+        else:
+            J[0][0]["chunk"] = 1 << 20
+        a = np.zeros(case["arena_bytes"], dtype=np.uint8)
+        assert oracle.store(L, C, pool, case["t_src"], J, a) & oracle.ST_BAD_JOB, bad
+
+
+ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",
+       "check_budget", "check_page_formulas", "check_k3_groups", "check_closed_forms",
+       "check_non_overlap", "check_store_load_cases"]
+
+
+def check_store_load_cases(lib):
+    check_store_load(lib, tiny_case(lib, 0))
+    rng = np.random.default_rng(11)
+    for t in range(8):
+        spec = random_spec(rng, int(rng.integers(2, 7)))
+        spec[0] = W.mla(int(rng.choice([16, 32])))
+        spec[-1] = {"kind": "KDA", "token_bytes": 0, "conv_bytes": 48, "rec_bytes": 256, "window": 0}
+        N = int(rng.choice([2, 4]))
+        lengths = [int(x) for x in rng.integers(N, 12 * N, size=3)]
+        case = tiny_case(lib, spec=spec, N=N, req_chunk=int(rng.integers(1, 3 * N)),
+                         packed=bool(t % 2), lengths=lengths, seed=t,
+                         snapshot="block", split=bool((t // 2) % 2), separate=bool((t // 4) % 2 == 0))
+        check_store_load(lib, case)
+    check_errors(lib, tiny_case(lib, 0))
+
+
+if __name__ == "__main__":
+    handle = oracle.load_variant(sys.argv[1])
+    for name in ALL:
+        globals()[name](handle)
+    print("all pins hold")

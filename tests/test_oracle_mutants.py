@@ -1,0 +1,51 @@
+"""Each plausible mistake planted in a copy of the CPU oracle must make at
+least one pin fail. The mutants are compiled from a copy in a temporary
+directory and run in a child process, so a mutant that crashes counts as
+caught and cannot take the test run down."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(os.path.dirname(HERE), "oracle", "oracle.c")
+
+MUTANTS = [
+    ("negotiation does not round up", "k += 1;", "k += 0;"),
+    ("non-positive request negotiates to 0", "*out = N;\n        return OR_OK;", "*out = 0;\n        return OR_OK;"),
+    ("budget boundary 2N included", "if (max_batched < 2 * N)", "if (max_batched <= 2 * N)"),
+    ("paged page one token short", "return N * l->token_bytes;", "return (N - 1) * l->token_bytes;"),
+    ("KDA page drops conv_state", "return l->conv_bytes + l->rec_bytes;", "return l->rec_bytes;"),
+    ("padded page is the first layer's", "if (L->real_bytes[i] > page)", "if (i == 0)"),
+    ("padded slab base ignores num_blocks", "L->base[i] = (int64_t)L->slot[i] * page * nb;",
+     "L->base[i] = (int64_t)L->slot[i] * page;"),
+    ("runs per spec rounded down", "runs = (cnt + smallest - 1) / smallest;", "runs = cnt / smallest + (cnt % smallest > 1);"),
+    ("sliding windows merged", "return a->window == b->window;", "return 1;"),
+    ("packed offset counted after the page", "offset_in_group[i] = group_total[k];\n                        group_total[k] += L->real_bytes[i];",
+     "group_total[k] += L->real_bytes[i];\n                        offset_in_group[i] = group_total[k] - L->real_bytes[0];"),
+    ("packed stride is the first group's", "if (group_total[k] > stride)", "if (k == 0)"),
+    ("KDA snapshot from the chunk's first block", "int64_t pos = (c + 1) * m - 1;", "int64_t pos = c * m;"),
+    ("paged blocks reversed in the object", "int64_t pos = c * m + j;", "int64_t pos = c * m + (m - 1 - j);"),
+    ("page copy one byte short", "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer]);",
+     "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer] - 1);"),
+    ("misaligned object offsets accepted", "job->offset % 16 != 0 ||", ""),
+    ("block id upper bound off by one", "block >= L->num_blocks", "block > L->num_blocks"),
+    ("object size counts KDA per block", "        if (L->layers[i].kind == OR_KDA)\n            total += L->real_bytes[i];",
+     "        if (0)\n            total += L->real_bytes[i];"),
+]
+
+
+@pytest.mark.parametrize("what,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, what, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site not found: {old!r}"
+    mutated = tmp_path / "oracle.c"
+    mutated.write_text(src.replace(old, new, 1))
+    so = str(tmp_path / "libmutant.so")
+    oracle.build(out_path=so, src_path=str(mutated))
+    r = subprocess.run([sys.executable, os.path.join(HERE, "oracle_pins.py"), so],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant survived every pin: {what}"
