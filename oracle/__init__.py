@@ -105,6 +105,19 @@ class _Tables(ctypes.Structure):
                 ("num_cols", ctypes.POINTER(ctypes.c_int64))]
 
 
+class _Page(ctypes.Structure):
+    _fields_ = [("pool_offset", ctypes.c_int64), ("object_offset", ctypes.c_int64), ("bytes", ctypes.c_int64),
+                ("layer", ctypes.c_int32), ("block", ctypes.c_int32)]
+
+
+PAGE_DTYPE = np.dtype([("pool_offset", "<i8"), ("object_offset", "<i8"), ("bytes", "<i8"),
+                       ("layer", "<i4"), ("block", "<i4")])
+
+
+class _PageList(ctypes.Structure):
+    _fields_ = [("pages", ctypes.c_void_p), ("capacity", ctypes.c_int64), ("count", ctypes.c_int64)]
+
+
 class _Jobs(ctypes.Structure):
     _fields_ = [("num_object_groups", ctypes.c_int32), ("pad_", ctypes.c_int32),
                 ("jobs", ctypes.POINTER(ctypes.POINTER(_Job))),
@@ -121,6 +134,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("or_store", "or_load"):
         getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_void_p, P(_Tables),
                                        P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
+    lib.or_list_pages.argtypes = [P(_Layout), ctypes.c_int64, P(_Tables), P(_Jobs), ctypes.c_int64,
+                                  P(ctypes.c_uint32), P(_PageList)]
+    lib.or_unified_block_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P(ctypes.c_int64)]
     return lib
 
 
@@ -148,6 +164,15 @@ def negotiate_chunk(requested: int, N: int, strict: bool = False, _lib=None) -> 
     rc = (_lib or lib()).or_negotiate_chunk(int(requested), int(N), int(bool(strict)), ctypes.byref(out))
     if rc != OK:
         raise OracleError(rc, f"negotiate_chunk({requested}, {N}, strict={strict})")
+    return out.value
+
+
+def unified_block_size(attn_token_bytes: int, state_page_bytes: int, align: int = 16, _lib=None) -> int:
+    out = ctypes.c_int64(0)
+    rc = (_lib or lib()).or_unified_block_size(int(attn_token_bytes), int(state_page_bytes), int(align),
+                                               ctypes.byref(out))
+    if rc != OK:
+        raise OracleError(rc, "unified_block_size")
     return out.value
 
 
@@ -294,3 +319,24 @@ def load(L: Layout, C: int, pool: np.ndarray, tables, jobs, arena: np.ndarray) -
     if rc != OK:
         raise OracleError(rc, "load")
     return st.value
+
+
+def list_pages(L: Layout, C: int, tables, jobs, arena_bytes: int):
+    """The pages a store/load of `jobs` touches, as a PAGE_DTYPE array
+    (pool offset, arena offset, bytes, layer, block), plus the status bits."""
+    T, J, keep = _marshal(L, tables, jobs)
+    st = ctypes.c_uint32(0)
+    pl = _PageList(None, 0, 0)
+    rc = L._lib.or_list_pages(ctypes.byref(L._c), int(C), ctypes.byref(T), ctypes.byref(J), int(arena_bytes),
+                              ctypes.byref(st), ctypes.byref(pl))
+    if rc != OK:
+        raise OracleError(rc, "list_pages")
+    out = np.zeros(pl.count, dtype=PAGE_DTYPE)
+    pl = _PageList(out.ctypes.data, out.size, 0)
+    st = ctypes.c_uint32(0)
+    rc = L._lib.or_list_pages(ctypes.byref(L._c), int(C), ctypes.byref(T), ctypes.byref(J), int(arena_bytes),
+                              ctypes.byref(st), ctypes.byref(pl))
+    if rc != OK:
+        raise OracleError(rc, "list_pages")
+    assert pl.count == out.size
+    return out, st.value

@@ -319,16 +319,29 @@ int64_t or_object_bytes(const or_layout *L, int64_t C, int og)
 /* Store and load.                                                      */
 /* ------------------------------------------------------------------ */
 
-/* One page copy between the pool and an object, in either direction.
- * Returns the status bits raised (0 when the copy was done). */
+/* One page copy between the pool and an object, in either direction, or,
+ * when `list` is given, a record of the page instead of the copy.
+ * Returns the status bits raised (0 when the page was valid). */
 static uint32_t copy_page(const or_layout *L, int layer, int64_t block,
                           uint8_t *pool, uint8_t *obj_bytes, int to_object,
-                          uint32_t missing_bit)
+                          uint32_t missing_bit, or_page_list *list, int64_t obj_offset)
 {
     if (block == -1)
         return missing_bit;
     if (block < 0 || block >= L->num_blocks)
         return OR_ST_BLOCK_OOR;
+    if (list != NULL) {
+        if (list->count < list->capacity) {
+            or_page *pg = &list->pages[list->count];
+            pg->pool_offset = L->base[layer] + block * L->stride[layer];
+            pg->object_offset = obj_offset;
+            pg->bytes = L->real_bytes[layer];
+            pg->layer = layer;
+            pg->block = (int32_t)block;
+        }
+        list->count++;
+        return 0;
+    }
     uint8_t *page = pool + L->base[layer] + block * L->stride[layer];
     if (to_object)
         memcpy(obj_bytes, page, (size_t)L->real_bytes[layer]);
@@ -352,9 +365,9 @@ static int check_tables(const or_layout *L, const or_tables *T)
 static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
                         const or_tables *T, const or_jobs *J,
                         uint8_t *arena, int64_t arena_bytes, uint32_t *status,
-                        int to_object)
+                        int to_object, or_page_list *list)
 {
-    if (L == NULL || pool == NULL || J == NULL || status == NULL)
+    if (L == NULL || (pool == NULL && list == NULL) || J == NULL || status == NULL)
         return OR_ERR_INVALID_ARG;
     if (C <= 0 || C % L->N != 0)
         return OR_ERR_NOT_MULTIPLE;
@@ -379,7 +392,7 @@ static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
                 *status |= OR_ST_BAD_JOB;
                 continue;
             }
-            uint8_t *obj = arena + job->offset;
+            uint8_t *obj = arena == NULL ? NULL : arena + job->offset;
             int64_t cursor = 0;
             for (int i = 0; i < L->num_layers; i++) {
                 if (L->object_group[i] != og)
@@ -395,7 +408,8 @@ static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
                         *status |= OR_ST_BAD_JOB;
                     else
                         *status |= copy_page(L, i, row[pos], pool, obj + cursor,
-                                             to_object, OR_ST_NO_SNAPSHOT);
+                                             to_object, OR_ST_NO_SNAPSHOT, list,
+                                             job->offset + cursor);
                     cursor += L->real_bytes[i];
                 } else {
                     /* The chunk's C tokens are its m consecutive blocks. */
@@ -405,7 +419,8 @@ static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
                             *status |= OR_ST_BAD_JOB;
                         else
                             *status |= copy_page(L, i, row[pos], pool, obj + cursor,
-                                                 to_object, OR_ST_NO_BLOCK);
+                                                 to_object, OR_ST_NO_BLOCK, list,
+                                                 job->offset + cursor);
                         cursor += L->real_bytes[i];
                     }
                 }
@@ -421,7 +436,7 @@ int or_store(const or_layout *L, int64_t C, const uint8_t *pool,
 {
     if (arena == NULL)
         return OR_ERR_INVALID_ARG;
-    return move_objects(L, C, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1);
+    return move_objects(L, C, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1, NULL);
 }
 
 int or_load(const or_layout *L, int64_t C, uint8_t *pool,
@@ -430,5 +445,39 @@ int or_load(const or_layout *L, int64_t C, uint8_t *pool,
 {
     if (arena == NULL)
         return OR_ERR_INVALID_ARG;
-    return move_objects(L, C, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0);
+    return move_objects(L, C, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0, NULL);
+}
+
+/* The pages a store or load of the jobs touches, in the order it touches
+ * them, without moving bytes: pool offset, object offset (arena-relative)
+ * and length of each. Used to check large cases one object at a time.
+ * Returns OR_OK and sets list->count to the number of pages (records past
+ * list->capacity are counted but not written). */
+int or_list_pages(const or_layout *L, int64_t C, const or_tables *T, const or_jobs *J,
+                  int64_t arena_bytes, uint32_t *status, or_page_list *list)
+{
+    if (list == NULL || (list->capacity > 0 && list->pages == NULL))
+        return OR_ERR_INVALID_ARG;
+    list->count = 0;
+    return move_objects(L, C, NULL, T, J, NULL, arena_bytes, status, 1, list);
+}
+
+/* Smallest multiple of `align` tokens whose attention page
+ * (N * attn_token_bytes) holds at least state_page_bytes ([HM] Step 1: one
+ * block size for all groups, large enough that the attention page is >= the
+ * state page; [KL] note: 944 at TP 2 and 1888 at TP 1). Found by counting
+ * up, one alignment step at a time. */
+int or_unified_block_size(int64_t attn_token_bytes, int64_t state_page_bytes,
+                          int64_t align, int64_t *out)
+{
+    if (out == NULL || attn_token_bytes <= 0 || state_page_bytes <= 0 || align <= 0)
+        return OR_ERR_INVALID_ARG;
+    int64_t n = align;
+    while (n * attn_token_bytes < state_page_bytes) {
+        if (n > INT64_MAX / attn_token_bytes - align)
+            return OR_ERR_OVERFLOW;
+        n += align;
+    }
+    *out = n;
+    return OR_OK;
 }

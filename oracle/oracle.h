@@ -87,6 +87,20 @@ typedef struct {
     const int64_t *num_jobs;   /* [object group] */
 } or_jobs;
 
+typedef struct {
+    int64_t pool_offset;
+    int64_t object_offset;
+    int64_t bytes;
+    int32_t layer;
+    int32_t block;
+} or_page;
+
+typedef struct {
+    or_page *pages;
+    int64_t capacity;
+    int64_t count;
+} or_page_list;
+
 int or_negotiate_chunk(int64_t requested, int64_t N, int strict, int64_t *out);
 int or_check_step_budget(int64_t N, int64_t max_batched, int separate_object_groups);
 int or_layout_build(or_layout *L);
@@ -97,5 +111,10 @@ int or_store(const or_layout *L, int64_t C, const uint8_t *pool,
 int or_load(const or_layout *L, int64_t C, uint8_t *pool,
             const or_tables *T, const or_jobs *J,
             const uint8_t *arena, int64_t arena_bytes, uint32_t *status);
+
+int or_list_pages(const or_layout *L, int64_t C, const or_tables *T, const or_jobs *J,
+                  int64_t arena_bytes, uint32_t *status, or_page_list *list);
+int or_unified_block_size(int64_t attn_token_bytes, int64_t state_page_bytes,
+                          int64_t align, int64_t *out);
 
 #endif

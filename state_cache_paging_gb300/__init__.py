@@ -1,0 +1,284 @@
+"""state_cache_paging_gb300 -- paging a hybrid KDA + MLA model's cache between
+a vLLM-style paged GPU pool and LMCache-style per-chunk objects on GB300.
+
+A thin ctypes binding over ``liblmc.so`` (C ABI in ``include/lmc.h``). The
+Python functions carry the C names and only marshal arguments: the layout,
+negotiation and budget rules run in the library's host code, and every byte
+of a store or load is moved by the library's sm_103a kernels. PyTorch is used
+for device memory and streams only.
+
+Importing this package raises ImportError when ``liblmc.so`` has not been
+built (``python state_cache_paging_gb300/build.py``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblmc.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"liblmc.so is not built at {LIB_PATH}: run `python state_cache_paging_gb300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+LMC_OK = 0
+LMC_ERR_INVALID_ARG = -1
+LMC_ERR_ALIGN = -2
+LMC_ERR_NOT_MULTIPLE = -3
+LMC_ERR_NO_MEMORY = -4
+LMC_ERR_CUDA = -5
+LMC_ERR_OVERFLOW = -6
+LMC_ERR_BUDGET = -7
+
+LMC_ST_BLOCK_OOR = 0x1
+LMC_ST_NO_BLOCK = 0x2
+LMC_ST_NO_SNAPSHOT = 0x4
+LMC_ST_BAD_JOB = 0x8
+
+LMC_LAYER = {"MLA": 0, "KDA": 1, "SWA": 2}
+LMC_LAYER_NAME = {v: k for k, v in LMC_LAYER.items()}
+LMC_MAX_LAYERS = 256
+
+# An lmc_job record: request int32, chunk int32, arena offset int64.
+JOB_DTYPE = np.dtype([("request", "<i4"), ("chunk", "<i4"), ("offset", "<i8")])
+
+
+class LmcError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {lmc_strerror(code)}")
+        self.code = code
+
+
+class lmc_layer_spec(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32), ("token_bytes", ctypes.c_int64),
+                ("conv_bytes", ctypes.c_int64), ("rec_bytes", ctypes.c_int64)]
+
+
+class lmc_layout_params(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("mode", ctypes.c_int32), ("grouping", ctypes.c_int32),
+                ("separate_object_groups", ctypes.c_int32), ("block_size", ctypes.c_int64),
+                ("mem_bytes", ctypes.c_int64), ("layers", ctypes.POINTER(lmc_layer_spec))]
+
+
+class lmc_layer_desc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("kv_group", ctypes.c_int32), ("slot", ctypes.c_int32),
+                ("object_group", ctypes.c_int32), ("real_bytes", ctypes.c_int64),
+                ("page_bytes", ctypes.c_int64), ("base", ctypes.c_int64), ("stride", ctypes.c_int64)]
+
+
+class lmc_layout_info(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_kv_groups", ctypes.c_int32),
+                ("num_object_groups", ctypes.c_int32), ("num_slabs", ctypes.c_int32),
+                ("block_size", ctypes.c_int64), ("page_size", ctypes.c_int64),
+                ("block_stride", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
+                ("pool_bytes", ctypes.c_int64), ("layers", ctypes.POINTER(lmc_layer_desc)),
+                ("kv_group_kind", ctypes.POINTER(ctypes.c_int32)),
+                ("kv_group_size", ctypes.POINTER(ctypes.c_int32)),
+                ("object_group_kind", ctypes.POINTER(ctypes.c_int32))]
+
+
+class lmc_block_table(ctypes.Structure):
+    _fields_ = [("table", ctypes.c_void_p), ("row_stride", ctypes.c_int64), ("num_cols", ctypes.c_int64)]
+
+
+class lmc_batch(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int32), ("num_kv_groups", ctypes.c_int32),
+                ("tables", ctypes.POINTER(lmc_block_table)), ("num_object_groups", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("jobs", ctypes.POINTER(ctypes.c_void_p)),
+                ("num_jobs", ctypes.POINTER(ctypes.c_int64))]
+
+
+_P = ctypes.POINTER
+_i64 = ctypes.c_int64
+_lib.lmc_layout_build.argtypes = [_P(lmc_layout_params), _P(ctypes.c_void_p)]
+_lib.lmc_layout_query.argtypes = [ctypes.c_void_p, _P(lmc_layout_info)]
+_lib.lmc_layout_free.argtypes = [ctypes.c_void_p]
+_lib.lmc_layout_free.restype = None
+_lib.lmc_object_bytes.argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, _P(_i64)]
+_lib.lmc_negotiate_chunk.argtypes = [_i64, _i64, ctypes.c_int, _P(_i64)]
+_lib.lmc_check_step_budget.argtypes = [_i64, _i64, ctypes.c_int]
+_lib.lmc_unified_block_size.argtypes = [_i64, _i64, _i64, _P(_i64)]
+for _name in ("lmc_store", "lmc_load"):
+    getattr(_lib, _name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
+                                     _i64, ctypes.c_void_p, ctypes.c_void_p]
+_lib.lmc_strerror.argtypes = [ctypes.c_int]
+_lib.lmc_strerror.restype = ctypes.c_char_p
+
+
+def lmc_strerror(code: int) -> str:
+    return _lib.lmc_strerror(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != LMC_OK:
+        raise LmcError(rc, what)
+
+
+# ----------------------------------------------------------------------------
+# Host rules
+# ----------------------------------------------------------------------------
+
+def lmc_negotiate_chunk(requested: int, block_size: int, strict: bool = False) -> int:
+    out = _i64(0)
+    _check(_lib.lmc_negotiate_chunk(int(requested), int(block_size), int(bool(strict)), ctypes.byref(out)),
+           f"lmc_negotiate_chunk({requested}, {block_size}, strict={strict})")
+    return out.value
+
+
+def lmc_check_step_budget(block_size: int, max_batched: int, separate_object_groups: bool) -> int:
+    """Returns the library's code (LMC_OK when the budget is allowed)."""
+    return _lib.lmc_check_step_budget(int(block_size), int(max_batched), int(bool(separate_object_groups)))
+
+
+def lmc_unified_block_size(attn_token_bytes: int, state_page_bytes: int, align: int = 16) -> int:
+    out = _i64(0)
+    _check(_lib.lmc_unified_block_size(int(attn_token_bytes), int(state_page_bytes), int(align), ctypes.byref(out)),
+           "lmc_unified_block_size")
+    return out.value
+
+
+# ----------------------------------------------------------------------------
+# Layout
+# ----------------------------------------------------------------------------
+
+class Layout:
+    """An immutable pool layout built by ``lmc_layout_build`` (freed on GC)."""
+
+    def __init__(self, handle: int):
+        self._h = ctypes.c_void_p(handle)
+        info = lmc_layout_info()
+        _check(_lib.lmc_layout_query(self._h, ctypes.byref(info)), "lmc_layout_query")
+        n, g, o = info.num_layers, info.num_kv_groups, info.num_object_groups
+        self.num_layers = n
+        self.num_kv_groups = g
+        self.num_object_groups = o
+        self.num_slabs = info.num_slabs
+        self.block_size = self.N = info.block_size
+        self.page_size = info.page_size
+        self.block_stride = info.block_stride
+        self.num_blocks = info.num_blocks
+        self.pool_bytes = info.pool_bytes
+        d = [info.layers[i] for i in range(n)]
+        self.kinds = [LMC_LAYER_NAME[x.kind] for x in d]
+        self.kv_group = [x.kv_group for x in d]
+        self.slot = [x.slot for x in d]
+        self.object_group = [x.object_group for x in d]
+        self.real_bytes = [x.real_bytes for x in d]
+        self.page_bytes = [x.page_bytes for x in d]
+        self.base = [x.base for x in d]
+        self.stride = [x.stride for x in d]
+        self.kv_group_kind = [LMC_LAYER_NAME[info.kv_group_kind[k]] for k in range(g)]
+        self.kv_group_size = [info.kv_group_size[k] for k in range(g)]
+        self.object_group_kind = [LMC_LAYER_NAME[info.object_group_kind[k]] for k in range(o)]
+
+    @property
+    def handle(self):
+        return self._h
+
+    def object_bytes(self, chunk: int, object_group: int) -> int:
+        return lmc_object_bytes(self, chunk, object_group)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            _lib.lmc_layout_free(h)
+            self._h = None
+
+
+def lmc_layout_build(layers, block_size: int, packed: bool, mem_bytes: int, split_groups: bool = True,
+                     separate_object_groups: bool = True) -> Layout:
+    """`layers`: model-order list of dicts {"kind", "token_bytes", "conv_bytes", "rec_bytes", "window"}."""
+    n = len(layers)
+    arr = (lmc_layer_spec * max(n, 1))()
+    for i, l in enumerate(layers):
+        arr[i] = lmc_layer_spec(LMC_LAYER[l["kind"]], int(l.get("window", 0)), int(l.get("token_bytes", 0)),
+                                int(l.get("conv_bytes", 0)), int(l.get("rec_bytes", 0)))
+    p = lmc_layout_params(n, 1 if packed else 0, 0 if split_groups else 1, int(bool(separate_object_groups)),
+                          int(block_size), int(mem_bytes), arr)
+    h = ctypes.c_void_p()
+    _check(_lib.lmc_layout_build(ctypes.byref(p), ctypes.byref(h)), "lmc_layout_build")
+    return Layout(h.value)
+
+
+def lmc_object_bytes(layout: Layout, chunk: int, object_group: int) -> int:
+    out = _i64(0)
+    _check(_lib.lmc_object_bytes(layout.handle, int(chunk), int(object_group), ctypes.byref(out)),
+           "lmc_object_bytes")
+    return out.value
+
+
+# ----------------------------------------------------------------------------
+# Store / load
+# ----------------------------------------------------------------------------
+
+def jobs_to_device(jobs: np.ndarray, device):
+    """Uploads a JOB_DTYPE numpy array as a uint8 device tensor of 16-byte records."""
+    import torch
+    a = np.ascontiguousarray(jobs, dtype=JOB_DTYPE)
+    return torch.from_numpy(a.view(np.uint8).copy()).to(device)
+
+
+def _batch(layout: Layout, tables, jobs):
+    g = layout.num_kv_groups
+    if len(tables) != g:
+        raise LmcError(LMC_ERR_INVALID_ARG, f"{g} block tables expected, got {len(tables)}")
+    nreq = int(tables[0].shape[0]) if g else 0
+    tarr = (lmc_block_table * max(g, 1))()
+    for k, t in enumerate(tables):
+        if t.dim() != 2 or t.element_size() != 4 or t.stride(1) != 1 or int(t.shape[0]) != nreq:
+            raise LmcError(LMC_ERR_INVALID_ARG, "block tables must be int32 [num_requests, cols] with unit column stride")
+        tarr[k] = lmc_block_table(t.data_ptr(), int(t.stride(0)), int(t.shape[1]))
+    o = layout.num_object_groups
+    if len(jobs) != o:
+        raise LmcError(LMC_ERR_INVALID_ARG, f"{o} job arrays expected, got {len(jobs)}")
+    jarr = (ctypes.c_void_p * max(o, 1))()
+    narr = (_i64 * max(o, 1))()
+    for q, j in enumerate(jobs):
+        nbytes = j.numel() * j.element_size()
+        if nbytes % 16 or not j.is_contiguous():
+            raise LmcError(LMC_ERR_INVALID_ARG, "job arrays hold contiguous 16-byte lmc_job records")
+        jarr[q] = j.data_ptr() if nbytes else None
+        narr[q] = nbytes // 16
+    b = lmc_batch(nreq, g, tarr, o, 0, jarr, narr)
+    return b, (tarr, jarr, narr)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_pool(layout: Layout, pool):
+    if pool.numel() * pool.element_size() < layout.pool_bytes:
+        raise LmcError(LMC_ERR_INVALID_ARG, f"pool holds {pool.numel() * pool.element_size()} bytes, "
+                                            f"the layout addresses {layout.pool_bytes}")
+
+
+def lmc_store(layout: Layout, chunk: int, pool, tables, jobs, arena, status, stream=None) -> None:
+    """Gathers the jobs' objects from `pool` into `arena` (device tensors) on
+    `stream` (default: torch's current stream). Device errors are OR-ed into
+    the 4-byte `status` tensor."""
+    _check_pool(layout, pool)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_store(layout.handle, int(chunk), pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
+                          arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+           "lmc_store")
+
+
+def lmc_load(layout: Layout, chunk: int, pool, tables, jobs, arena, status, stream=None) -> None:
+    """Scatters the jobs' objects from `arena` into `pool` (device tensors)."""
+    _check_pool(layout, pool)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_load(layout.handle, int(chunk), pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
+                         arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+           "lmc_load")
+
+
+__all__ = [n for n in dir() if n.startswith(("lmc_", "LMC_"))] + ["Layout", "LmcError", "JOB_DTYPE",
+                                                                  "jobs_to_device"]

@@ -1,0 +1,81 @@
+"""Builds liblmc.so in-tree for sm_103a (nvcc + g++, no cmake).
+
+Usage: ``python state_cache_paging_gb300/build.py [--force] [-v]`` (run by
+path: importing the package itself requires the built library). The two translation units
+compile in parallel; the CUDA runtime is linked statically, so the library
+loads without torch and shares the primary context with whatever else runs
+in the process.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(PKG, "_build")
+LIB_PATH = os.path.join(PKG, "liblmc.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC = os.environ.get("NVCC", "nvcc")
+CXX = os.environ.get("CXX", "g++")
+
+
+def _sources():
+    out = []
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cpp", ".h")):
+            out.append(os.path.join(CSRC, name))
+    out.append(os.path.join(INCLUDE, "lmc.h"))
+    return out
+
+
+def _stale(target: str) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(s) > t for s in _sources())
+
+
+def build_library(force: bool = False, extra_nvcc=(), out_path: str | None = None, verbose: bool = False) -> str:
+    """Compiles and links liblmc.so; returns its path. `extra_nvcc` adds flags
+    (e.g. -D tuning constants) to the CUDA translation unit."""
+    out = out_path or LIB_PATH
+    if not force and not extra_nvcc and out_path is None and not _stale(out):
+        return out
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tag = f"{os.getpid()}"
+    cu_obj = os.path.join(BUILD_DIR, f"paging.{tag}.o")
+    cpp_obj = os.path.join(BUILD_DIR, f"layout.{tag}.o")
+    ptxas_log = os.path.join(BUILD_DIR, "ptxas.log")
+    cmds = [
+        [NVCC, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
+         "-I", INCLUDE, "-I", CSRC, *extra_nvcc, "-c", os.path.join(CSRC, "paging.cu"), "-o", cu_obj],
+        [CXX, "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE, "-I", CSRC,
+         "-c", os.path.join(CSRC, "layout.cpp"), "-o", cpp_obj],
+    ]
+    procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True) for c in cmds]
+    logs = [p.communicate()[0] for p in procs]
+    for c, p, log in zip(cmds, procs, logs):
+        if p.returncode != 0:
+            raise RuntimeError(f"compile failed: {' '.join(c)}\n{log}")
+    with open(ptxas_log, "w") as f:
+        f.write(logs[0])
+    if verbose:
+        print(logs[0])
+    tmp = out + f".tmp{tag}"
+    link = [NVCC, "-shared", *ARCH, "-o", tmp, cu_obj, cpp_obj]
+    r = subprocess.run(link, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout}{r.stderr}")
+    os.replace(tmp, out)
+    for o in (cu_obj, cpp_obj):
+        os.remove(o)
+    return out
+
+
+if __name__ == "__main__":
+    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))

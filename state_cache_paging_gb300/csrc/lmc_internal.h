@@ -1,0 +1,33 @@
+// lmc_internal.h -- the layout object shared by the host builder and the
+// store/load launchers inside liblmc (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "lmc.h"
+
+struct lmc_layout {
+    int64_t block_size = 0;
+    int32_t mode = LMC_LAYOUT_PADDED;
+    int32_t num_slabs = 0;
+    int64_t page_size = 0;
+    int64_t block_stride = 0;
+    int64_t num_blocks = 0;
+    int64_t pool_bytes = 0;
+    std::vector<lmc_layer_spec> specs;      // model order
+    std::vector<lmc_layer_desc> desc;       // model order
+    std::vector<int32_t> kv_group_kind;
+    std::vector<int32_t> kv_group_size;
+    std::vector<int32_t> object_group_kind;
+    // layers of each object group, in model order
+    std::vector<std::vector<int32_t>> object_group_layers;
+};
+
+namespace lmc {
+
+// Checked 64-bit arithmetic (false on overflow).
+inline bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
+inline bool add_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_add_overflow(a, b, out); }
+
+}  // namespace lmc

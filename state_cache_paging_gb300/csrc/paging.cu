@@ -1,0 +1,347 @@
+// paging.cu -- store (gather pages -> chunk objects) and load (scatter chunk
+// objects -> pages) for sm_103a.
+//
+// What is moved ("Hybrid Attention Models" (LMCache docs), Object-group
+// separation; "Kimi-Linear" (LMCache recipe), Why these settings; "How vLLM
+// manages the KV cache of hybrid models", §3.1/§3.2/§4): one object per
+// (request, chunk, object group); inside it, the group's layers in model
+// order; a paged attention layer contributes the chunk's m = C / N blocks,
+// token-major, a KDA layer the state snapshot stored at the chunk's last
+// block position. The cached pages are byte-opaque, so this is pure data
+// movement: every byte is read once from HBM and written once.
+//
+// GPU design. The work of one launch is a flat list of equal-sized tiles
+// (each at most kTileBytes, 16-byte multiples, never crossing a page). Tile
+// t resolves to (object group, job, layer, page, piece) with integer math on
+// the launch plan held in kernel parameter space, reads one block id from
+// the caller's block table, and copies one contiguous range: 16-byte
+// vector loads that bypass L1 and streaming (evict-first) stores, several in
+// flight per thread. One CTA per tile, many CTAs resident per SM, so the
+// dependent block-table read of one CTA hides under the copies of others.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "lmc_internal.h"
+
+#ifndef LMC_TILE_BYTES
+#define LMC_TILE_BYTES 65536
+#endif
+#ifndef LMC_THREADS
+#define LMC_THREADS 256
+#endif
+#ifndef LMC_UNROLL
+#define LMC_UNROLL 4
+#endif
+
+namespace {
+
+constexpr int kMaxEntries = LMC_MAX_LAYERS;  // layers in one launch
+constexpr int kMaxGroups = 16;               // object groups in one launch
+constexpr int kMaxKv = 64;                   // KV groups (block tables)
+constexpr int kTileBytes = LMC_TILE_BYTES;
+constexpr int kThreads = LMC_THREADS;
+constexpr int kUnroll = LMC_UNROLL;
+
+// One layer's run of pages inside an object of one group.
+struct Entry {
+    int64_t pool_base;    // pool byte offset of block 0's page
+    int64_t pool_stride;  // bytes between consecutive blocks' pages
+    int64_t obj_off;      // byte offset of the layer's first page in the object
+    int32_t seg_bytes;    // real bytes of one page
+    int32_t tile_bytes;   // bytes per tile of this page (last tile shorter)
+    int32_t tiles_per_seg;
+    int32_t tile_start;   // tiles of earlier layers in the object
+    int32_t pos_add;      // block position = chunk * m + pos_add + page index
+    int16_t kv;           // KV group (block table)
+    uint8_t kda;          // 1: a single snapshot page
+    uint8_t pad;
+};
+
+struct Group {
+    const lmc_job *jobs;
+    int64_t num_jobs;
+    int64_t tile_begin;  // first launch-wide tile of this group
+    int64_t obj_bytes;
+    int32_t tiles_per_obj;
+    int32_t first_entry;
+    int32_t num_entries;
+    int32_t pad;
+};
+
+struct Table {
+    const int32_t *ptr;
+    int64_t row_stride;
+    int64_t num_cols;
+};
+
+struct Plan {
+    const uint8_t *src_base;  // store: pool; load: arena
+    uint8_t *dst_base;        // store: arena; load: pool
+    uint32_t *status;
+    int64_t arena_bytes;
+    int64_t num_blocks;
+    int64_t total_tiles;
+    int32_t m;
+    int32_t num_requests;
+    int32_t num_groups;
+    int32_t store;  // 1: pool -> arena
+    Group groups[kMaxGroups];
+    Table tables[kMaxKv];
+    Entry entries[kMaxEntries];
+};
+static_assert(sizeof(Plan) <= 32000, "kernel parameter space");
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// A resolved tile: copy `bytes` from src to dst.
+struct Span {
+    const uint8_t *src;
+    uint8_t *dst;
+    int32_t bytes;
+};
+
+// Resolves tile -> span; returns the status bits to raise (0: copy it).
+__device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s) {
+    int g = 0;
+    while (g + 1 < P.num_groups && tile >= P.groups[g + 1].tile_begin)
+        g++;
+    const Group &G = P.groups[g];
+    const int64_t local = tile - G.tile_begin;
+    const int64_t q = local / G.tiles_per_obj;  // job index
+    const int32_t t = (int32_t)(local - q * G.tiles_per_obj);
+
+    // layer entry: the last one whose first tile is <= t
+    int lo = G.first_entry, hi = G.first_entry + G.num_entries - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.entries[mid].tile_start <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const Entry &E = P.entries[lo];
+    const int32_t u = t - E.tile_start;
+    const int32_t j = u / E.tiles_per_seg;  // page index within the layer
+    const int32_t k = u - j * E.tiles_per_seg;
+
+    const lmc_job job = G.jobs[q];
+    if (job.request < 0 || job.request >= P.num_requests || job.chunk < 0 || job.offset < 0 ||
+        (job.offset & 15) != 0 || job.offset > P.arena_bytes - G.obj_bytes)
+        return LMC_ST_BAD_JOB;
+    const Table &T = P.tables[E.kv];
+    const int64_t pos = (int64_t)job.chunk * P.m + E.pos_add + j;
+    if (pos >= T.num_cols)
+        return LMC_ST_BAD_JOB;
+    const int32_t block = __ldg(T.ptr + (int64_t)job.request * T.row_stride + pos);
+    if (block == -1)
+        return E.kda ? LMC_ST_NO_SNAPSHOT : LMC_ST_NO_BLOCK;
+    if (block < 0 || block >= P.num_blocks)
+        return LMC_ST_BLOCK_OOR;
+
+    const int64_t piece = (int64_t)k * E.tile_bytes;
+    const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + piece;
+    const int64_t obj = job.offset + E.obj_off + (int64_t)j * E.seg_bytes + piece;
+    s.bytes = min(E.tile_bytes, (int32_t)(E.seg_bytes - piece));
+    s.src = P.src_base + (P.store ? page : obj);
+    s.dst = P.dst_base + (P.store ? obj : page);
+    return 0;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) page_copy_kernel(const __grid_constant__ Plan P) {
+    for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
+        Span s;
+        const uint32_t bad = resolve(P, tile, s);
+        if (bad) {
+            if (threadIdx.x == 0)
+                atomicOr(P.status, bad);
+            continue;
+        }
+        if (kVec) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(s.src);
+            uint4 *dst = reinterpret_cast<uint4 *>(s.dst);
+            const int n = s.bytes >> 4;
+            int i = threadIdx.x;
+            for (; i + (kUnroll - 1) * kThreads < n; i += kUnroll * kThreads) {
+                uint4 v[kUnroll];
+#pragma unroll
+                for (int w = 0; w < kUnroll; w++)
+                    v[w] = ld_stream(src + i + w * kThreads);
+#pragma unroll
+                for (int w = 0; w < kUnroll; w++)
+                    st_stream(dst + i + w * kThreads, v[w]);
+            }
+            for (; i < n; i += kThreads)
+                st_stream(dst + i, ld_stream(src + i));
+        } else {
+            for (int i = threadIdx.x; i < s.bytes; i += kThreads)
+                s.dst[i] = s.src[i];
+        }
+    }
+}
+
+int sm_count() {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev)
+        cache.resize(dev + 1, 0);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool aligned16(int64_t x) { return (x & 15) == 0; }
+
+// Host-side validation and launch plan; shared by store and load.
+int build_plan(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_batch *b,
+               const void *arena, int64_t arena_bytes, uint32_t *status, bool store, Plan &P,
+               bool &vec) {
+    if (L == nullptr || b == nullptr || status == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    if (chunk <= 0 || chunk % L->block_size != 0)
+        return LMC_ERR_NOT_MULTIPLE;
+    if (((uintptr_t)status & 3) != 0)
+        return LMC_ERR_ALIGN;
+    const int64_t m64 = chunk / L->block_size;
+    if (m64 > INT32_MAX)
+        return LMC_ERR_OVERFLOW;
+    const int nkv = (int)L->kv_group_kind.size();
+    const int nog = (int)L->object_group_layers.size();
+    if (b->num_requests < 0 || b->num_kv_groups != nkv || b->num_object_groups != nog ||
+        arena_bytes < 0 || (nkv > 0 && b->tables == nullptr) || b->num_jobs == nullptr ||
+        b->jobs == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    if (nkv > kMaxKv || nog > kMaxGroups)
+        return LMC_ERR_INVALID_ARG;
+
+    std::memset(&P, 0, sizeof(P));
+    P.m = (int32_t)m64;
+    P.num_requests = b->num_requests;
+    P.num_blocks = L->num_blocks;
+    P.arena_bytes = arena_bytes;
+    P.status = status;
+    P.store = store ? 1 : 0;
+    for (int k = 0; k < nkv; k++) {
+        const lmc_block_table &t = b->tables[k];
+        if (t.num_cols < 0 || t.row_stride < t.num_cols ||
+            (b->num_requests > 0 && t.num_cols > 0 && t.table == nullptr))
+            return LMC_ERR_INVALID_ARG;
+        P.tables[k] = Table{t.table, t.row_stride, t.num_cols};
+    }
+
+    vec = aligned16((int64_t)(uintptr_t)pool) && aligned16((int64_t)(uintptr_t)arena);
+    int64_t total = 0;
+    int ne = 0;
+    for (int og = 0; og < nog; og++) {
+        const int64_t nj = b->num_jobs[og];
+        if (nj < 0 || (nj > 0 && b->jobs[og] == nullptr))
+            return LMC_ERR_INVALID_ARG;
+        if (nj == 0)
+            continue;
+        Group &G = P.groups[P.num_groups];
+        G.jobs = b->jobs[og];
+        G.num_jobs = nj;
+        G.first_entry = ne;
+        int64_t obj = 0, tiles = 0;
+        for (int32_t i : L->object_group_layers[og]) {
+            const lmc_layer_desc &d = L->desc[i];
+            if (d.real_bytes > INT32_MAX - kTileBytes)
+                return LMC_ERR_INVALID_ARG;  // one page must stay below 2 GiB
+            const int32_t seg = (int32_t)d.real_bytes;
+            const int32_t pieces = (seg + kTileBytes - 1) / kTileBytes;
+            int32_t tb = (seg + pieces - 1) / pieces;
+            tb = (tb + 15) & ~15;  // 16-byte pieces; the last one is shorter
+            Entry &E = P.entries[ne++];
+            E.pool_base = d.base;
+            E.pool_stride = d.stride;
+            E.obj_off = obj;
+            E.seg_bytes = seg;
+            E.tile_bytes = tb;
+            E.tiles_per_seg = (seg + tb - 1) / tb;
+            E.tile_start = (int32_t)tiles;
+            E.kda = d.kind == LMC_LAYER_KDA;
+            E.pos_add = E.kda ? P.m - 1 : 0;
+            E.kv = (int16_t)d.kv_group;
+            const int64_t pages = E.kda ? 1 : m64;
+            obj += pages * seg;
+            tiles += pages * E.tiles_per_seg;
+            if (tiles > INT32_MAX)
+                return LMC_ERR_OVERFLOW;
+            vec = vec && aligned16(d.base) && aligned16(d.stride) && aligned16(seg);
+        }
+        G.num_entries = ne - G.first_entry;
+        G.obj_bytes = obj;
+        G.tiles_per_obj = (int32_t)tiles;
+        G.tile_begin = total;
+        int64_t add;
+        if (!lmc::mul_ok(nj, tiles, &add) || !lmc::add_ok(total, add, &total))
+            return LMC_ERR_OVERFLOW;
+        P.num_groups++;
+    }
+    P.total_tiles = total;
+    if (total > 0 && (pool == nullptr || arena == nullptr))
+        return LMC_ERR_INVALID_ARG;
+    P.src_base = static_cast<const uint8_t *>(store ? pool : arena);
+    P.dst_base = static_cast<uint8_t *>(const_cast<void *>(store ? arena : pool));
+    return LMC_OK;
+}
+
+int launch(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_batch *b,
+           const void *arena, int64_t arena_bytes, uint32_t *status, void *stream, bool store) {
+    Plan P;
+    bool vec = false;
+    int rc = build_plan(L, chunk, pool, b, arena, arena_bytes, status, store, P, vec);
+    if (rc != LMC_OK || P.total_tiles == 0)
+        return rc;
+    // One CTA per tile, capped; the kernel strides over the rest.
+    const int sms = sm_count();
+    if (sms <= 0)
+        return LMC_ERR_CUDA;
+    const int64_t cap = (int64_t)sms * 2048;
+    const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, cap);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (vec)
+        page_copy_kernel<true><<<grid, kThreads, 0, s>>>(P);
+    else
+        page_copy_kernel<false><<<grid, kThreads, 0, s>>>(P);
+    return cudaGetLastError() == cudaSuccess ? LMC_OK : LMC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int lmc_store(const lmc_layout *layout, int64_t chunk_size, const void *pool,
+                         const lmc_batch *batch, void *arena, int64_t arena_bytes, uint32_t *status,
+                         void *stream) {
+    return launch(layout, chunk_size, pool, batch, arena, arena_bytes, status, stream, true);
+}
+
+extern "C" int lmc_load(const lmc_layout *layout, int64_t chunk_size, void *pool,
+                        const lmc_batch *batch, const void *arena, int64_t arena_bytes,
+                        uint32_t *status, void *stream) {
+    return launch(layout, chunk_size, pool, batch, arena, arena_bytes, status, stream, false);
+}

@@ -121,6 +121,21 @@ def check_page_formulas(lib):
                 assert mla_page < kda_page
 
 
+def check_unified_block_size(lib):
+    """N = the smallest 16-token multiple whose MLA page covers the KDA state
+    page: 944 at TP 2 and 1888 at TP 1 for Kimi-Linear."""
+    for tp, N in _rows("block_size.txt"):
+        tp, N = int(tp), int(N)
+        state = (12288 // tp) * 3 * 2 + (32 // tp) * 128 * 128 * 4
+        assert oracle.unified_block_size(1152, state, 16, _lib=lib) == N
+    # exhaustive on small sizes: smallest multiple of align covering the state
+    for tb in range(1, 12):
+        for state in range(1, 200):
+            for align in (1, 2, 8, 16):
+                n = oracle.unified_block_size(tb, state, align, _lib=lib)
+                assert n % align == 0 and n * tb >= state and (n - align) * tb < state
+
+
 def check_k3_groups(lib):
     rows = {r[0]: r[1:] for r in _rows("k3_groups.txt")}
     L = oracle.layout(W.CONFIGS[3].layers, 768, False, 1 << 50, _lib=lib)
@@ -314,6 +329,24 @@ def check_store_load(lib, case):
     assert np.array_equal(arena, arena2), "store(load(x)) != x"
     # 4) every object byte came from the source pool: objects are non-trivial
     assert arena.any()
+    # 5) the page list names exactly the pages the store reads: a pool that
+    #    holds only those pages (zeros elsewhere) stores the same objects,
+    #    and the listed pieces tile every object without gaps
+    pages, st = oracle.list_pages(L, C, case["t_src"], jobs, case["arena_bytes"])
+    assert st == 0
+    sparse = np.zeros_like(pool)
+    for pg in pages:
+        lo = int(pg["pool_offset"])
+        sparse[lo:lo + int(pg["bytes"])] = pool[lo:lo + int(pg["bytes"])]
+    arena3 = np.zeros_like(arena)
+    assert oracle.store(L, C, sparse, case["t_src"], jobs, arena3) == 0
+    assert np.array_equal(arena, arena3), "page list misses a page the store reads"
+    covered = np.zeros(arena.size, dtype=np.int64)
+    for pg in pages:
+        o = int(pg["object_offset"])
+        covered[o:o + int(pg["bytes"])] += 1
+    total = sum(case["sizes"][og] * len(J) for og, J in enumerate(jobs))
+    assert int((covered == 1).sum()) == total and covered.max() == 1
 
 
 def L_spec(case):
@@ -366,7 +399,7 @@ def check_errors(lib, case):
 
 
 ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",
-       "check_budget", "check_page_formulas", "check_k3_groups", "check_closed_forms",
+       "check_budget", "check_page_formulas", "check_unified_block_size", "check_k3_groups", "check_closed_forms",
        "check_non_overlap", "check_store_load_cases"]
 
 

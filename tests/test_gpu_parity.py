@@ -1,0 +1,254 @@
+"""GPU parity: liblmc's store and load against the CPU oracle, byte for byte.
+
+Small cases (the tiny workload, random specs, every error path) are compared
+in full. The full-size workloads run in the launch configuration the
+benchmark times and are checked on oracle-recomputed samples plus properties
+that hold at any size (store after load reproduces the objects; pool bytes
+outside the addressed pages stay untouched).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins as P
+import workloads as W
+from gpu_harness import (case_inputs, check_load_sampled, check_store_sampled, check_untouched,
+                         dev_jobs, dev_tables)
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    torch.cuda.empty_cache()
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _full_exact(lmc, inp, Lp, pool_offset=0, arena_offset=0):
+    """Store + load of every job, compared in full with the oracle."""
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, inp.cfg.seed + 17)
+    buf = torch.empty(Lo.pool_bytes + 64, dtype=torch.uint8, device=DEV)
+    pool = buf[pool_offset:pool_offset + Lo.pool_bytes]
+    pool.copy_(torch.from_numpy(pool_h))
+    abuf = torch.full((inp.arena_bytes + 64,), 0x3C, dtype=torch.uint8, device=DEV)
+    arena = abuf[arena_offset:arena_offset + inp.arena_bytes]
+    fbuf = torch.full((Lo.pool_bytes + 64,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    fresh = fbuf[pool_offset:pool_offset + Lo.pool_bytes]
+    st = _status()
+    jobs = dev_jobs(inp.jobs, DEV)
+    lmc.lmc_store(Lp, C, pool, dev_tables(inp.tables_src, DEV), jobs, arena, st)
+    lmc.lmc_load(Lp, C, fresh, dev_tables(inp.tables_dst, DEV), jobs, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    arena_o = np.full(inp.arena_bytes, 0x3C, dtype=np.uint8)
+    assert oracle.store(Lo, C, pool_h, inp.tables_src, inp.jobs, arena_o) == 0
+    fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    assert oracle.load(Lo, C, fresh_o, inp.tables_dst, inp.jobs, arena_o) == 0
+    assert np.array_equal(arena.cpu().numpy(), arena_o)
+    assert np.array_equal(fresh.cpu().numpy(), fresh_o)
+    # guard bytes around the buffers are untouched
+    assert (abuf[:arena_offset] == 0x3C).all() and (abuf[arena_offset + inp.arena_bytes:] == 0x3C).all()
+    assert (fbuf[:pool_offset] == W.SENTINEL).all() and (fbuf[pool_offset + Lo.pool_bytes:] == W.SENTINEL).all()
+
+
+def test_tiny_workload_exact(lmc):
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    _full_exact(lmc, inp, Lp)
+
+
+@pytest.mark.parametrize("pool_offset,arena_offset", [(0, 0), (8, 0), (0, 4), (3, 5)])
+def test_tiny_workload_unaligned_buffers(lmc, pool_offset, arena_offset):
+    """Buffers that are not 16-byte aligned take the byte-wise path."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    _full_exact(lmc, inp, Lp, pool_offset, arena_offset)
+
+
+def _random_cfg(rng, t):
+    spec = P.random_spec(rng, int(rng.integers(2, 9)))
+    spec[0] = W.mla(int(rng.choice([16, 32, 48, 1152])))
+    spec[-1] = W.kda(int(rng.choice([8, 64, 768])), 3, int(rng.choice([1, 2, 4])), int(rng.choice([8, 16, 64])))
+    N = int(rng.choice([2, 4, 16, 64]))
+    lengths = tuple(int(x) for x in rng.integers(N, 40 * N, size=int(rng.integers(1, 6))))
+    return W.Config(100 + t, "random", spec, N=N, requested_chunk=int(rng.integers(0, 5 * N)),
+                    packed=bool(t % 2), num_requests=len(lengths), lengths="fixed",
+                    fixed_lengths=lengths, snapshot=("block" if t % 3 else "chunk"), seed=t)
+
+
+@pytest.mark.parametrize("t", range(24))
+def test_random_specs_exact(lmc, t):
+    rng = np.random.default_rng(1000 + t)
+    cfg = _random_cfg(rng, t)
+    inp, Lp = case_inputs(cfg, split=bool((t // 2) % 2), separate=bool((t // 4) % 2 == 0))
+    _full_exact(lmc, inp, Lp)
+
+
+def test_odd_page_sizes_exact(lmc):
+    """Pages that are not 16-byte multiples (byte-wise path, ragged tiles)."""
+    spec = [W.mla(18), {"kind": "KDA", "token_bytes": 0, "conv_bytes": 6, "rec_bytes": 70001, "window": 0},
+            W.swa(7, 32), W.mla(18)]
+    cfg = W.Config(200, "odd", spec, N=8, requested_chunk=20, packed=True, num_requests=3,
+                   lengths="fixed", fixed_lengths=(50, 97, 33), seed=5)
+    inp, Lp = case_inputs(cfg)
+    _full_exact(lmc, inp, Lp)
+
+
+def test_large_pages_exact(lmc):
+    """Pages far larger than one tile (a 33 MB KDA state, 1.2 MB MLA page)."""
+    spec = [W.kda(3 * 64 * 128, 3, 128, 256), W.mla(1152), W.kda(3 * 64 * 128, 3, 128, 256)]
+    cfg = W.Config(201, "large", spec, N=1024, requested_chunk=2000, packed=False, num_requests=2,
+                   lengths="fixed", fixed_lengths=(4100, 6200), seed=6)
+    inp, Lp = case_inputs(cfg)
+    _full_exact(lmc, inp, Lp)
+
+
+def test_error_paths_match_oracle(lmc):
+    """Bad block ids and bad jobs: same status bits and same arena bytes as
+    the oracle (the offending page or object is skipped)."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 3)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    kda_g = Lo.kv_group_kind.index("KDA")
+    mla_g = Lo.kv_group_kind.index("MLA")
+    m = C // Lo.N
+    cases = []
+    for what in ("oor", "neg", "snap", "mla", "req", "align", "end", "chunk", "negchunk", "negoff", "cols"):
+        tabs = [t.copy() for t in inp.tables_src]
+        jobs = [j.copy() for j in inp.jobs]
+        if what == "oor":
+            tabs[mla_g][1, 2] = Lo.num_blocks
+        elif what == "neg":
+            tabs[mla_g][0, 0] = -9
+        elif what == "snap":
+            tabs[kda_g][1, 2 * m - 1] = -1
+        elif what == "mla":
+            tabs[mla_g][0, 1] = -1
+        elif what == "req":
+            jobs[0][1]["request"] = 2
+        elif what == "align":
+            jobs[1][0]["offset"] += 8
+        elif what == "end":
+            jobs[1][2]["offset"] = inp.arena_bytes - 16
+        elif what == "chunk":
+            jobs[0][0]["chunk"] = 1000
+        elif what == "negchunk":
+            jobs[0][3]["chunk"] = -1
+        elif what == "negoff":
+            jobs[1][3]["offset"] = -16
+        elif what == "cols":
+            tabs = [t[:, :3].copy() for t in tabs]
+        cases.append((what, tabs, jobs))
+    for what, tabs, jobs in cases:
+        arena = torch.full((inp.arena_bytes,), 0x77, dtype=torch.uint8, device=DEV)
+        st = _status()
+        lmc.lmc_store(Lp, C, pool, dev_tables(tabs, DEV), dev_jobs(jobs, DEV), arena, st)
+        torch.cuda.synchronize()
+        arena_o = np.full(inp.arena_bytes, 0x77, dtype=np.uint8)
+        st_o = oracle.store(Lo, C, pool_h, tabs, jobs, arena_o)
+        assert st_o != 0, what
+        assert int(st.item()) == st_o, (what, int(st.item()), st_o)
+        assert np.array_equal(arena.cpu().numpy(), arena_o), what
+        # the same faults on the load side
+        fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+        st = _status()
+        src = torch.from_numpy(arena_o).to(DEV)
+        lmc.lmc_load(Lp, C, fresh, dev_tables(tabs, DEV), dev_jobs(jobs, DEV), src, st)
+        torch.cuda.synchronize()
+        fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        assert oracle.load(Lo, C, fresh_o, tabs, jobs, arena_o) == st_o
+        assert int(st.item()) == st_o, what
+        assert np.array_equal(fresh.cpu().numpy(), fresh_o), what
+
+
+def test_status_bits_accumulate(lmc):
+    """Status bits are OR-ed into the caller's word, never cleared."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    pool = torch.zeros(inp.layout.pool_bytes, dtype=torch.uint8, device=DEV)
+    arena = torch.zeros(inp.arena_bytes, dtype=torch.uint8, device=DEV)
+    st = torch.full((1,), 0x100, dtype=torch.int32, device=DEV)
+    tabs = [t.copy() for t in inp.tables_src]
+    tabs[0][0, 1] = -1
+    lmc.lmc_store(Lp, inp.C, pool, dev_tables(tabs, DEV), dev_jobs(inp.jobs, DEV), arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0x100 | lmc.LMC_ST_NO_SNAPSHOT
+
+
+def test_empty_batch_launches_nothing(lmc):
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    pool = torch.zeros(inp.layout.pool_bytes, dtype=torch.uint8, device=DEV)
+    arena = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    st = _status()
+    empty = [torch.zeros(0, dtype=torch.uint8, device=DEV) for _ in inp.jobs]
+    lmc.lmc_store(Lp, inp.C, pool, dev_tables(inp.tables_src, DEV), empty, arena, st)
+    lmc.lmc_load(Lp, inp.C, pool, dev_tables(inp.tables_src, DEV), empty, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and not pool.any()
+
+
+def test_object_at_arena_end(lmc):
+    """An object that ends exactly at the arena's last byte is moved."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 4)
+    size = inp.object_bytes[1]
+    job = np.array([(1, 3, 0)], dtype=W.JOB_DTYPE)
+    jobs = [np.zeros(0, dtype=W.JOB_DTYPE), job]
+    arena = torch.zeros(size, dtype=torch.uint8, device=DEV)
+    st = _status()
+    lmc.lmc_store(Lp, C, torch.from_numpy(pool_h).to(DEV), dev_tables(inp.tables_src, DEV),
+                  dev_jobs(jobs, DEV), arena, st)
+    torch.cuda.synchronize()
+    arena_o = np.zeros(size, dtype=np.uint8)
+    assert oracle.store(Lo, C, pool_h, inp.tables_src, jobs, arena_o) == 0
+    assert int(st.item()) == 0 and np.array_equal(arena.cpu().numpy(), arena_o)
+
+
+def _full_size(lmc, cfg, request_ids=None, per_group=12):
+    """Full-size store + load in the benchmark's launch configuration."""
+    inp, Lp = case_inputs(cfg, request_ids)
+    Lo, C = inp.layout, inp.C
+    rng = np.random.default_rng(cfg.seed)
+    pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, cfg.seed)
+    arena = torch.empty(inp.arena_bytes, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+    jobs = dev_jobs(inp.jobs, DEV)
+    lmc.lmc_store(Lp, C, pool, t_src, jobs, arena, st)
+    lmc.lmc_load(Lp, C, fresh, t_dst, jobs, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert check_store_sampled(inp, pool, arena, inp.jobs, inp.tables_src, inp.arena_bytes, per_group, rng) > 0
+    assert check_load_sampled(inp, fresh, arena, inp.jobs, inp.tables_dst, inp.arena_bytes, per_group, rng) > 0
+    del pool
+    # store after load under the load's tables reproduces every object
+    arena2 = torch.empty_like(arena)
+    lmc.lmc_store(Lp, C, fresh, t_dst, jobs, arena2, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(arena, arena2)
+    del arena2, arena
+    assert check_untouched(inp, fresh, inp.jobs, inp.tables_dst, inp.arena_bytes, W.SENTINEL)
+
+
+def test_full_size_kimi_linear_padded(lmc):
+    _full_size(lmc, W.CONFIGS[1])
+
+
+def test_full_size_kimi_linear_packed_lognormal(lmc):
+    _full_size(lmc, W.CONFIGS[2])
+
+
+def test_full_size_k3_one_wave(lmc):
+    """K3 (93 layers, N = 768, chunk 1536): one request of 131,072 tokens."""
+    _full_size(lmc, W.CONFIGS[3], request_ids=[2], per_group=6)

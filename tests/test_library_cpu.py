@@ -1,0 +1,141 @@
+"""liblmc on the host (no GPU): exported symbols, layout / negotiation /
+budget parity with the oracle, and the store/load argument checks that run
+before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as P
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "lmc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lmc_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lmc):
+    names = _declared()
+    assert {"lmc_layout_build", "lmc_layout_query", "lmc_layout_free", "lmc_negotiate_chunk",
+            "lmc_store", "lmc_load", "lmc_strerror"} <= set(names)
+    so = ctypes.CDLL(lmc.LIB_PATH)
+    missing = [n for n in names if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def assert_same_layout(p, o):
+    for f in ("num_kv_groups", "num_object_groups", "num_slabs", "page_size", "block_stride",
+              "num_blocks", "pool_bytes", "kv_group", "slot", "object_group", "kv_group_kind",
+              "kv_group_size", "real_bytes", "page_bytes", "base", "stride", "kinds"):
+        assert getattr(p, f) == getattr(o, f), f
+
+
+@pytest.mark.parametrize("cfg_index", sorted(W.CONFIGS))
+@pytest.mark.parametrize("packed", [False, True])
+def test_layout_matches_oracle_on_workloads(lmc, cfg_index, packed):
+    cfg = W.CONFIGS[cfg_index]
+    for mem in (1 << 34, 123_456_789_012):
+        for split in (True, False):
+            for sep in (True, False):
+                p = lmc.lmc_layout_build(cfg.layers, cfg.N, packed, mem, split, sep)
+                o = oracle.layout(cfg.layers, cfg.N, packed, mem, split, sep)
+                assert_same_layout(p, o)
+                for C in (cfg.N, 2 * cfg.N, 7 * cfg.N):
+                    for g in range(o.num_object_groups):
+                        assert p.object_bytes(C, g) == o.object_bytes(C, g)
+                assert p.object_group_kind == [cfg.layers[p.object_group.index(g)]["kind"]
+                                               for g in range(p.num_object_groups)]
+
+
+def test_layout_matches_oracle_random(lmc):
+    rng = np.random.default_rng(3)
+    for t in range(400):
+        spec = P.random_spec(rng, int(rng.integers(1, 40)))
+        N = int(rng.integers(1, 3000))
+        mem = int(rng.integers(0, 1 << 36))
+        packed, split, sep = bool(t & 1), bool(t & 2), bool(t & 4)
+        try:
+            o = oracle.layout(spec, N, packed, mem, split, sep)
+        except oracle.OracleError as e:
+            with pytest.raises(lmc.LmcError) as ei:
+                lmc.lmc_layout_build(spec, N, packed, mem, split, sep)
+            assert ei.value.code == e.code
+            continue
+        assert_same_layout(lmc.lmc_layout_build(spec, N, packed, mem, split, sep), o)
+
+
+def test_layout_rejects_bad_specs_like_oracle(lmc):
+    bad = [
+        ([W.mla(0)], 16), ([W.swa(16, 0)], 16), ([{"kind": "KDA", "conv_bytes": 0, "rec_bytes": 0}], 16),
+        ([{"kind": "KDA", "conv_bytes": -16, "rec_bytes": 32}], 16), ([W.mla(1 << 40)], 1 << 30),
+        ([W.mla(16)], 0), ([W.mla(16)], -4),
+    ]
+    for spec, N in bad:
+        with pytest.raises(oracle.OracleError) as eo:
+            oracle.layout(spec, N, False, 1 << 30)
+        with pytest.raises(lmc.LmcError) as ep:
+            lmc.lmc_layout_build(spec, N, False, 1 << 30)
+        assert eo.value.code == ep.value.code, spec
+    with pytest.raises(lmc.LmcError) as ep:
+        lmc.lmc_layout_build([W.mla(16)] * 257, 16, False, 1 << 30)
+    assert ep.value.code == lmc.LMC_ERR_INVALID_ARG
+
+
+def test_negotiation_and_budget_match_oracle(lmc):
+    for N in list(range(1, 50)) + [768, 944, 1888, 12288]:
+        for req in list(range(-2, 200)) + [1500, 12287, 12288, 12289, 2**62]:
+            for strict in (False, True):
+                try:
+                    o = oracle.negotiate_chunk(req, N, strict)
+                except oracle.OracleError as e:
+                    with pytest.raises(lmc.LmcError) as ep:
+                        lmc.lmc_negotiate_chunk(req, N, strict)
+                    assert ep.value.code == e.code
+                    continue
+                assert lmc.lmc_negotiate_chunk(req, N, strict) == o
+    for N in range(-1, 40):
+        for B in range(-1, 120):
+            for sep in (False, True):
+                assert lmc.lmc_check_step_budget(N, B, sep) == oracle.check_step_budget(N, B, sep)
+    for tb in (1, 7, 576, 1152):
+        for state in (1, 100, 70_144, 1_085_440, 2_170_880, 4_341_760):
+            for align in (1, 8, 16, 64):
+                assert lmc.lmc_unified_block_size(tb, state, align) == oracle.unified_block_size(tb, state, align)
+    assert lmc.lmc_strerror(lmc.LMC_ERR_NOT_MULTIPLE).startswith("LMC_ERR_NOT_MULTIPLE")
+
+
+def _raw_call(lmc, fn, L, chunk, nkv=None, nog=None, status_off=0, njobs=0, null_jobs=False):
+    """Calls lmc_store/lmc_load through ctypes with dummy host pointers: every
+    case here fails (or finishes with nothing to do) before any CUDA call."""
+    nkv = L.num_kv_groups if nkv is None else nkv
+    nog = L.num_object_groups if nog is None else nog
+    buf = (ctypes.c_uint8 * 64)()
+    addr = ctypes.addressof(buf)
+    tables = (lmc.lmc_block_table * max(nkv, 1))(*[lmc.lmc_block_table(addr, 4, 4) for _ in range(nkv)])
+    jobs = (ctypes.c_void_p * max(nog, 1))(*[None if null_jobs else addr for _ in range(nog)])
+    counts = (ctypes.c_int64 * max(nog, 1))(*[njobs] * nog)
+    b = lmc.lmc_batch(2, nkv, tables, nog, 0, jobs, counts)
+    return getattr(lmc._lib, fn)(L.handle, chunk, addr, ctypes.byref(b), addr, 64, addr + status_off, None)
+
+
+@pytest.mark.parametrize("fn", ["lmc_store", "lmc_load"])
+def test_store_load_host_checks(lmc, fn):
+    cfg = W.CONFIGS[1]
+    L = lmc.lmc_layout_build(cfg.layers, cfg.N, False, 1 << 34)
+    assert _raw_call(lmc, fn, L, 1000) == lmc.LMC_ERR_NOT_MULTIPLE
+    assert _raw_call(lmc, fn, L, 0) == lmc.LMC_ERR_NOT_MULTIPLE
+    assert _raw_call(lmc, fn, L, 944, status_off=2) == lmc.LMC_ERR_ALIGN
+    assert _raw_call(lmc, fn, L, 944, nkv=3) == lmc.LMC_ERR_INVALID_ARG
+    assert _raw_call(lmc, fn, L, 944, nog=1) == lmc.LMC_ERR_INVALID_ARG
+    assert _raw_call(lmc, fn, L, 944, njobs=-1) == lmc.LMC_ERR_INVALID_ARG
+    assert _raw_call(lmc, fn, L, 944, njobs=3, null_jobs=True) == lmc.LMC_ERR_INVALID_ARG
+    # nothing to move: returns OK without touching the device
+    assert _raw_call(lmc, fn, L, 944, njobs=0) == lmc.LMC_OK
+    assert _raw_call(lmc, fn, L, 944, njobs=0, null_jobs=True) == lmc.LMC_OK

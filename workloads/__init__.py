@@ -254,3 +254,63 @@ def fill_normal_np(n: int, seed: int) -> np.ndarray:
     buf[:n4] = rng.standard_normal(n4 // 4, dtype=np.float32).view(np.uint8)
     buf[n4:] = rng.integers(0, 256, n - n4, dtype=np.uint8)
     return buf
+
+
+# ----------------------------------------------------------------------------
+# A whole batch of inputs for one workload
+# ----------------------------------------------------------------------------
+
+@dataclass
+class Inputs:
+    cfg: Config
+    C: int
+    layout: object
+    request_ids: list
+    lengths: np.ndarray
+    object_bytes: list
+    tables_src: list                  # store-side pool (and the mixed step's single pool)
+    tables_dst: list | None = None    # load-side fresh pool
+    jobs: list | None = None          # store jobs, also loaded back
+    arena_bytes: int = 0
+    hits: np.ndarray | None = None
+    load_jobs: list | None = None     # mixed step
+    load_arena_bytes: int = 0
+    store_jobs: list | None = None
+    store_arena_bytes: int = 0
+
+    @property
+    def payload_bytes(self):
+        """Bytes of objects moved by one store (or one load) of `jobs`."""
+        if self.jobs is None:
+            return 0
+        return sum(int(self.object_bytes[g]) * len(j) for g, j in enumerate(self.jobs))
+
+
+def make_inputs(cfg: Config, build_layout, C: int, request_ids=None) -> Inputs:
+    """Seeded inputs for `cfg`. `build_layout(mem_bytes)` builds the layout
+    under test (oracle or library) and `C` is the negotiated chunk; the pool
+    gets exactly the blocks the batch needs (or the workload's fixed count)."""
+    all_lengths = request_lengths(cfg)
+    ids = list(range(cfg.num_requests)) if request_ids is None else list(request_ids)
+    lengths = all_lengths[ids]
+    probe = build_layout(1 << 60)
+    per_block = probe.pool_bytes // probe.num_blocks
+    hits = hit_chunks(cfg, all_lengths, C)[ids] if cfg.mixed else None
+    need = count_blocks(cfg, probe.kv_group_kind, lengths, cfg.N, C, hits)
+    nb = cfg.pool_blocks or need
+    layout = build_layout(nb * per_block)
+    assert layout.num_blocks == nb
+    sizes = [layout.object_bytes(C, g) for g in range(layout.num_object_groups)]
+    seed = cfg.seed + 7919 * (ids[0] if ids else 0)
+    src = block_tables(cfg, layout.kv_group_kind, lengths, cfg.N, C, nb, seed, hits)
+    inp = Inputs(cfg=cfg, C=C, layout=layout, request_ids=ids, lengths=lengths, object_bytes=sizes,
+                 tables_src=src, hits=hits)
+    if cfg.mixed:
+        og_kinds = [cfg.layers[layout.object_group.index(g)]["kind"] for g in range(layout.num_object_groups)]
+        lu, su = mixed_units(cfg, lengths, hits, C, og_kinds)
+        inp.load_jobs, inp.load_arena_bytes = pack_jobs(lu, sizes)
+        inp.store_jobs, inp.store_arena_bytes = pack_jobs(su, sizes)
+    else:
+        inp.tables_dst = block_tables(cfg, layout.kv_group_kind, lengths, cfg.N, C, nb, seed + 1000)
+        inp.jobs, inp.arena_bytes = pack_jobs(store_units(lengths, C, layout.num_object_groups), sizes)
+    return inp
