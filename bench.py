@@ -337,7 +337,7 @@ def run_gpu(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        line["cpu_baseline"] = oracle_sample(args.config, requests=8, reps=3, threads=threads)
+        line["cpu_baseline"] = oracle_sample(args.config, requests=8, reps=20, threads=threads)
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -64,6 +64,8 @@ extern "C" {
 #define LMC_ST_BAD_JOB 0x8u     /* request out of range, chunk < 0, block position
                                    past the table's columns, or an object that is
                                    not 16-byte aligned or does not fit the arena */
+#define LMC_ST_TIMEOUT 0x10u    /* a bounded wait inside the kernel gave up; the
+                                   launch's output is incomplete */
 
 /* ---- layer specs --------------------------------------------------------- */
 #define LMC_LAYER_MLA 0 /* full attention, one latent entry per token */

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "liblmc.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"liblmc.so is not built at {LIB_PATH}: run `python state_cache_paging_gb300/build.py`")
 
-_lib = ctypes.CDLL(LIB_PATH)
+_lib = None  # bound by _use_library below
 
 LMC_OK = 0
 LMC_ERR_INVALID_ARG = -1
@@ -38,6 +38,7 @@ LMC_ST_BLOCK_OOR = 0x1
 LMC_ST_NO_BLOCK = 0x2
 LMC_ST_NO_SNAPSHOT = 0x4
 LMC_ST_BAD_JOB = 0x8
+LMC_ST_TIMEOUT = 0x10
 
 LMC_LAYER = {"MLA": 0, "KDA": 1, "SWA": 2}
 LMC_LAYER_NAME = {v: k for k, v in LMC_LAYER.items()}
@@ -94,19 +95,34 @@ class lmc_batch(ctypes.Structure):
 
 _P = ctypes.POINTER
 _i64 = ctypes.c_int64
-_lib.lmc_layout_build.argtypes = [_P(lmc_layout_params), _P(ctypes.c_void_p)]
-_lib.lmc_layout_query.argtypes = [ctypes.c_void_p, _P(lmc_layout_info)]
-_lib.lmc_layout_free.argtypes = [ctypes.c_void_p]
-_lib.lmc_layout_free.restype = None
-_lib.lmc_object_bytes.argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, _P(_i64)]
-_lib.lmc_negotiate_chunk.argtypes = [_i64, _i64, ctypes.c_int, _P(_i64)]
-_lib.lmc_check_step_budget.argtypes = [_i64, _i64, ctypes.c_int]
-_lib.lmc_unified_block_size.argtypes = [_i64, _i64, _i64, _P(_i64)]
-for _name in ("lmc_store", "lmc_load"):
-    getattr(_lib, _name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
-                                     _i64, ctypes.c_void_p, ctypes.c_void_p]
-_lib.lmc_strerror.argtypes = [ctypes.c_int]
-_lib.lmc_strerror.restype = ctypes.c_char_p
+
+
+def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
+    so.lmc_layout_build.argtypes = [_P(lmc_layout_params), _P(ctypes.c_void_p)]
+    so.lmc_layout_query.argtypes = [ctypes.c_void_p, _P(lmc_layout_info)]
+    so.lmc_layout_free.argtypes = [ctypes.c_void_p]
+    so.lmc_layout_free.restype = None
+    so.lmc_object_bytes.argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, _P(_i64)]
+    so.lmc_negotiate_chunk.argtypes = [_i64, _i64, ctypes.c_int, _P(_i64)]
+    so.lmc_check_step_budget.argtypes = [_i64, _i64, ctypes.c_int]
+    so.lmc_unified_block_size.argtypes = [_i64, _i64, _i64, _P(_i64)]
+    for name in ("lmc_store", "lmc_load"):
+        getattr(so, name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
+                                      _i64, ctypes.c_void_p, ctypes.c_void_p]
+    so.lmc_strerror.argtypes = [ctypes.c_int]
+    so.lmc_strerror.restype = ctypes.c_char_p
+    return so
+
+
+def _use_library(path: str) -> None:
+    """Binds the package to another build of liblmc (e.g. one compiled with
+    other tile constants). Layouts built before the switch must not be used
+    after it."""
+    global _lib
+    _lib = _bind(ctypes.CDLL(path))
+
+
+_use_library(LIB_PATH)
 
 
 def lmc_strerror(code: int) -> str:

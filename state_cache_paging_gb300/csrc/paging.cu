@@ -37,6 +37,15 @@
 #ifndef LMC_UNROLL
 #define LMC_UNROLL 4
 #endif
+#ifndef LMC_ENGINE
+#define LMC_ENGINE 0  // 0: vector loads/stores, 1: bulk (TMA) copies through shared memory
+#endif
+#ifndef LMC_BULK_STAGES
+#define LMC_BULK_STAGES 4
+#endif
+#ifndef LMC_BULK_CTAS_PER_SM
+#define LMC_BULK_CTAS_PER_SM 1
+#endif
 
 namespace {
 
@@ -46,6 +55,11 @@ constexpr int kMaxKv = 64;                   // KV groups (block tables)
 constexpr int kTileBytes = LMC_TILE_BYTES;
 constexpr int kThreads = LMC_THREADS;
 constexpr int kUnroll = LMC_UNROLL;
+constexpr int kEngine = LMC_ENGINE;
+constexpr int kBulkStages = LMC_BULK_STAGES;
+constexpr int kBulkCtasPerSm = LMC_BULK_CTAS_PER_SM;
+static_assert(kEngine != 1 || kBulkCtasPerSm * (kBulkStages * kTileBytes + 1024) <= 228 * 1024,
+              "bulk stages must fit the SM's shared memory");
 
 // One layer's run of pages inside an object of one group.
 struct Entry {
@@ -164,8 +178,10 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
     return 0;
 }
 
+// Vector engine: every thread of the CTA copies 16-byte vectors of the tile,
+// kUnroll loads in flight before the matching stores.
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) page_copy_kernel(const __grid_constant__ Plan P) {
+__device__ __forceinline__ void copy_tiles(const Plan &P) {
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
         Span s;
         const uint32_t bad = resolve(P, tile, s);
@@ -195,6 +211,157 @@ __global__ void __launch_bounds__(kThreads) page_copy_kernel(const __grid_consta
                 s.dst[i] = s.src[i];
         }
     }
+}
+
+// Distinct names for the two directions (they share the body; the plan says
+// which side is the pool).
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) lmc_store_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<kVec>(P);
+}
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) lmc_load_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<kVec>(P);
+}
+
+// ---------------------------------------------------------------------------
+// Bulk engine: one thread per CTA moves each tile global -> shared -> global
+// with the bulk-copy (TMA) unit: cp.async.bulk into a shared-memory stage
+// completing on an mbarrier, then cp.async.bulk back out as a bulk group.
+// kStages stages form a ring, so kStages - 1 loads and the trailing stores
+// are in flight per CTA. Every wait is bounded; on time-out the kernel raises
+// LMC_ST_TIMEOUT, drains its own copies (bounded) and returns.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds (each may suspend)
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t k = 0; k < kWaitLimit; k++)
+        if (mbar_try_wait(bar, parity))
+            return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+template <int kStages>
+__device__ __forceinline__ void bulk_tiles(const Plan &P) {
+    static_assert(kStages >= 2, "the ring needs a stage to fill while another drains");
+    extern __shared__ __align__(128) uint8_t stage_mem[];
+    __shared__ uint64_t bars[kStages];
+    if (threadIdx.x != 0)
+        return;
+    for (int s = 0; s < kStages; s++)
+        mbar_init(&bars[s]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+    Span span[kStages];
+    int32_t state[kStages];  // -1: no tile left, 0: skipped tile, 1: load in flight, 2: stored
+    uint32_t parity = 0;     // bit s: phase parity to wait for on stage s
+    int64_t next = blockIdx.x;
+
+    auto issue = [&](int s) {
+        if (next >= P.total_tiles) {
+            state[s] = -1;
+            return;
+        }
+        const uint32_t bad = resolve(P, next, span[s]);
+        next += gridDim.x;
+        if (bad) {
+            atomicOr(P.status, bad);
+            state[s] = 0;
+            return;
+        }
+        uint8_t *buf = stage_mem + (size_t)s * kTileBytes;
+        mbar_arrive_expect(&bars[s], (uint32_t)span[s].bytes);
+        bulk_load(buf, span[s].src, (uint32_t)span[s].bytes, &bars[s]);
+        state[s] = 1;
+    };
+
+    for (int s = 0; s < kStages - 1; s++)
+        issue(s);
+    state[kStages - 1] = -1;
+    bool timed_out = false;
+    for (int64_t i = 0;; i++) {
+        const int s = (int)(i % kStages);  // stage holding this CTA's i-th tile
+        if (state[s] < 0)
+            break;
+        if (state[s] == 1) {
+            if (!mbar_wait(&bars[s], (parity >> s) & 1u)) {
+                timed_out = true;
+                break;
+            }
+            parity ^= 1u << s;
+            bulk_store(span[s].dst, stage_mem + (size_t)s * kTileBytes, (uint32_t)span[s].bytes);
+            state[s] = 2;
+        }
+        bulk_commit();
+        // all stores but the one just issued have read their stage: the
+        // stage of tile i - 1 is free for tile i + kStages - 1
+        bulk_wait_read_all_but_one();
+        issue((int)((i + kStages - 1) % kStages));
+    }
+    if (timed_out) {
+        atomicOr(P.status, LMC_ST_TIMEOUT);
+        // let the loads still in flight land before the CTA's shared memory goes away
+        for (int s = 0; s < kStages; s++)
+            if (state[s] == 1)
+                mbar_wait(&bars[s], (parity >> s) & 1u);
+    }
+    bulk_wait_all();
+}
+
+template <int kStages>
+__global__ void __launch_bounds__(32) lmc_store_bulk_kernel(const __grid_constant__ Plan P) {
+    bulk_tiles<kStages>(P);
+}
+template <int kStages>
+__global__ void __launch_bounds__(32) lmc_load_bulk_kernel(const __grid_constant__ Plan P) {
+    bulk_tiles<kStages>(P);
 }
 
 int sm_count() {
@@ -318,17 +485,26 @@ int launch(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_batch
     int rc = build_plan(L, chunk, pool, b, arena, arena_bytes, status, store, P, vec);
     if (rc != LMC_OK || P.total_tiles == 0)
         return rc;
-    // One CTA per tile, capped; the kernel strides over the rest.
     const int sms = sm_count();
     if (sms <= 0)
         return LMC_ERR_CUDA;
-    const int64_t cap = (int64_t)sms * 2048;
-    const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, cap);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec)
-        page_copy_kernel<true><<<grid, kThreads, 0, s>>>(P);
-    else
-        page_copy_kernel<false><<<grid, kThreads, 0, s>>>(P);
+    if (vec && kEngine == 1) {
+        // persistent: kBulkCtasPerSm CTAs per SM, each a ring of stages
+        const size_t smem = (size_t)kBulkStages * kTileBytes;
+        auto kern = store ? lmc_store_bulk_kernel<kBulkStages> : lmc_load_bulk_kernel<kBulkStages>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return LMC_ERR_CUDA;
+        const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * kBulkCtasPerSm);
+        kern<<<grid, 32, smem, s>>>(P);
+    } else {
+        // one CTA per tile, capped; the kernel strides over the rest
+        const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * 2048);
+        if (vec)
+            (store ? lmc_store_kernel<true> : lmc_load_kernel<true>)<<<grid, kThreads, 0, s>>>(P);
+        else
+            (store ? lmc_store_kernel<false> : lmc_load_kernel<false>)<<<grid, kThreads, 0, s>>>(P);
+    }
     return cudaGetLastError() == cudaSuccess ? LMC_OK : LMC_ERR_CUDA;
 }
 
