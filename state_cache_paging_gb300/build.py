@@ -9,8 +9,10 @@ in the process.
 from __future__ import annotations
 
 import os
+import shutil
 import subprocess
 import sys
+import tempfile
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -47,9 +49,9 @@ def build_library(force: bool = False, extra_nvcc=(), out_path: str | None = Non
     if not force and not extra_nvcc and out_path is None and not _stale(out):
         return out
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tag = f"{os.getpid()}"
-    cu_obj = os.path.join(BUILD_DIR, f"paging.{tag}.o")
-    cpp_obj = os.path.join(BUILD_DIR, f"layout.{tag}.o")
+    work = tempfile.mkdtemp(dir=BUILD_DIR)  # private per build (builds may run concurrently)
+    cu_obj = os.path.join(work, "paging.o")
+    cpp_obj = os.path.join(work, "layout.o")
     ptxas_log = os.path.join(BUILD_DIR, "ptxas.log")
     cmds = [
         [NVCC, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
@@ -66,14 +68,13 @@ def build_library(force: bool = False, extra_nvcc=(), out_path: str | None = Non
         f.write(logs[0])
     if verbose:
         print(logs[0])
-    tmp = out + f".tmp{tag}"
+    tmp = os.path.join(work, "liblmc.so")
     link = [NVCC, "-shared", *ARCH, "-o", tmp, cu_obj, cpp_obj]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout}{r.stderr}")
     os.replace(tmp, out)
-    for o in (cu_obj, cpp_obj):
-        os.remove(o)
+    shutil.rmtree(work, ignore_errors=True)
     return out
 
 
