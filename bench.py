@@ -133,38 +133,71 @@ def _dist():
 # CPU oracle leg (cpu_baseline and --impl reference)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(cfg_index: int, requests: int, reps: int, threads: int, warmup: int = 1):
-    """Times the CPU oracle's store + load on a bounded sample of the workload
-    (the first `requests` requests), `threads` workers over disjoint jobs."""
+def oracle_sample(cfg_index: int, requests: int, reps: int, threads: int, warmup: int = 1,
+                  budget_bytes: int = 3 << 30):
+    """Times the CPU oracle on a bounded sample of the workload: the first
+    `requests` requests, each cut to at most the tokens that keep the sample's
+    payload near `budget_bytes`; `threads` workers over disjoint jobs. Plain
+    workloads: store then load into a fresh pool; the mixed step: load of the
+    cached chunks and store of the new chunks on one pool."""
+    import dataclasses
     from concurrent.futures import ThreadPoolExecutor
+
+    import torch
 
     import oracle
     cfg = W.CONFIGS[cfg_index]
     C = oracle.negotiate_chunk(cfg.requested_chunk, cfg.N)
     ids = list(range(min(requests, cfg.num_requests)))
-    inp = W.make_inputs(cfg, functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed), C, ids)
+    build = functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed)
+    probe = oracle.layout(cfg.layers, cfg.N, cfg.packed, 1 << 60)
+    per_chunk = sum(probe.object_bytes(C, g) for g in range(probe.num_object_groups))
+    max_chunks = max(1, budget_bytes // (per_chunk * len(ids)))
+    lengths = W.request_lengths(cfg)
+    if lengths.max() // C > max_chunks:
+        capped = tuple(int(min(x, max_chunks * C + C // 2)) for x in lengths)
+        cfg = dataclasses.replace(cfg, lengths="fixed", fixed_lengths=capped)
+    inp = W.make_inputs(cfg, build, C, ids)
     L = inp.layout
-    import torch
     pool = W.fill_normal(torch.empty(L.pool_bytes, dtype=torch.uint8), cfg.seed).numpy()
-    fresh = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
-    arena = np.zeros(inp.arena_bytes, dtype=np.uint8)
-    # split every group's jobs into `threads` disjoint slices
-    parts = [[J[k::threads] for J in inp.jobs] for k in range(threads)]
-    payload = inp.payload_bytes
+    sizes = inp.object_bytes
+    if cfg.mixed:
+        src = W.fill_normal(torch.empty(inp.load_arena_bytes, dtype=torch.uint8), cfg.seed + 7).numpy()
+        out = np.zeros(inp.store_arena_bytes, dtype=np.uint8)
+        lparts = [[J[k::threads] for J in inp.load_jobs] for k in range(threads)]
+        sparts = [[J[k::threads] for J in inp.store_jobs] for k in range(threads)]
+        payload = (sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.load_jobs)) +
+                   sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.store_jobs)))
+
+        def one_pass(ex):
+            a = list(ex.map(lambda p: oracle.load(L, C, pool, inp.tables_src, p, src), lparts))
+            b = list(ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, out), sparts))
+            return a + b
+        chunks = sum(len(j) for j in inp.store_jobs) // max(1, L.num_object_groups)
+    else:
+        fresh = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        arena = np.zeros(inp.arena_bytes, dtype=np.uint8)
+        parts = [[J[k::threads] for J in inp.jobs] for k in range(threads)]
+        payload = 2 * inp.payload_bytes
+
+        def one_pass(ex):
+            a = list(ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, arena), parts))
+            b = list(ex.map(lambda p: oracle.load(L, C, fresh, inp.tables_dst, p, arena), parts))
+            return a + b
+        chunks = sum(int(x) // C for x in inp.lengths)
     with ThreadPoolExecutor(threads) as ex:
         for _ in range(warmup):
-            list(ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, arena), parts))
-            list(ex.map(lambda p: oracle.load(L, C, fresh, inp.tables_dst, p, arena), parts))
+            one_pass(ex)
         t0 = time.perf_counter()
         for _ in range(reps):
-            assert all(s == 0 for s in ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, arena), parts))
-            assert all(s == 0 for s in ex.map(lambda p: oracle.load(L, C, fresh, inp.tables_dst, p, arena), parts))
+            assert all(st == 0 for st in one_pass(ex))
         dt = time.perf_counter() - t0
-    chunks = sum(int(x) // C for x in inp.lengths)
-    gbs = 4 * payload * reps / dt / 1e9
+    gbs = 2 * payload * reps / dt / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {len(ids)} of {cfg.num_requests} requests ({payload} payload bytes per direction), "
-                      f"{reps} timed store+load passes after {warmup} warm-up, {threads} threads over disjoint jobs",
+            "sample": f"first {len(ids)} of {W.CONFIGS[cfg_index].num_requests} requests"
+                      f"{' (cut to ' + str(max_chunks) + ' chunks each)' if cfg is not W.CONFIGS[cfg_index] else ''}"
+                      f", {payload} object bytes moved per pass (store + load), {reps} timed passes after "
+                      f"{warmup} warm-up, {threads} threads over disjoint jobs",
             "chunks_per_s": round(chunks * reps / dt, 2), "seconds": round(dt, 3)}
 
 
@@ -191,6 +224,129 @@ def run_reference(args):
 # GPU arm
 # ----------------------------------------------------------------------------
 
+class PagingStep:
+    """Device inputs and one step of the hot path for a workload.
+
+    Plain workloads: the store (pool -> objects) then the load (objects ->
+    a fresh pool under new block tables), on one stream. The mixed step
+    (one pool): the load of cached chunks and the store of new chunks,
+    issued concurrently on two streams that touch disjoint blocks."""
+
+    def __init__(self, lmc, torch, cfg, dev, rank, ids):
+        self.lmc, self.torch, self.cfg, self.dev = lmc, torch, cfg, dev
+        C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
+        build = functools.partial(lmc.lmc_layout_build, cfg.layers, cfg.N, cfg.packed)
+        inp = W.make_inputs(cfg, build, C, ids)
+        self.inp, self.L, self.C = inp, inp.layout, C
+        L = self.L
+        T = torch
+        self.main = T.cuda.current_stream(dev)
+        self.pool = T.empty(L.pool_bytes, dtype=T.uint8, device=dev)
+        W.fill_normal(self.pool, cfg.seed + 101 * rank)
+        self.status = T.zeros(1, dtype=T.int32, device=dev)
+        self.t_src = [T.from_numpy(t).to(dev) for t in inp.tables_src]
+        if cfg.mixed:
+            sizes = inp.object_bytes
+            self.load_payload = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.load_jobs))
+            self.store_payload = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.store_jobs))
+            self.load_arena = T.empty(inp.load_arena_bytes, dtype=T.uint8, device=dev)
+            W.fill_normal(self.load_arena, cfg.seed + 7)
+            self.store_arena = T.empty(inp.store_arena_bytes, dtype=T.uint8, device=dev)
+            self.load_jobs = [lmc.jobs_to_device(j, dev) for j in inp.load_jobs]
+            self.store_jobs = [lmc.jobs_to_device(j, dev) for j in inp.store_jobs]
+            self.sa = T.cuda.Stream(dev)
+            self.sb = T.cuda.Stream(dev)
+            self.chunks = int(sum(len(j) for j in inp.store_jobs) // max(1, L.num_object_groups))
+            self.launches_per_step = 2
+        else:
+            self.load_payload = self.store_payload = inp.payload_bytes
+            self.fresh = T.full((L.pool_bytes,), W.SENTINEL, dtype=T.uint8, device=dev)
+            self.arena = T.empty(inp.arena_bytes, dtype=T.uint8, device=dev)
+            self.t_dst = [T.from_numpy(t).to(dev) for t in inp.tables_dst]
+            self.jobs = [lmc.jobs_to_device(j, dev) for j in inp.jobs]
+            self.chunks = int(sum(int(x) // C for x in inp.lengths))
+            self.launches_per_step = 2
+        # every payload byte is read once and written once, by the store and by the load
+        self.bytes_per_step = 2 * (self.load_payload + self.store_payload)
+
+    def new_events(self):
+        E = self.torch.cuda.Event
+        return [E(enable_timing=True) for _ in range(4)]
+
+    def step(self, ev=None):
+        lmc, L, C = self.lmc, self.L, self.C
+        if not self.cfg.mixed:
+            if ev is not None:
+                ev[0].record(self.main)
+            lmc.lmc_store(L, C, self.pool, self.t_src, self.jobs, self.arena, self.status, self.main)
+            if ev is not None:
+                ev[1].record(self.main)
+                ev[2].record(self.main)
+            lmc.lmc_load(L, C, self.fresh, self.t_dst, self.jobs, self.arena, self.status, self.main)
+            if ev is not None:
+                ev[3].record(self.main)
+            return
+        fork = self.torch.cuda.Event()
+        fork.record(self.main)
+        self.sa.wait_event(fork)
+        self.sb.wait_event(fork)
+        if ev is not None:
+            ev[2].record(self.sa)
+            ev[0].record(self.sb)
+        lmc.lmc_load(L, C, self.pool, self.t_src, self.load_jobs, self.load_arena, self.status, self.sa)
+        lmc.lmc_store(L, C, self.pool, self.t_src, self.store_jobs, self.store_arena, self.status, self.sb)
+        if ev is not None:
+            ev[3].record(self.sa)
+            ev[1].record(self.sb)
+        ja, jb = self.torch.cuda.Event(), self.torch.cuda.Event()
+        ja.record(self.sa)
+        jb.record(self.sb)
+        self.main.wait_event(ja)
+        self.main.wait_event(jb)
+
+    def setup_e2e(self):
+        """Pinned host buffers for the end-to-end step: block tables and jobs
+        go host -> device each step; objects leave the device for the host
+        cache tier (store) and come back from it (load)."""
+        T, inp = self.torch, self.inp
+        pin = lambda a: T.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        self.h_tables = [pin(t) for t in inp.tables_src] + ([pin(t) for t in inp.tables_dst] if not self.cfg.mixed else [])
+        self.d_tables = self.t_src + ([] if self.cfg.mixed else self.t_dst)
+        if self.cfg.mixed:
+            self.h_jobs = [pin(j.view(np.uint8)) for j in inp.load_jobs + inp.store_jobs]
+            self.d_jobs = self.load_jobs + self.store_jobs
+            self.h_load = T.empty(inp.load_arena_bytes, dtype=T.uint8, pin_memory=True)
+            self.h_load.copy_(self.load_arena)
+            self.h_store = T.empty(inp.store_arena_bytes, dtype=T.uint8, pin_memory=True)
+            objs_in, objs_out = inp.load_arena_bytes, inp.store_arena_bytes
+        else:
+            self.h_jobs = [pin(j.view(np.uint8)) for j in inp.jobs]
+            self.d_jobs = self.jobs
+            self.h_arena = T.empty(inp.arena_bytes, dtype=T.uint8, pin_memory=True)
+            objs_in, objs_out = inp.arena_bytes, inp.arena_bytes
+        self.h_status = T.zeros(1, dtype=T.int32, pin_memory=True)
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_tables) + \
+            sum(j.numel() for j in self.h_jobs) + objs_in
+        self.d2h = objs_out + 4
+
+    def e2e_step(self):
+        lmc, L, C = self.lmc, self.L, self.C
+        for h, d in zip(self.h_tables, self.d_tables):
+            d.copy_(h, non_blocking=True)
+        for h, d in zip(self.h_jobs, self.d_jobs):
+            d.copy_(h, non_blocking=True)
+        if self.cfg.mixed:
+            self.load_arena.copy_(self.h_load, non_blocking=True)
+            self.step()
+            self.h_store.copy_(self.store_arena, non_blocking=True)
+        else:
+            lmc.lmc_store(L, C, self.pool, self.t_src, self.jobs, self.arena, self.status, self.main)
+            self.h_arena.copy_(self.arena, non_blocking=True)
+            self.arena.copy_(self.h_arena, non_blocking=True)
+            lmc.lmc_load(L, C, self.fresh, self.t_dst, self.jobs, self.arena, self.status, self.main)
+        self.h_status.copy_(self.status, non_blocking=True)
+
+
 def run_gpu(args):
     import torch
 
@@ -202,37 +358,12 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = W.CONFIGS[args.config]
-    if cfg.mixed:
-        raise SystemExit("the mixed step is measured by --config 4 in bench_mixed mode only")
-
-    C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
-    ids = list(range(cfg.num_requests)) if args.requests is None else list(range(args.requests))
+    n_req = cfg.num_requests if args.requests is None else min(args.requests, cfg.num_requests)
+    if cfg.waves > 1 and args.requests is None:
+        n_req = cfg.num_requests // cfg.waves  # one wave fits the device; the step is one wave
     # each rank runs its own independent copy of the batch (weak scaling)
-    build = functools.partial(lmc.lmc_layout_build, cfg.layers, cfg.N, cfg.packed)
-    inp = W.make_inputs(cfg, build, C, ids)
-    L = inp.layout
-    payload = inp.payload_bytes
-    chunks = sum(int(x) // C for x in inp.lengths)
-
-    pool = torch.empty(L.pool_bytes, dtype=torch.uint8, device=dev)
-    W.fill_normal(pool, cfg.seed + 101 * rank)
-    fresh = torch.full((L.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=dev)
-    arena = torch.empty(inp.arena_bytes, dtype=torch.uint8, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    t_src = [torch.from_numpy(t).to(dev) for t in inp.tables_src]
-    t_dst = [torch.from_numpy(t).to(dev) for t in inp.tables_dst]
-    jobs = [lmc.jobs_to_device(j, dev) for j in inp.jobs]
-    stream = torch.cuda.current_stream(dev)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        lmc.lmc_store(L, C, pool, t_src, jobs, arena, status, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        lmc.lmc_load(L, C, fresh, t_dst, jobs, arena, status, stream)
-        if ev is not None:
-            ev[2].record(stream)
+    S = PagingStep(lmc, torch, cfg, dev, rank, list(range(n_req)))
+    L = S.L
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -240,60 +371,39 @@ def run_gpu(args):
             dist.barrier()
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        S.step()
     barrier()
-    assert int(status.item()) == 0, f"device status {int(status.item()):#x}"
+    assert int(S.status.item()) == 0, f"device status {int(S.status.item()):#x}"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [S.new_events() for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         barrier()
-        t_start.record(stream)
+        t_start.record(S.main)
         for k in range(args.steps):
-            step(evs[k])
-        t_end.record(stream)
+            S.step(evs[k])
+        t_end.record(S.main)
         barrier()
     clocks = clk.summary()
     total_ms = t_start.elapsed_time(t_end)
     store_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    load_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    assert int(status.item()) == 0
+    load_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    assert int(S.status.item()) == 0
 
-    # end to end through the public API with host buffers: per step, the
-    # block tables and jobs go host -> device, the stored objects go device ->
-    # host (the host cache tier), come back host -> device and are loaded.
-    host_arena = torch.empty(inp.arena_bytes, dtype=torch.uint8, pin_memory=True)
-    host_tables = [torch.from_numpy(t).pin_memory() for t in inp.tables_src + inp.tables_dst]
-    host_jobs = [torch.from_numpy(np.ascontiguousarray(j).view(np.uint8)).pin_memory() for j in inp.jobs]
-    host_status = torch.zeros(1, dtype=torch.int32, pin_memory=True)
-    dev_tables = t_src + t_dst
-    h2d = sum(t.numel() * 4 for t in host_tables) + sum(j.numel() for j in host_jobs) + inp.arena_bytes
-    d2h = inp.arena_bytes + 4
-
-    def e2e_step():
-        for h, d in zip(host_tables, dev_tables):
-            d.copy_(h, non_blocking=True)
-        for h, d in zip(host_jobs, jobs):
-            d.copy_(h, non_blocking=True)
-        lmc.lmc_store(L, C, pool, t_src, jobs, arena, status, stream)
-        host_arena.copy_(arena, non_blocking=True)
-        arena.copy_(host_arena, non_blocking=True)
-        lmc.lmc_load(L, C, fresh, t_dst, jobs, arena, status, stream)
-        host_status.copy_(status, non_blocking=True)
-
+    S.setup_e2e()
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     for _ in range(2):
-        e2e_step()
+        S.e2e_step()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(S.main)
     for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+        S.e2e_step()
+    e1.record(S.main)
     barrier()
-    assert int(host_status.item()) == 0
+    assert int(S.h_status.item()) == 0
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     ms_per_step = total_ms / args.steps
@@ -305,34 +415,39 @@ def run_gpu(args):
         dist.destroy_process_group()
         return
 
-    bytes_per_step = 4 * payload  # store and load each read and write every payload byte
-    value = bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
+    value = S.bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = _peaks()
     st_avg, ld_avg = statistics.mean(store_ms), statistics.mean(load_ms)
-    dominant, dom_ms = ("store", st_avg) if st_avg >= ld_avg else ("load", ld_avg)
-    achieved = 2 * payload / (dom_ms * 1e-3) / 1e9
+    if cfg.mixed:
+        # the two kernels share HBM concurrently: the roofline is the step's
+        dominant, dom_bytes, dom_ms = "store+load (concurrent)", S.bytes_per_step, ms_per_step
+    elif st_avg >= ld_avg:
+        dominant, dom_bytes, dom_ms = "store", 2 * S.store_payload, st_avg
+    else:
+        dominant, dom_bytes, dom_ms = "load", 2 * S.load_payload, ld_avg
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": cfg.name, "index": cfg.index, "requests": len(ids),
-                   "payload_bytes_per_direction": payload, "chunk": C, "N": cfg.N,
-                   "layout": "packed" if cfg.packed else "padded", "pool_bytes": L.pool_bytes,
-                   "l2": "inputs larger than L2 (pool and objects are each > 11 GB; no flush)",
+        "config": {"workload": cfg.name, "index": cfg.index, "requests": n_req,
+                   "store_payload_bytes": S.store_payload, "load_payload_bytes": S.load_payload,
+                   "chunk": S.C, "N": cfg.N, "layout": "packed" if cfg.packed else "padded",
+                   "pool_bytes": L.pool_bytes,
+                   "l2": "inputs larger than L2 (pool and objects are each many GB; no flush)",
                    "parallelism": f"{world} independent replica(s), no exchange"},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "chunks_per_s": round(chunks * world / (ms_per_step * 1e-3), 1),
-        "store": {"ms": round(st_avg, 4), "gbs": round(2 * payload / (st_avg * 1e-3) / 1e9, 2)},
-        "load": {"ms": round(ld_avg, 4), "gbs": round(2 * payload / (ld_avg * 1e-3) / 1e9, 2)},
+        "chunks_per_s": round(S.chunks * world / (ms_per_step * 1e-3), 1),
+        "store": {"ms": round(st_avg, 4), "gbs": round(2 * S.store_payload / (st_avg * 1e-3) / 1e9, 2)},
+        "load": {"ms": round(ld_avg, 4), "gbs": round(2 * S.load_payload / (ld_avg * 1e-3) / 1e9, 2)},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic(dominant, cfg.index),
-                     "algorithmic_bytes_per_launch": 2 * payload},
-        "e2e": {"value": round(bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
+                     "traffic": _traffic(dominant, cfg.index), "algorithmic_bytes_per_launch": dom_bytes},
+        "e2e": {"value": round(S.bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h},
+        "gpu_launches": S.launches_per_step * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -28,11 +28,14 @@
 
 #include "lmc_internal.h"
 
+// Defaults picked by measurement on GB300 (Kimi-Linear and K3 workloads):
+// 32 KB tiles, 512 threads, 4 vectors in flight per thread, i.e. one CTA
+// moves its whole tile with a single round of loads and stores.
 #ifndef LMC_TILE_BYTES
-#define LMC_TILE_BYTES 65536
+#define LMC_TILE_BYTES 32768
 #endif
 #ifndef LMC_THREADS
-#define LMC_THREADS 256
+#define LMC_THREADS 512
 #endif
 #ifndef LMC_UNROLL
 #define LMC_UNROLL 4
@@ -110,17 +113,38 @@ struct Plan {
 };
 static_assert(sizeof(Plan) <= 32000, "kernel parameter space");
 
+#ifndef LMC_LD_HINT
+#define LMC_LD_HINT 0  // 0: .nc.L1::no_allocate, 1: + .L2::256B prefetch, 2: plain
+#endif
+#ifndef LMC_ST_HINT
+#define LMC_ST_HINT 0  // 0: .cs (evict-first), 1: plain write-back, 2: .L1::no_allocate
+#endif
+
+// Source bytes are read once: bypass L1 (and never alias the destination).
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
+#if LMC_LD_HINT == 0
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+#elif LMC_LD_HINT == 1
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+#else
+    asm("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+#endif
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
     return v;
 }
 
+// Destination bytes are not read back by this kernel.
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
+#if LMC_ST_HINT == 0
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+#elif LMC_ST_HINT == 1
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+#else
+    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};"
+#endif
+                 ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
 

@@ -21,11 +21,12 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-@pytest.fixture(scope="module", autouse=True)
+@pytest.fixture(autouse=True)
 def _gpu():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     yield
+    torch.cuda.synchronize()
     torch.cuda.empty_cache()
 
 
@@ -252,3 +253,74 @@ def test_full_size_kimi_linear_packed_lognormal(lmc):
 def test_full_size_k3_one_wave(lmc):
     """K3 (93 layers, N = 768, chunk 1536): one request of 131,072 tokens."""
     _full_size(lmc, W.CONFIGS[3], request_ids=[2], per_group=6)
+
+
+def _mixed_run(lmc, inp, Lp, pool, load_arena):
+    """The mixed serving step: load of cached chunks on one stream, store of
+    new chunks on another, both on the same pool (disjoint blocks)."""
+    store_arena = torch.empty(inp.store_arena_bytes, dtype=torch.uint8, device=DEV)
+    st = _status()
+    tabs = dev_tables(inp.tables_src, DEV)
+    lj, sj = dev_jobs(inp.load_jobs, DEV), dev_jobs(inp.store_jobs, DEV)
+    sa, sb = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    fork = torch.cuda.Event()
+    fork.record()
+    sa.wait_event(fork)
+    sb.wait_event(fork)
+    lmc.lmc_load(Lp, inp.C, pool, tabs, lj, load_arena, st, sa)
+    lmc.lmc_store(Lp, inp.C, pool, tabs, sj, store_arena, st, sb)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return store_arena, tabs, lj
+
+
+def test_mixed_step_exact_first_requests(lmc):
+    """The mixed step on the first 24 requests, compared in full."""
+    inp, Lp = case_inputs(W.CONFIGS[4], request_ids=list(range(24)))
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 41)
+    load_h = W.fill_normal_np(inp.load_arena_bytes, 42)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    store_arena, _, _ = _mixed_run(lmc, inp, Lp, pool, torch.from_numpy(load_h).to(DEV))
+    # the oracle, in either order: the blocks are disjoint
+    assert oracle.load(Lo, C, pool_h, inp.tables_src, inp.load_jobs, load_h) == 0
+    store_o = np.zeros(inp.store_arena_bytes, dtype=np.uint8)
+    assert oracle.store(Lo, C, pool_h, inp.tables_src, inp.store_jobs, store_o) == 0
+    assert np.array_equal(pool.cpu().numpy(), pool_h)
+    assert np.array_equal(store_arena.cpu().numpy(), store_o)
+
+
+def test_full_size_mixed_two_streams(lmc):
+    """The full mixed step: 256 requests, 3 object groups (KDA, SWA-4096,
+    MLA), load of hits concurrent with the store of new chunks."""
+    cfg = W.CONFIGS[4]
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    rng = np.random.default_rng(4)
+    pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, 40)
+    load_arena = torch.empty(inp.load_arena_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(load_arena, 42)
+    store_arena, tabs, lj = _mixed_run(lmc, inp, Lp, pool, load_arena)
+    assert check_store_sampled(inp, pool, store_arena, inp.store_jobs, inp.tables_src,
+                               inp.store_arena_bytes, 8, rng) > 0
+    assert check_load_sampled(inp, pool, load_arena, inp.load_jobs, inp.tables_src,
+                              inp.load_arena_bytes, 8, rng) > 0
+    del store_arena
+    # storing the loaded chunks back reproduces the loaded objects
+    again = torch.empty_like(load_arena)
+    st = _status()
+    lmc.lmc_store(Lp, C, pool, tabs, lj, again, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(again, load_arena)
+    del again, load_arena
+    torch.cuda.empty_cache()
+    # every pool byte outside the loaded pages is the original pool's
+    ref = torch.empty_like(pool)
+    W.fill_normal(ref, 40)
+    pages, s0 = oracle.list_pages(Lo, C, inp.tables_src, inp.load_jobs, inp.load_arena_bytes)
+    assert s0 == 0
+    for pg in pages:
+        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
+        ref[lo:lo + n] = pool[lo:lo + n]
+    assert torch.equal(ref, pool)
