@@ -119,6 +119,14 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def _reduce_max(dist, values, device):
+    """Max over ranks of per-rank timings (the only cross-rank step)."""
+    import torch
+    t = torch.tensor(values, device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 def _dist():
     if int(os.environ.get("WORLD_SIZE", "1")) <= 1:
         return None, 0, 1, 0
@@ -304,10 +312,13 @@ class PagingStep:
         self.main.wait_event(ja)
         self.main.wait_event(jb)
 
-    def setup_e2e(self):
+    def setup_e2e(self, parts: int = 8):
         """Pinned host buffers for the end-to-end step: block tables and jobs
         go host -> device each step; objects leave the device for the host
-        cache tier (store) and come back from it (load)."""
+        cache tier (store) and come back from it (load). Plain workloads are
+        pipelined over `parts` request ranges so that a part's device -> host
+        copy overlaps the next part's store and its host -> device copy the
+        previous part's load."""
         T, inp = self.torch, self.inp
         pin = lambda a: T.from_numpy(np.ascontiguousarray(a)).pin_memory()
         self.h_tables = [pin(t) for t in inp.tables_src] + ([pin(t) for t in inp.tables_dst] if not self.cfg.mixed else [])
@@ -324,13 +335,34 @@ class PagingStep:
             self.d_jobs = self.jobs
             self.h_arena = T.empty(inp.arena_bytes, dtype=T.uint8, pin_memory=True)
             objs_in, objs_out = inp.arena_bytes, inp.arena_bytes
+            # request ranges -> (per-group job row ranges, arena byte range)
+            n = len(inp.lengths)
+            bounds = [round(k * n / parts) for k in range(parts + 1)]
+            self.parts = []
+            for a, b in zip(bounds[:-1], bounds[1:]):
+                if a == b:
+                    continue
+                rows, lo, hi = [], None, None
+                for g, J in enumerate(inp.jobs):
+                    sel = np.flatnonzero((J["request"] >= a) & (J["request"] < b))
+                    r0, r1 = (int(sel[0]), int(sel[-1]) + 1) if sel.size else (0, 0)
+                    rows.append((r0, r1))
+                    if sel.size:
+                        lo = int(J["offset"][r0]) if lo is None else min(lo, int(J["offset"][r0]))
+                        end = int(J["offset"][r1 - 1]) + int(inp.object_bytes[g])
+                        hi = end if hi is None else max(hi, end)
+                if lo is not None:
+                    self.parts.append((rows, lo, hi))
+            self.s_out = T.cuda.Stream(self.dev)
+            self.s_in = T.cuda.Stream(self.dev)
+            self.s_load = T.cuda.Stream(self.dev)
         self.h_status = T.zeros(1, dtype=T.int32, pin_memory=True)
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_tables) + \
             sum(j.numel() for j in self.h_jobs) + objs_in
         self.d2h = objs_out + 4
 
     def e2e_step(self):
-        lmc, L, C = self.lmc, self.L, self.C
+        lmc, L, C, T = self.lmc, self.L, self.C, self.torch
         for h, d in zip(self.h_tables, self.d_tables):
             d.copy_(h, non_blocking=True)
         for h, d in zip(self.h_jobs, self.d_jobs):
@@ -339,11 +371,31 @@ class PagingStep:
             self.load_arena.copy_(self.h_load, non_blocking=True)
             self.step()
             self.h_store.copy_(self.store_arena, non_blocking=True)
-        else:
-            lmc.lmc_store(L, C, self.pool, self.t_src, self.jobs, self.arena, self.status, self.main)
-            self.h_arena.copy_(self.arena, non_blocking=True)
-            self.arena.copy_(self.h_arena, non_blocking=True)
-            lmc.lmc_load(L, C, self.fresh, self.t_dst, self.jobs, self.arena, self.status, self.main)
+            self.h_status.copy_(self.status, non_blocking=True)
+            return
+        ready = T.cuda.Event()
+        ready.record(self.main)
+        self.s_load.wait_event(ready)
+        for rows, lo, hi in self.parts:
+            jobs = [j[16 * r0:16 * r1] for j, (r0, r1) in zip(self.jobs, rows)]
+            lmc.lmc_store(L, C, self.pool, self.t_src, jobs, self.arena, self.status, self.main)
+            stored = T.cuda.Event()
+            stored.record(self.main)
+            with T.cuda.stream(self.s_out):
+                self.s_out.wait_event(stored)
+                self.h_arena[lo:hi].copy_(self.arena[lo:hi], non_blocking=True)
+                out = T.cuda.Event()
+                out.record(self.s_out)
+            with T.cuda.stream(self.s_in):
+                self.s_in.wait_event(out)
+                self.arena[lo:hi].copy_(self.h_arena[lo:hi], non_blocking=True)
+                back = T.cuda.Event()
+                back.record(self.s_in)
+            self.s_load.wait_event(back)
+            lmc.lmc_load(L, C, self.fresh, self.t_dst, jobs, self.arena, self.status, self.s_load)
+        done = T.cuda.Event()
+        done.record(self.s_load)
+        self.main.wait_event(done)
         self.h_status.copy_(self.status, non_blocking=True)
 
 
@@ -408,9 +460,7 @@ def run_gpu(args):
 
     ms_per_step = total_ms / args.steps
     if dist is not None:
-        t = torch.tensor([ms_per_step, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step, e2e_ms = float(t[0]), float(t[1])
+        ms_per_step, e2e_ms = _reduce_max(dist, [ms_per_step, e2e_ms], dev)
     if rank != 0:
         dist.destroy_process_group()
         return
