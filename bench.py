@@ -494,7 +494,8 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic(dominant, cfg.index), "algorithmic_bytes_per_launch": dom_bytes},
+                     "traffic": _traffic(dominant, cfg.index) if args.requests is None else None,
+                     "algorithmic_bytes_per_launch": dom_bytes},
         "e2e": {"value": round(S.bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h},
         "gpu_launches": S.launches_per_step * args.steps,
