@@ -118,6 +118,18 @@ class _PageList(ctypes.Structure):
     _fields_ = [("pages", ctypes.c_void_p), ("capacity", ctypes.c_int64), ("count", ctypes.c_int64)]
 
 
+class _Pair(ctypes.Structure):
+    _fields_ = [("src_block", ctypes.c_int32), ("dst_block", ctypes.c_int32)]
+
+
+PAIR_DTYPE = np.dtype([("src_block", "<i4"), ("dst_block", "<i4")])
+
+
+class _CopyBatch(ctypes.Structure):
+    _fields_ = [("num_kv_groups", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("pairs", ctypes.POINTER(ctypes.POINTER(_Pair))), ("num_pairs", ctypes.POINTER(ctypes.c_int64))]
+
+
 class _Jobs(ctypes.Structure):
     _fields_ = [("num_object_groups", ctypes.c_int32), ("pad_", ctypes.c_int32),
                 ("jobs", ctypes.POINTER(ctypes.POINTER(_Job))),
@@ -136,6 +148,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                        P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
     lib.or_list_pages.argtypes = [P(_Layout), ctypes.c_int64, P(_Tables), P(_Jobs), ctypes.c_int64,
                                   P(ctypes.c_uint32), P(_PageList)]
+    lib.or_list_pages_any.argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P(_Tables),
+                                      P(_Jobs), ctypes.c_int64, P(ctypes.c_uint32), P(_PageList)]
+    lib.or_object_bytes_blocks.argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    lib.or_object_bytes_blocks.restype = ctypes.c_int64
+    for name in ("or_store_blocks", "or_load_blocks"):
+        getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, P(_Tables),
+                                       P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
+    lib.or_copy_blocks.argtypes = [P(_Layout), ctypes.c_void_p, P(_CopyBatch), P(ctypes.c_uint32)]
     lib.or_unified_block_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P(ctypes.c_int64)]
     return lib
 
@@ -212,6 +232,9 @@ class Layout:
 
     def object_bytes(self, C: int, og: int) -> int:
         return int(self._lib.or_object_bytes(ctypes.byref(self._c), int(C), int(og)))
+
+    def object_bytes_blocks(self, nb: int, kda_every: bool, og: int) -> int:
+        return int(self._lib.or_object_bytes_blocks(ctypes.byref(self._c), int(nb), int(bool(kda_every)), int(og)))
 
 
 def _fill_layout(spec_layers, N, packed, mem_bytes, split_groups, separate_object_groups) -> _Layout:
@@ -321,22 +344,70 @@ def load(L: Layout, C: int, pool: np.ndarray, tables, jobs, arena: np.ndarray) -
     return st.value
 
 
-def list_pages(L: Layout, C: int, tables, jobs, arena_bytes: int):
-    """The pages a store/load of `jobs` touches, as a PAGE_DTYPE array
-    (pool offset, arena offset, bytes, layer, block), plus the status bits."""
+def store_blocks(L: Layout, nb: int, kda_every: bool, pool: np.ndarray, tables, jobs, arena: np.ndarray) -> int:
+    """Block-granular store: each job's `chunk` field is its first block
+    position; every object covers `nb` blocks. Returns the status bits."""
+    assert pool.dtype == np.uint8 and arena.dtype == np.uint8 and arena.flags.writeable
     T, J, keep = _marshal(L, tables, jobs)
     st = ctypes.c_uint32(0)
-    pl = _PageList(None, 0, 0)
-    rc = L._lib.or_list_pages(ctypes.byref(L._c), int(C), ctypes.byref(T), ctypes.byref(J), int(arena_bytes),
-                              ctypes.byref(st), ctypes.byref(pl))
+    rc = L._lib.or_store_blocks(ctypes.byref(L._c), int(nb), int(bool(kda_every)), pool.ctypes.data,
+                                ctypes.byref(T), ctypes.byref(J), arena.ctypes.data, arena.size, ctypes.byref(st))
     if rc != OK:
-        raise OracleError(rc, "list_pages")
+        raise OracleError(rc, "store_blocks")
+    return st.value
+
+
+def load_blocks(L: Layout, nb: int, kda_every: bool, pool: np.ndarray, tables, jobs, arena: np.ndarray) -> int:
+    assert pool.dtype == np.uint8 and arena.dtype == np.uint8 and pool.flags.writeable
+    T, J, keep = _marshal(L, tables, jobs)
+    st = ctypes.c_uint32(0)
+    rc = L._lib.or_load_blocks(ctypes.byref(L._c), int(nb), int(bool(kda_every)), pool.ctypes.data,
+                               ctypes.byref(T), ctypes.byref(J), arena.ctypes.data, arena.size, ctypes.byref(st))
+    if rc != OK:
+        raise OracleError(rc, "load_blocks")
+    return st.value
+
+
+def copy_blocks(L: Layout, pool: np.ndarray, pairs) -> int:
+    """In-pool copies: pairs[g] is a PAIR_DTYPE array for KV group g."""
+    assert pool.dtype == np.uint8 and pool.flags.writeable and pool.size >= L.pool_bytes
+    g = L.num_kv_groups
+    if len(pairs) != g:
+        raise OracleError(ERR_INVALID_ARG, "one pair array per KV group is required")
+    ptrs = (ctypes.POINTER(_Pair) * g)()
+    counts = (ctypes.c_int64 * g)()
+    keep = []
+    for k, p in enumerate(pairs):
+        p = np.ascontiguousarray(p, dtype=PAIR_DTYPE)
+        keep.append(p)
+        ptrs[k] = p.ctypes.data_as(ctypes.POINTER(_Pair))
+        counts[k] = p.shape[0]
+    B = _CopyBatch(num_kv_groups=g, pairs=ptrs, num_pairs=counts)
+    st = ctypes.c_uint32(0)
+    rc = L._lib.or_copy_blocks(ctypes.byref(L._c), pool.ctypes.data, ctypes.byref(B), ctypes.byref(st))
+    if rc != OK:
+        raise OracleError(rc, "copy_blocks")
+    return st.value
+
+
+def list_pages(L: Layout, C: int, tables, jobs, arena_bytes: int, nb: int = 0, kda_every: bool = False):
+    """The pages a store/load of `jobs` touches, as a PAGE_DTYPE array
+    (pool offset, arena offset, bytes, layer, block), plus the status bits.
+    nb > 0 selects the block-granular form (C is then ignored)."""
+    T, J, keep = _marshal(L, tables, jobs)
+
+    def run(pl):
+        st = ctypes.c_uint32(0)
+        rc = L._lib.or_list_pages_any(ctypes.byref(L._c), int(C), int(nb), int(bool(kda_every)), ctypes.byref(T),
+                                      ctypes.byref(J), int(arena_bytes), ctypes.byref(st), ctypes.byref(pl))
+        if rc != OK:
+            raise OracleError(rc, "list_pages")
+        return st.value
+
+    pl = _PageList(None, 0, 0)
+    run(pl)
     out = np.zeros(pl.count, dtype=PAGE_DTYPE)
     pl = _PageList(out.ctypes.data, out.size, 0)
-    st = ctypes.c_uint32(0)
-    rc = L._lib.or_list_pages(ctypes.byref(L._c), int(C), ctypes.byref(T), ctypes.byref(J), int(arena_bytes),
-                              ctypes.byref(st), ctypes.byref(pl))
-    if rc != OK:
-        raise OracleError(rc, "list_pages")
+    st = run(pl)
     assert pl.count == out.size
-    return out, st.value
+    return out, st

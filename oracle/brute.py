@@ -115,40 +115,62 @@ class BruteLayout:
                           writeable=pool.flags.writeable)
 
 
-def _object_pieces(BL: BruteLayout, og_layers, tables, r, c, C):
-    """Yields (layer view index tuple, nbytes) in object order, one token at
-    a time for paged layers and one snapshot for KDA layers."""
+def _object_pieces(BL: BruteLayout, og_layers, tables, r, first_tok, ntok, kda_every=False):
+    """Yields (layer, view index tuple) in object order for the object that
+    covers tokens [first_tok, first_tok + ntok): one token at a time for
+    paged layers; for KDA layers the snapshot taken after the object's last
+    token, or, with kda_every, the snapshot after each of its blocks."""
     N = BL.N
     for i in og_layers:
         row = tables[BL.kv_group_of[i]][r]
         if BL.spec[i]["kind"] == "KDA":
-            # The state after the first (c+1)*C tokens lives in the block that
-            # ends at that token count.
-            end_tok = (c + 1) * C
-            yield i, (int(row[end_tok // N - 1]),)
+            ends = range(first_tok + N, first_tok + ntok + 1, N) if kda_every else [first_tok + ntok]
+            for end_tok in ends:
+                # the state after `end_tok` tokens lives in the block ending there
+                yield i, (int(row[end_tok // N - 1]),)
         else:
-            for t in range(c * C, (c + 1) * C):
+            for t in range(first_tok, first_tok + ntok):
                 yield i, (int(row[t // N]), t % N)
 
 
-def store(BL: BruteLayout, C, pool, tables, jobs, arena, separate=True):
+def _span(BL, job, C, nb):
+    """Token range of a job: chunk jobs cover chunk * C .. + C; block jobs
+    (nb > 0) cover their first block's tokens onward for nb blocks."""
+    if nb:
+        return int(job["chunk"]) * BL.N, nb * BL.N
+    return int(job["chunk"]) * C, C
+
+
+def store(BL: BruteLayout, C, pool, tables, jobs, arena, separate=True, nb=0, kda_every=False):
     ogs = object_groups(BL.spec, separate)
     for og, layers in enumerate(ogs):
         for job in jobs[og]:
+            first, n = _span(BL, job, C, nb)
             parts = [BL.view(pool, i)[idx].reshape(-1)
-                     for i, idx in _object_pieces(BL, layers, tables, int(job["request"]), int(job["chunk"]), C)]
+                     for i, idx in _object_pieces(BL, layers, tables, int(job["request"]), first, n, kda_every)]
             blob = np.concatenate(parts)
             off = int(job["offset"])
             arena[off:off + blob.size] = blob
 
 
-def load(BL: BruteLayout, C, pool, tables, jobs, arena, separate=True):
+def load(BL: BruteLayout, C, pool, tables, jobs, arena, separate=True, nb=0, kda_every=False):
     ogs = object_groups(BL.spec, separate)
     for og, layers in enumerate(ogs):
         for job in jobs[og]:
+            first, n = _span(BL, job, C, nb)
             cur = int(job["offset"])
-            for i, idx in _object_pieces(BL, layers, tables, int(job["request"]), int(job["chunk"]), C):
+            for i, idx in _object_pieces(BL, layers, tables, int(job["request"]), first, n, kda_every):
                 v = BL.view(pool, i)
-                n = v[idx].size
-                v[idx] = arena[cur:cur + n].reshape(v[idx].shape)
-                cur += n
+                k = v[idx].size
+                v[idx] = arena[cur:cur + k].reshape(v[idx].shape)
+                cur += k
+
+
+def copy_blocks(BL: BruteLayout, pool, pairs):
+    """pairs[g]: (src, dst) block pairs of KV group g; every layer's view row
+    dst takes row src."""
+    for g, P in enumerate(pairs):
+        for p in P:
+            for i in BL.groups[g]:
+                v = BL.view(pool, i)
+                v[int(p["dst_block"])] = v[int(p["src_block"])].copy()

@@ -297,22 +297,34 @@ int or_layout_build(or_layout *L)
     return OR_OK;
 }
 
-/* Bytes of one object of group og for chunk size C: the group's layers in
- * model order; a paged layer holds the C tokens of the chunk (C/N pages),
- * a KDA layer holds one state snapshot. */
-int64_t or_object_bytes(const or_layout *L, int64_t C, int og)
+/* Bytes of one object of group og covering nb consecutive blocks: the
+ * group's layers in model order; a paged layer holds all nb pages (the
+ * object's tokens), a KDA layer one state snapshot (the last block's), or
+ * nb snapshots (one per block) when kda_every is set. */
+static int64_t object_bytes_nb(const or_layout *L, int64_t nb, int kda_every, int og)
 {
-    int64_t m = C / L->N;
     int64_t total = 0;
     for (int i = 0; i < L->num_layers; i++) {
         if (L->object_group[i] != og)
             continue;
-        if (L->layers[i].kind == OR_KDA)
+        if (L->layers[i].kind == OR_KDA && !kda_every)
             total += L->real_bytes[i];
         else
-            total += m * L->real_bytes[i];
+            total += nb * L->real_bytes[i];
     }
     return total;
+}
+
+/* Bytes of one object of group og for chunk size C (C / N blocks). */
+int64_t or_object_bytes(const or_layout *L, int64_t C, int og)
+{
+    return object_bytes_nb(L, C / L->N, 0, og);
+}
+
+/* Bytes of one object of group og for a block-granular call. */
+int64_t or_object_bytes_blocks(const or_layout *L, int64_t nb, int kda_every, int og)
+{
+    return object_bytes_nb(L, nb, kda_every, og);
 }
 
 /* ------------------------------------------------------------------ */
@@ -361,25 +373,32 @@ static int check_tables(const or_layout *L, const or_tables *T)
     return OR_OK;
 }
 
+/* How the jobs of one call map to block positions: an object covers nb
+ * consecutive positions starting at `first`, where first = chunk * nb for
+ * chunk jobs and the job's own value for block jobs. */
+typedef struct {
+    int64_t nb;
+    int first_is_block;
+    int kda_every;
+} obj_shape;
+
 /* Moves every object of every job, in either direction. */
-static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
+static int move_objects(const or_layout *L, const obj_shape *sh, uint8_t *pool,
                         const or_tables *T, const or_jobs *J,
                         uint8_t *arena, int64_t arena_bytes, uint32_t *status,
                         int to_object, or_page_list *list)
 {
     if (L == NULL || (pool == NULL && list == NULL) || J == NULL || status == NULL)
         return OR_ERR_INVALID_ARG;
-    if (C <= 0 || C % L->N != 0)
-        return OR_ERR_NOT_MULTIPLE;
     int rc = check_tables(L, T);
     if (rc != OR_OK)
         return rc;
     if (J->num_object_groups != L->num_object_groups)
         return OR_ERR_INVALID_ARG;
-    int64_t m = C / L->N;
+    int64_t nb = sh->nb;
 
     for (int og = 0; og < L->num_object_groups; og++) {
-        int64_t obj_size = or_object_bytes(L, C, og);
+        int64_t obj_size = object_bytes_nb(L, nb, sh->kda_every, og);
         for (int64_t q = 0; q < J->num_jobs[og]; q++) {
             const or_job *job = &J->jobs[og][q];
             int64_t r = job->request;
@@ -392,6 +411,7 @@ static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
                 *status |= OR_ST_BAD_JOB;
                 continue;
             }
+            int64_t first = sh->first_is_block ? c : c * nb;
             uint8_t *obj = arena == NULL ? NULL : arena + job->offset;
             int64_t cursor = 0;
             for (int i = 0; i < L->num_layers; i++) {
@@ -399,11 +419,11 @@ static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
                     continue;
                 int k = L->kv_group[i];
                 const int32_t *row = T->table[k] + r * T->row_stride[k];
-                if (L->layers[i].kind == OR_KDA) {
+                if (L->layers[i].kind == OR_KDA && !sh->kda_every) {
                     /* The state a restore resumes from is the snapshot
-                     * taken at the end of the chunk's last block ([KL]
+                     * taken at the end of the object's last block ([KL]
                      * "Why these settings"; [MC] checkpoint boundaries). */
-                    int64_t pos = (c + 1) * m - 1;
+                    int64_t pos = first + nb - 1;
                     if (pos >= T->num_cols[k])
                         *status |= OR_ST_BAD_JOB;
                     else
@@ -411,10 +431,23 @@ static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
                                              to_object, OR_ST_NO_SNAPSHOT, list,
                                              job->offset + cursor);
                     cursor += L->real_bytes[i];
+                } else if (L->layers[i].kind == OR_KDA) {
+                    /* One snapshot per block boundary ([VB] §7, "all"-style
+                     * snapshots kept per object). */
+                    for (int64_t s = 0; s < nb; s++) {
+                        int64_t pos = first + s;
+                        if (pos >= T->num_cols[k])
+                            *status |= OR_ST_BAD_JOB;
+                        else
+                            *status |= copy_page(L, i, row[pos], pool, obj + cursor,
+                                                 to_object, OR_ST_NO_SNAPSHOT, list,
+                                                 job->offset + cursor);
+                        cursor += L->real_bytes[i];
+                    }
                 } else {
-                    /* The chunk's C tokens are its m consecutive blocks. */
-                    for (int64_t j = 0; j < m; j++) {
-                        int64_t pos = c * m + j;
+                    /* The object's tokens are its nb consecutive blocks. */
+                    for (int64_t j = 0; j < nb; j++) {
+                        int64_t pos = first + j;
                         if (pos >= T->num_cols[k])
                             *status |= OR_ST_BAD_JOB;
                         else
@@ -430,36 +463,145 @@ static int move_objects(const or_layout *L, int64_t C, uint8_t *pool,
     return OR_OK;
 }
 
+static int chunk_shape(const or_layout *L, int64_t C, obj_shape *sh)
+{
+    if (L == NULL)
+        return OR_ERR_INVALID_ARG;
+    if (C <= 0 || C % L->N != 0)
+        return OR_ERR_NOT_MULTIPLE;
+    sh->nb = C / L->N;
+    sh->first_is_block = 0;
+    sh->kda_every = 0;
+    return OR_OK;
+}
+
+static int block_shape(int64_t nb, int kda_every, obj_shape *sh)
+{
+    if (nb <= 0 || (kda_every != 0 && kda_every != 1))
+        return OR_ERR_INVALID_ARG;
+    sh->nb = nb;
+    sh->first_is_block = 1;
+    sh->kda_every = kda_every;
+    return OR_OK;
+}
+
 int or_store(const or_layout *L, int64_t C, const uint8_t *pool,
              const or_tables *T, const or_jobs *J,
              uint8_t *arena, int64_t arena_bytes, uint32_t *status)
 {
+    obj_shape sh;
+    int rc = chunk_shape(L, C, &sh);
+    if (rc != OR_OK)
+        return rc;
     if (arena == NULL)
         return OR_ERR_INVALID_ARG;
-    return move_objects(L, C, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1, NULL);
+    return move_objects(L, &sh, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1, NULL);
 }
 
 int or_load(const or_layout *L, int64_t C, uint8_t *pool,
             const or_tables *T, const or_jobs *J,
             const uint8_t *arena, int64_t arena_bytes, uint32_t *status)
 {
+    obj_shape sh;
+    int rc = chunk_shape(L, C, &sh);
+    if (rc != OR_OK)
+        return rc;
     if (arena == NULL)
         return OR_ERR_INVALID_ARG;
-    return move_objects(L, C, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0, NULL);
+    return move_objects(L, &sh, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0, NULL);
+}
+
+/* Block-granular store/load: every object covers nb consecutive block
+ * positions from the job's own first position (its `chunk` field), e.g. the
+ * whole blocks past a request's last whole chunk, or a chunk's blocks with
+ * one KDA snapshot per block (kda_every). */
+int or_store_blocks(const or_layout *L, int64_t nb, int kda_every, const uint8_t *pool,
+                    const or_tables *T, const or_jobs *J,
+                    uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    obj_shape sh;
+    int rc = block_shape(nb, kda_every, &sh);
+    if (rc != OR_OK)
+        return rc;
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    return move_objects(L, &sh, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1, NULL);
+}
+
+int or_load_blocks(const or_layout *L, int64_t nb, int kda_every, uint8_t *pool,
+                   const or_tables *T, const or_jobs *J,
+                   const uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    obj_shape sh;
+    int rc = block_shape(nb, kda_every, &sh);
+    if (rc != OR_OK)
+        return rc;
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    return move_objects(L, &sh, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0, NULL);
 }
 
 /* The pages a store or load of the jobs touches, in the order it touches
  * them, without moving bytes: pool offset, object offset (arena-relative)
  * and length of each. Used to check large cases one object at a time.
  * Returns OR_OK and sets list->count to the number of pages (records past
- * list->capacity are counted but not written). */
-int or_list_pages(const or_layout *L, int64_t C, const or_tables *T, const or_jobs *J,
-                  int64_t arena_bytes, uint32_t *status, or_page_list *list)
+ * list->capacity are counted but not written). nb <= 0 selects the chunk
+ * form with chunk size C; otherwise the block form. */
+int or_list_pages_any(const or_layout *L, int64_t C, int64_t nb, int kda_every,
+                      const or_tables *T, const or_jobs *J,
+                      int64_t arena_bytes, uint32_t *status, or_page_list *list)
 {
     if (list == NULL || (list->capacity > 0 && list->pages == NULL))
         return OR_ERR_INVALID_ARG;
+    obj_shape sh;
+    int rc = nb <= 0 ? chunk_shape(L, C, &sh) : block_shape(nb, kda_every, &sh);
+    if (rc != OR_OK)
+        return rc;
     list->count = 0;
-    return move_objects(L, C, NULL, T, J, NULL, arena_bytes, status, 1, list);
+    return move_objects(L, &sh, NULL, T, J, NULL, arena_bytes, status, 1, list);
+}
+
+int or_list_pages(const or_layout *L, int64_t C, const or_tables *T, const or_jobs *J,
+                  int64_t arena_bytes, uint32_t *status, or_page_list *list)
+{
+    return or_list_pages_any(L, C, 0, 0, T, J, arena_bytes, status, list);
+}
+
+/* In-pool block copies ([MC] "Copy-on-Write", "Snapshot": a shared
+ * checkpoint's state is copied into a private slot, a running state into a
+ * spare buffer). For every pair of KV group g, each layer of g gets the real
+ * bytes of block src copied to block dst. A pair naming -1 or a block outside
+ * the pool is skipped and raises its bit. */
+int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, uint32_t *status)
+{
+    if (L == NULL || pool == NULL || B == NULL || status == NULL ||
+        B->num_kv_groups != L->num_kv_groups)
+        return OR_ERR_INVALID_ARG;
+    for (int g = 0; g < L->num_kv_groups; g++) {
+        if (B->num_pairs[g] < 0 || (B->num_pairs[g] > 0 && B->pairs[g] == NULL))
+            return OR_ERR_INVALID_ARG;
+    }
+    for (int g = 0; g < L->num_kv_groups; g++) {
+        for (int64_t q = 0; q < B->num_pairs[g]; q++) {
+            int64_t src = B->pairs[g][q].src_block;
+            int64_t dst = B->pairs[g][q].dst_block;
+            if (src == -1 || dst == -1) {
+                *status |= OR_ST_NO_BLOCK;
+                continue;
+            }
+            if (src < 0 || src >= L->num_blocks || dst < 0 || dst >= L->num_blocks) {
+                *status |= OR_ST_BLOCK_OOR;
+                continue;
+            }
+            for (int i = 0; i < L->num_layers; i++) {
+                if (L->kv_group[i] != g)
+                    continue;
+                memmove(pool + L->base[i] + dst * L->stride[i],
+                        pool + L->base[i] + src * L->stride[i], (size_t)L->real_bytes[i]);
+            }
+        }
+    }
+    return OR_OK;
 }
 
 /* Smallest multiple of `align` tokens whose attention page

@@ -114,6 +114,30 @@ int or_load(const or_layout *L, int64_t C, uint8_t *pool,
 
 int or_list_pages(const or_layout *L, int64_t C, const or_tables *T, const or_jobs *J,
                   int64_t arena_bytes, uint32_t *status, or_page_list *list);
+int or_list_pages_any(const or_layout *L, int64_t C, int64_t nb, int kda_every,
+                      const or_tables *T, const or_jobs *J,
+                      int64_t arena_bytes, uint32_t *status, or_page_list *list);
+int64_t or_object_bytes_blocks(const or_layout *L, int64_t nb, int kda_every, int og);
+int or_store_blocks(const or_layout *L, int64_t nb, int kda_every, const uint8_t *pool,
+                    const or_tables *T, const or_jobs *J,
+                    uint8_t *arena, int64_t arena_bytes, uint32_t *status);
+int or_load_blocks(const or_layout *L, int64_t nb, int kda_every, uint8_t *pool,
+                   const or_tables *T, const or_jobs *J,
+                   const uint8_t *arena, int64_t arena_bytes, uint32_t *status);
+
+typedef struct {
+    int32_t src_block;
+    int32_t dst_block;
+} or_pair;
+
+typedef struct {
+    int32_t num_kv_groups;
+    int32_t pad_;
+    const or_pair *const *pairs; /* [kv group] -> pair array */
+    const int64_t *num_pairs;    /* [kv group] */
+} or_copy_batch;
+
+int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, uint32_t *status);
 int or_unified_block_size(int64_t attn_token_bytes, int64_t state_page_bytes,
                           int64_t align, int64_t *out);
 

@@ -398,9 +398,137 @@ def check_errors(lib, case):
         assert oracle.store(L, C, pool, case["t_src"], J, a) & oracle.ST_BAD_JOB, bad
 
 
+def _block_jobs(units, sizes):
+    """units[og] = list of (request, first block); packed like chunk jobs."""
+    return W.pack_jobs(units, sizes)
+
+
+def check_block_objects(lib):
+    cfg0 = W.CONFIGS[0]
+    # chunk 150 -> 192 (3 blocks): requests of 300 and 517 tokens leave 1 and
+    # 2 whole tail blocks past their last whole chunk
+    _check_block_objects(lib, tiny_case(lib, spec=cfg0.layers, N=64, req_chunk=150, packed=False,
+                                        lengths=[300, 517], seed=3))
+    rng = np.random.default_rng(13)
+    for t in range(4):
+        spec = random_spec(rng, int(rng.integers(2, 7)))
+        spec[0] = W.mla(int(rng.choice([16, 32])))
+        spec[-1] = {"kind": "KDA", "token_bytes": 0, "conv_bytes": 48, "rec_bytes": 256, "window": 0}
+        lengths = [int(x) for x in rng.integers(20, 90, size=3)]
+        _check_block_objects(lib, tiny_case(lib, spec=spec, N=4, req_chunk=12, packed=bool(t % 2),
+                                            lengths=lengths, seed=t, split=bool(t // 2)))
+
+
+def _check_block_objects(lib, case):
+    """Block-granular objects: (1) nb = C/N blocks from chunk * m with the
+    last-block snapshot are exactly the chunk objects; (2) tail objects (whole
+    blocks past the last whole chunk) and (3) chunk objects with one snapshot
+    per block agree with the per-token brute force, and load inverts store."""
+    L, C = case["L"], case["C"]
+    m = C // L.N
+    pool, lengths = case["pool"], case["lengths"]
+    B = brute.BruteLayout(L_spec(case), L.N, L.packed, L.pool_bytes, case["split"])
+    og_n = L.num_object_groups
+    # (1) the chunk form as a special case of the block form
+    arena_c = np.zeros(case["arena_bytes"], dtype=np.uint8)
+    assert oracle.store(L, C, pool, case["t_src"], case["jobs"], arena_c) == 0
+    jb = [j.copy() for j in case["jobs"]]
+    for j in jb:
+        j["chunk"] = j["chunk"] * m
+    arena_b = np.zeros_like(arena_c)
+    assert oracle.store_blocks(L, m, False, pool, case["t_src"], jb, arena_b) == 0
+    assert np.array_equal(arena_c, arena_b), "block form with nb = C/N differs from the chunk form"
+    # (2) tails and (3) every-block snapshots
+    tails = {}
+    for r, Lr in enumerate(lengths):
+        full_blocks = int(Lr) // L.N
+        t = full_blocks - (int(Lr) // C) * m
+        if t > 0:
+            tails.setdefault(t, []).append((r, (int(Lr) // C) * m))
+    shapes = [(nb, False, [units] * og_n) for nb, units in tails.items()]
+    shapes.append((m, True, [[(r, c * m) for r, Lr in enumerate(lengths) for c in range(int(Lr) // C)]] * og_n))
+    for nb, every, units in shapes:
+        sizes = [L.object_bytes_blocks(nb, every, g) for g in range(og_n)]
+        if every:
+            kda_og = [L.object_group[i] for i in range(len(L.kinds)) if L.kinds[i] == "KDA"]
+            for g in set(kda_og):
+                assert sizes[g] == nb * sum(L.real_bytes[i] for i in range(len(L.kinds))
+                                            if L.object_group[i] == g)
+        jobs, nbytes = _block_jobs(units, sizes)
+        arena = np.zeros(nbytes, dtype=np.uint8)
+        assert oracle.store_blocks(L, nb, every, pool, case["t_src"], jobs, arena) == 0
+        arena_brute = np.zeros_like(arena)
+        brute.store(B, C, pool, case["t_src"], jobs, arena_brute, case["separate"], nb=nb, kda_every=every)
+        assert np.array_equal(arena, arena_brute), ("block store differs from the brute force", nb, every)
+        dst = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        assert oracle.load_blocks(L, nb, every, dst, case["t_dst"], jobs, arena) == 0
+        dst_b = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        brute.load(B, C, dst_b, case["t_dst"], jobs, arena, case["separate"], nb=nb, kda_every=every)
+        assert np.array_equal(dst, dst_b), ("block load differs from the brute force", nb, every)
+        again = np.zeros_like(arena)
+        assert oracle.store_blocks(L, nb, every, dst, case["t_dst"], jobs, again) == 0
+        assert np.array_equal(arena, again)
+        pages, st = oracle.list_pages(L, C, case["t_dst"], jobs, nbytes, nb=nb, kda_every=every)
+        assert st == 0 and int(pages["bytes"].sum()) == sum(sizes[g] * len(j) for g, j in enumerate(jobs))
+    assert len(shapes) >= 2
+
+
+def check_copy_blocks(lib):
+    """In-pool block copies agree with the brute force; the destination pages
+    equal the source pages; no other byte changes; bad ids raise bits."""
+    rng = np.random.default_rng(21)
+    for t in range(10):
+        spec = random_spec(rng, int(rng.integers(2, 8)))
+        N = int(rng.choice([2, 4, 8]))
+        try:
+            L = oracle.layout(spec, N, bool(t % 2), int(rng.integers(20000, 60000)), split_groups=bool(t % 3),
+                              _lib=lib)
+        except oracle.OracleError:
+            continue
+        if L.num_blocks < 4:
+            continue
+        pool = W.fill_normal_np(L.pool_bytes, t)
+        perm = rng.permutation(L.num_blocks)
+        half = L.num_blocks // 2
+        pairs = []
+        for g in range(L.num_kv_groups):
+            k = int(rng.integers(0, half // L.num_kv_groups + 1))
+            src = perm[:half][rng.choice(half, k, replace=False)] if k else np.zeros(0, int)
+            dst = perm[half:][g * (half // L.num_kv_groups):][:k]
+            pairs.append(np.array(list(zip(src, dst)), dtype=oracle.PAIR_DTYPE))
+        out = pool.copy()
+        assert oracle.copy_blocks(L, out, pairs) == 0
+        B = brute.BruteLayout(spec, N, L.packed, L.pool_bytes, bool(t % 3))
+        ref = pool.copy()
+        brute.copy_blocks(B, ref, pairs)
+        assert np.array_equal(out, ref), "copy differs from the brute force"
+        changed = np.zeros(L.pool_bytes, dtype=bool)
+        for g, P in enumerate(pairs):
+            for p in P:
+                for i in range(len(spec)):
+                    if L.kv_group[i] == g:
+                        s0 = L.base[i] + int(p["src_block"]) * L.stride[i]
+                        d0 = L.base[i] + int(p["dst_block"]) * L.stride[i]
+                        n = L.real_bytes[i]
+                        assert np.array_equal(out[d0:d0 + n], pool[s0:s0 + n])
+                        changed[d0:d0 + n] = True
+        assert np.array_equal(out[~changed], pool[~changed])
+    L = oracle.layout(W.CONFIGS[0].layers, 64, False, 64 * 73_728, _lib=lib)
+    pool = W.fill_normal_np(L.pool_bytes, 1)
+    for bad, bit in (((-1, 3), oracle.ST_NO_BLOCK), ((3, L.num_blocks), oracle.ST_BLOCK_OOR),
+                     ((-5, 3), oracle.ST_BLOCK_OOR)):
+        pairs = [np.zeros(0, dtype=oracle.PAIR_DTYPE) for _ in range(L.num_kv_groups)]
+        pairs[1] = np.array([bad, (7, 8)], dtype=oracle.PAIR_DTYPE)
+        out = pool.copy()
+        assert oracle.copy_blocks(L, out, pairs) == bit
+        ref = pool.copy()
+        oracle.copy_blocks(L, ref, [pairs[0], pairs[1][1:], pairs[2], pairs[3]])
+        assert np.array_equal(out, ref), "a bad pair must skip only itself"
+
+
 ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",
        "check_budget", "check_page_formulas", "check_unified_block_size", "check_k3_groups", "check_closed_forms",
-       "check_non_overlap", "check_store_load_cases"]
+       "check_non_overlap", "check_store_load_cases", "check_block_objects", "check_copy_blocks"]
 
 
 def check_store_load_cases(lib):

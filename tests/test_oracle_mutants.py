@@ -27,13 +27,20 @@ MUTANTS = [
     ("packed offset counted after the page", "offset_in_group[i] = group_total[k];\n                        group_total[k] += L->real_bytes[i];",
      "group_total[k] += L->real_bytes[i];\n                        offset_in_group[i] = group_total[k] - L->real_bytes[0];"),
     ("packed stride is the first group's", "if (group_total[k] > stride)", "if (k == 0)"),
-    ("KDA snapshot from the chunk's first block", "int64_t pos = (c + 1) * m - 1;", "int64_t pos = c * m;"),
-    ("paged blocks reversed in the object", "int64_t pos = c * m + j;", "int64_t pos = c * m + (m - 1 - j);"),
+    ("KDA snapshot from the object's first block", "int64_t pos = first + nb - 1;", "int64_t pos = first;"),
+    ("paged blocks reversed in the object", "int64_t pos = first + j;", "int64_t pos = first + (nb - 1 - j);"),
+    ("every-block snapshots all from the last block", "int64_t pos = first + s;", "int64_t pos = first + nb - 1;"),
+    ("block jobs start at chunk * nb", "int64_t first = sh->first_is_block ? c : c * nb;", "int64_t first = c * nb;"),
+    ("copy writes the source", "memmove(pool + L->base[i] + dst * L->stride[i],\n                        pool + L->base[i] + src * L->stride[i]",
+     "memmove(pool + L->base[i] + src * L->stride[i],\n                        pool + L->base[i] + dst * L->stride[i]"),
+    ("copy skips a group's last layer", "                if (L->kv_group[i] != g)\n                    continue;\n                memmove",
+     "                if (L->kv_group[i] != g || i == L->num_layers - 1)\n                    continue;\n                memmove"),
+    ("copy accepts block ids past the pool", "dst < 0 || dst >= L->num_blocks", "dst < 0 || dst > L->num_blocks + 1000000"),
     ("page copy one byte short", "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer]);",
      "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer] - 1);"),
     ("misaligned object offsets accepted", "job->offset % 16 != 0 ||", ""),
     ("block id upper bound off by one", "block >= L->num_blocks", "block > L->num_blocks"),
-    ("object size counts KDA per block", "        if (L->layers[i].kind == OR_KDA)\n            total += L->real_bytes[i];",
+    ("object size counts KDA per block", "        if (L->layers[i].kind == OR_KDA && !kda_every)\n            total += L->real_bytes[i];",
      "        if (0)\n            total += L->real_bytes[i];"),
 ]
 
