@@ -119,6 +119,10 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def _gbs(nbytes, ms):
+    return round(nbytes / (ms * 1e-3) / 1e9, 2) if nbytes and ms > 0 else None
+
+
 def _reduce_max(dist, values, device):
     """Max over ranks of per-rank timings (the only cross-rank step)."""
     import torch
@@ -240,11 +244,20 @@ class PagingStep:
     (one pool): the load of cached chunks and the store of new chunks,
     issued concurrently on two streams that touch disjoint blocks."""
 
-    def __init__(self, lmc, torch, cfg, dev, rank, ids):
-        self.lmc, self.torch, self.cfg, self.dev = lmc, torch, cfg, dev
+    def __init__(self, lmc, torch, cfg, dev, rank, ids, op="paging"):
+        self.lmc, self.torch, self.cfg, self.dev, self.op = lmc, torch, cfg, dev, op
         C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
         build = functools.partial(lmc.lmc_layout_build, cfg.layers, cfg.N, cfg.packed)
         inp = W.make_inputs(cfg, build, C, ids)
+        if op == "blocks":
+            # the same chunks as block-granular objects holding one KDA
+            # snapshot per block (every block boundary of the chunk)
+            m = C // cfg.N
+            units = [[(int(j["request"]), int(j["chunk"]) * m) for j in J] for J in inp.jobs]
+            inp.object_bytes = [inp.layout.object_bytes_blocks(m, True, g)
+                                for g in range(inp.layout.num_object_groups)]
+            inp.jobs, inp.arena_bytes = W.pack_jobs(units, inp.object_bytes)
+            self.nb = m
         self.inp, self.L, self.C = inp, inp.layout, C
         L = self.L
         T = torch
@@ -277,6 +290,22 @@ class PagingStep:
         # every payload byte is read once and written once, by the store and by the load
         self.bytes_per_step = 2 * (self.load_payload + self.store_payload)
 
+    def _store(self, pool, tables, jobs):
+        lmc = self.lmc
+        if self.op == "blocks":
+            lmc.lmc_store_blocks(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, pool, tables, jobs, self.arena,
+                                 self.status, self.main)
+        else:
+            lmc.lmc_store(self.L, self.C, pool, tables, jobs, self.arena, self.status, self.main)
+
+    def _load(self, pool, tables, jobs, stream):
+        lmc = self.lmc
+        if self.op == "blocks":
+            lmc.lmc_load_blocks(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, pool, tables, jobs, self.arena,
+                                self.status, stream)
+        else:
+            lmc.lmc_load(self.L, self.C, pool, tables, jobs, self.arena, self.status, stream)
+
     def new_events(self):
         E = self.torch.cuda.Event
         return [E(enable_timing=True) for _ in range(4)]
@@ -286,11 +315,11 @@ class PagingStep:
         if not self.cfg.mixed:
             if ev is not None:
                 ev[0].record(self.main)
-            lmc.lmc_store(L, C, self.pool, self.t_src, self.jobs, self.arena, self.status, self.main)
+            self._store(self.pool, self.t_src, self.jobs)
             if ev is not None:
                 ev[1].record(self.main)
                 ev[2].record(self.main)
-            lmc.lmc_load(L, C, self.fresh, self.t_dst, self.jobs, self.arena, self.status, self.main)
+            self._load(self.fresh, self.t_dst, self.jobs, self.main)
             if ev is not None:
                 ev[3].record(self.main)
             return
@@ -378,7 +407,7 @@ class PagingStep:
         self.s_load.wait_event(ready)
         for rows, lo, hi in self.parts:
             jobs = [j[16 * r0:16 * r1] for j, (r0, r1) in zip(self.jobs, rows)]
-            lmc.lmc_store(L, C, self.pool, self.t_src, jobs, self.arena, self.status, self.main)
+            self._store(self.pool, self.t_src, jobs)
             stored = T.cuda.Event()
             stored.record(self.main)
             with T.cuda.stream(self.s_out):
@@ -392,10 +421,72 @@ class PagingStep:
                 back = T.cuda.Event()
                 back.record(self.s_in)
             self.s_load.wait_event(back)
-            lmc.lmc_load(L, C, self.fresh, self.t_dst, jobs, self.arena, self.status, self.s_load)
+            self._load(self.fresh, self.t_dst, jobs, self.s_load)
         done = T.cuda.Event()
         done.record(self.s_load)
         self.main.wait_event(done)
+        self.h_status.copy_(self.status, non_blocking=True)
+
+
+class CopyStep:
+    """In-pool copy-on-write of every KDA snapshot of the batch: one pair per
+    (KDA group, request, snapshot) from the batch's block to a spare block of
+    a pool twice the batch's size."""
+
+    launches_per_step = 1
+
+    def __init__(self, lmc, torch, cfg, dev, rank, ids):
+        self.lmc, self.torch, self.cfg, self.dev = lmc, torch, cfg, dev
+        C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
+        build = functools.partial(lmc.lmc_layout_build, cfg.layers, cfg.N, cfg.packed)
+        inp = W.make_inputs(cfg, build, C, ids)
+        need = inp.layout.num_blocks
+        per_block = inp.layout.pool_bytes // need
+        self.L = L = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, 2 * need * per_block)
+        self.C, self.inp = C, inp
+        pairs, nxt, moved = [], need, 0
+        for g, kind in enumerate(L.kv_group_kind):
+            t = inp.tables_src[g]
+            src = t[t >= 0] if kind == "KDA" else np.zeros(0, np.int32)
+            pairs.append(np.array([(int(x), nxt + i) for i, x in enumerate(src)],
+                                  dtype=lmc.PAIR_DTYPE).reshape(-1))
+            nxt += len(src)
+            moved += len(src) * sum(L.real_bytes[i] for i in range(L.num_layers) if L.kv_group[i] == g)
+        T = torch
+        self.main = T.cuda.current_stream(dev)
+        self.pool = T.empty(L.pool_bytes, dtype=T.uint8, device=dev)
+        W.fill_normal(self.pool, cfg.seed + 101 * rank)
+        self.status = T.zeros(1, dtype=T.int32, device=dev)
+        self.pairs = [lmc.pairs_to_device(p, dev) for p in pairs]
+        self.h_pairs = pairs
+        self.store_payload, self.load_payload = moved, 0
+        self.bytes_per_step = 2 * moved
+        self.chunks = sum(len(p) for p in pairs)
+
+    def new_events(self):
+        E = self.torch.cuda.Event
+        return [E(enable_timing=True) for _ in range(4)]
+
+    def step(self, ev=None):
+        if ev is not None:
+            ev[0].record(self.main)
+        self.lmc.lmc_copy_blocks(self.L, self.pool, self.pairs, self.status, self.main)
+        if ev is not None:
+            ev[1].record(self.main)
+            ev[2].record(self.main)
+            ev[3].record(self.main)
+
+    def setup_e2e(self):
+        T = self.torch
+        self.h_p = [T.from_numpy(np.ascontiguousarray(p).view(np.uint8)).pin_memory() for p in self.h_pairs]
+        self.h_status = T.zeros(1, dtype=T.int32, pin_memory=True)
+        self.h2d = sum(p.numel() for p in self.h_p)
+        self.d2h = 4
+
+    def e2e_step(self):
+        for h, d in zip(self.h_p, self.pairs):
+            d.copy_(h, non_blocking=True)
+        self.step()
         self.h_status.copy_(self.status, non_blocking=True)
 
 
@@ -414,7 +505,10 @@ def run_gpu(args):
     if cfg.waves > 1 and args.requests is None:
         n_req = cfg.num_requests // cfg.waves  # one wave fits the device; the step is one wave
     # each rank runs its own independent copy of the batch (weak scaling)
-    S = PagingStep(lmc, torch, cfg, dev, rank, list(range(n_req)))
+    if args.op == "copy":
+        S = CopyStep(lmc, torch, cfg, dev, rank, list(range(n_req)))
+    else:
+        S = PagingStep(lmc, torch, cfg, dev, rank, list(range(n_req)), args.op)
     L = S.L
 
     def barrier():
@@ -468,7 +562,9 @@ def run_gpu(args):
     value = S.bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = _peaks()
     st_avg, ld_avg = statistics.mean(store_ms), statistics.mean(load_ms)
-    if cfg.mixed:
+    if args.op == "copy":
+        dominant, dom_bytes, dom_ms = "copy", S.bytes_per_step, st_avg
+    elif cfg.mixed:
         # the two kernels share HBM concurrently: the roofline is the step's
         dominant, dom_bytes, dom_ms = "store+load (concurrent)", S.bytes_per_step, ms_per_step
     elif st_avg >= ld_avg:
@@ -480,7 +576,7 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": cfg.name, "index": cfg.index, "requests": n_req,
+        "config": {"workload": cfg.name, "index": cfg.index, "op": args.op, "requests": n_req,
                    "store_payload_bytes": S.store_payload, "load_payload_bytes": S.load_payload,
                    "chunk": S.C, "N": cfg.N, "layout": "packed" if cfg.packed else "padded",
                    "pool_bytes": L.pool_bytes,
@@ -489,8 +585,8 @@ def run_gpu(args):
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "chunks_per_s": round(S.chunks * world / (ms_per_step * 1e-3), 1),
-        "store": {"ms": round(st_avg, 4), "gbs": round(2 * S.store_payload / (st_avg * 1e-3) / 1e9, 2)},
-        "load": {"ms": round(ld_avg, 4), "gbs": round(2 * S.load_payload / (ld_avg * 1e-3) / 1e9, 2)},
+        "store": {"ms": round(st_avg, 4), "gbs": _gbs(2 * S.store_payload, st_avg)},
+        "load": {"ms": round(ld_avg, 4), "gbs": _gbs(2 * S.load_payload, ld_avg)},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -501,7 +597,7 @@ def run_gpu(args):
         "gpu_launches": S.launches_per_step * args.steps,
         "clocks": clocks,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and args.op == "paging":
         threads = os.cpu_count() or 1
         line["cpu_baseline"] = oracle_sample(args.config, requests=8, reps=20, threads=threads)
     print(json.dumps(line))
@@ -519,6 +615,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--impl", choices=["lmc", "reference"], default="lmc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["paging", "blocks", "copy"], default="paging",
+                    help="paging: store + load by chunk; blocks: block-granular objects with one KDA "
+                         "snapshot per block; copy: in-pool copy of every KDA snapshot")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -237,6 +237,66 @@ int lmc_load(const lmc_layout *layout, int64_t chunk_size, void *pool,
              const lmc_batch *batch, const void *arena, int64_t arena_bytes, uint32_t *status,
              void *stream);
 
+/* ---- block-granular objects ---------------------------------------------- */
+
+/* How a block-granular object holds KDA state. */
+#define LMC_KDA_LAST_BLOCK 0  /* one snapshot: the object's last block */
+#define LMC_KDA_EVERY_BLOCK 1 /* one snapshot per block of the object, in order */
+
+/* Bytes of one block-granular object of `object_group` covering
+ * `blocks_per_object` blocks: paged layers hold all blocks' pages, KDA layers
+ * one snapshot (LMC_KDA_LAST_BLOCK) or one per block (LMC_KDA_EVERY_BLOCK).
+ * With blocks_per_object = chunk / N and LMC_KDA_LAST_BLOCK this equals
+ * lmc_object_bytes. Error INVALID_ARG for blocks_per_object <= 0 or an
+ * unknown kda_mode. */
+int lmc_object_bytes_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                            int32_t object_group, int64_t *out);
+
+/* Block-granular store/load: like lmc_store/lmc_load, but each job's `chunk`
+ * field is the object's FIRST BLOCK POSITION and every object covers
+ * `blocks_per_object` consecutive positions. This stores the whole blocks
+ * past a request's last whole chunk (a tail object), objects aligned to
+ * scheduler steps rather than chunks ([KL] "Why these settings": a step of
+ * >= 2N tokens snapshots only its last block), and, with
+ * LMC_KDA_EVERY_BLOCK, the snapshots of every block boundary inside an
+ * object ([KL] the [N, 2N) regime; [VB] §7). Same arguments, ownership,
+ * status bits and errors as lmc_store/lmc_load otherwise. */
+int lmc_store_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                     const void *pool, const lmc_batch *batch, void *arena, int64_t arena_bytes,
+                     uint32_t *status, void *stream);
+int lmc_load_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode, void *pool,
+                    const lmc_batch *batch, const void *arena, int64_t arena_bytes, uint32_t *status,
+                    void *stream);
+
+/* ---- in-pool block copies ------------------------------------------------ */
+
+/* One copy: every layer page of a KV group, from block src to block dst. */
+typedef struct {
+    int32_t src_block;
+    int32_t dst_block;
+} lmc_block_pair;
+
+typedef struct {
+    int32_t num_kv_groups;            /* must equal the layout's */
+    int32_t reserved;                 /* set to 0 */
+    const lmc_block_pair *const *pairs; /* host array [num_kv_groups] of device
+                                           pointers (NULL allowed when the count is 0) */
+    const int64_t *num_pairs;         /* host array [num_kv_groups] */
+} lmc_copy_batch;
+
+/* In-pool copies ([MC] "Copy-on-Write": a hit's shared KDA checkpoint is
+ * copied into a private execution slot before it is updated; "Snapshot": a
+ * running state is copied into a spare buffer at a cacheable boundary).
+ * For each pair of KV group g, the real bytes of every layer of g are copied
+ * from block src_block to block dst_block of `pool` (padding untouched).
+ * A request's whole KDA state is one pair per KDA KV group. Pairs naming -1
+ * raise LMC_ST_NO_BLOCK, ids outside [0, num_blocks) LMC_ST_BLOCK_OOR; such
+ * pairs are skipped. Destination blocks must be distinct and must not be the
+ * source of another pair of the same call (they would race); src == dst is
+ * a no-op. Asynchronous on `stream`; errors INVALID_ARG, ALIGN, CUDA. */
+int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy_batch *batch, uint32_t *status,
+                    void *stream);
+
 /* Static description of a code ("LMC_OK", ...); never NULL. */
 const char *lmc_strerror(int code);
 

@@ -40,12 +40,17 @@ LMC_ST_NO_SNAPSHOT = 0x4
 LMC_ST_BAD_JOB = 0x8
 LMC_ST_TIMEOUT = 0x10
 
+LMC_KDA_LAST_BLOCK = 0
+LMC_KDA_EVERY_BLOCK = 1
+
 LMC_LAYER = {"MLA": 0, "KDA": 1, "SWA": 2}
 LMC_LAYER_NAME = {v: k for k, v in LMC_LAYER.items()}
 LMC_MAX_LAYERS = 256
 
 # An lmc_job record: request int32, chunk int32, arena offset int64.
 JOB_DTYPE = np.dtype([("request", "<i4"), ("chunk", "<i4"), ("offset", "<i8")])
+# An lmc_block_pair record: source block int32, destination block int32.
+PAIR_DTYPE = np.dtype([("src_block", "<i4"), ("dst_block", "<i4")])
 
 
 class LmcError(RuntimeError):
@@ -86,6 +91,11 @@ class lmc_block_table(ctypes.Structure):
     _fields_ = [("table", ctypes.c_void_p), ("row_stride", ctypes.c_int64), ("num_cols", ctypes.c_int64)]
 
 
+class lmc_copy_batch(ctypes.Structure):
+    _fields_ = [("num_kv_groups", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("pairs", ctypes.POINTER(ctypes.c_void_p)), ("num_pairs", ctypes.POINTER(ctypes.c_int64))]
+
+
 class lmc_batch(ctypes.Structure):
     _fields_ = [("num_requests", ctypes.c_int32), ("num_kv_groups", ctypes.c_int32),
                 ("tables", ctypes.POINTER(lmc_block_table)), ("num_object_groups", ctypes.c_int32),
@@ -109,6 +119,12 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("lmc_store", "lmc_load"):
         getattr(so, name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
                                       _i64, ctypes.c_void_p, ctypes.c_void_p]
+    so.lmc_object_bytes_blocks.argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, ctypes.c_int32, _P(_i64)]
+    for name in ("lmc_store_blocks", "lmc_load_blocks"):
+        getattr(so, name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, ctypes.c_void_p, _P(lmc_batch),
+                                      ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p]
+    so.lmc_copy_blocks.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(lmc_copy_batch), ctypes.c_void_p,
+                                   ctypes.c_void_p]
     so.lmc_strerror.argtypes = [ctypes.c_int]
     so.lmc_strerror.restype = ctypes.c_char_p
     return so
@@ -198,6 +214,10 @@ class Layout:
     def object_bytes(self, chunk: int, object_group: int) -> int:
         return lmc_object_bytes(self, chunk, object_group)
 
+    def object_bytes_blocks(self, blocks_per_object: int, kda_every: bool, object_group: int) -> int:
+        return lmc_object_bytes_blocks(self, blocks_per_object,
+                                       LMC_KDA_EVERY_BLOCK if kda_every else LMC_KDA_LAST_BLOCK, object_group)
+
     def __del__(self):
         h = getattr(self, "_h", None)
         if h is not None and h.value:
@@ -224,6 +244,13 @@ def lmc_object_bytes(layout: Layout, chunk: int, object_group: int) -> int:
     out = _i64(0)
     _check(_lib.lmc_object_bytes(layout.handle, int(chunk), int(object_group), ctypes.byref(out)),
            "lmc_object_bytes")
+    return out.value
+
+
+def lmc_object_bytes_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, object_group: int) -> int:
+    out = _i64(0)
+    _check(_lib.lmc_object_bytes_blocks(layout.handle, int(blocks_per_object), int(kda_mode), int(object_group),
+                                        ctypes.byref(out)), "lmc_object_bytes_blocks")
     return out.value
 
 
@@ -296,5 +323,52 @@ def lmc_load(layout: Layout, chunk: int, pool, tables, jobs, arena, status, stre
            "lmc_load")
 
 
+def lmc_store_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool, tables, jobs, arena, status,
+                     stream=None) -> None:
+    """Block-granular store: each job's `chunk` field is its first block position."""
+    _check_pool(layout, pool)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_store_blocks(layout.handle, int(blocks_per_object), int(kda_mode), pool.data_ptr(),
+                                 ctypes.byref(b), arena.data_ptr(), arena.numel() * arena.element_size(),
+                                 status.data_ptr(), _stream_ptr(stream)), "lmc_store_blocks")
+
+
+def lmc_load_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool, tables, jobs, arena, status,
+                    stream=None) -> None:
+    _check_pool(layout, pool)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_load_blocks(layout.handle, int(blocks_per_object), int(kda_mode), pool.data_ptr(),
+                                ctypes.byref(b), arena.data_ptr(), arena.numel() * arena.element_size(),
+                                status.data_ptr(), _stream_ptr(stream)), "lmc_load_blocks")
+
+
+def pairs_to_device(pairs: np.ndarray, device):
+    """Uploads a PAIR_DTYPE numpy array as a uint8 device tensor of 8-byte records."""
+    import torch
+    a = np.ascontiguousarray(pairs, dtype=PAIR_DTYPE)
+    return torch.from_numpy(a.view(np.uint8).copy()).to(device)
+
+
+def lmc_copy_blocks(layout: Layout, pool, pairs, status, stream=None) -> None:
+    """In-pool copies: `pairs[g]` (device tensor of 8-byte lmc_block_pair
+    records) lists (src, dst) blocks of KV group g."""
+    _check_pool(layout, pool)
+    g = layout.num_kv_groups
+    if len(pairs) != g:
+        raise LmcError(LMC_ERR_INVALID_ARG, f"{g} pair arrays expected, got {len(pairs)}")
+    parr = (ctypes.c_void_p * max(g, 1))()
+    narr = (_i64 * max(g, 1))()
+    for k, p in enumerate(pairs):
+        nbytes = p.numel() * p.element_size()
+        if nbytes % 8 or not p.is_contiguous():
+            raise LmcError(LMC_ERR_INVALID_ARG, "pair arrays hold contiguous 8-byte lmc_block_pair records")
+        parr[k] = p.data_ptr() if nbytes else None
+        narr[k] = nbytes // 8
+    b = lmc_copy_batch(g, 0, parr, narr)
+    _check(_lib.lmc_copy_blocks(layout.handle, pool.data_ptr(), ctypes.byref(b), status.data_ptr(),
+                                _stream_ptr(stream)), "lmc_copy_blocks")
+
+
 __all__ = [n for n in dir() if n.startswith(("lmc_", "LMC_"))] + ["Layout", "LmcError", "JOB_DTYPE",
-                                                                  "jobs_to_device"]
+                                                                  "jobs_to_device",
+                                                                  "PAIR_DTYPE", "pairs_to_device"]

@@ -238,6 +238,25 @@ extern "C" int lmc_object_bytes(const lmc_layout *L, int64_t chunk, int32_t og, 
     return LMC_OK;
 }
 
+extern "C" int lmc_object_bytes_blocks(const lmc_layout *L, int64_t nb, int32_t kda_mode, int32_t og,
+                                       int64_t *out) {
+    if (L == nullptr || out == nullptr || og < 0 || (size_t)og >= L->object_group_layers.size() || nb <= 0 ||
+        (kda_mode != LMC_KDA_LAST_BLOCK && kda_mode != LMC_KDA_EVERY_BLOCK))
+        return LMC_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int32_t i : L->object_group_layers[og]) {
+        const lmc_layer_desc &d = L->desc[i];
+        int64_t part = d.real_bytes;
+        const bool one = d.kind == LMC_LAYER_KDA && kda_mode == LMC_KDA_LAST_BLOCK;
+        if (!one && !lmc::mul_ok(nb, d.real_bytes, &part))
+            return LMC_ERR_OVERFLOW;
+        if (!lmc::add_ok(total, part, &total))
+            return LMC_ERR_OVERFLOW;
+    }
+    *out = total;
+    return LMC_OK;
+}
+
 extern "C" int lmc_negotiate_chunk(int64_t requested, int64_t N, int strict, int64_t *out) {
     if (out == nullptr || N <= 0)
         return LMC_ERR_INVALID_ARG;

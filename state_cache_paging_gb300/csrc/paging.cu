@@ -1,23 +1,26 @@
-// paging.cu -- store (gather pages -> chunk objects) and load (scatter chunk
-// objects -> pages) for sm_103a.
+// paging.cu -- store (gather pages -> chunk objects), load (scatter chunk
+// objects -> pages) and in-pool block copies for sm_103a.
 //
 // What is moved ("Hybrid Attention Models" (LMCache docs), Object-group
 // separation; "Kimi-Linear" (LMCache recipe), Why these settings; "How vLLM
-// manages the KV cache of hybrid models", §3.1/§3.2/§4): one object per
-// (request, chunk, object group); inside it, the group's layers in model
-// order; a paged attention layer contributes the chunk's m = C / N blocks,
-// token-major, a KDA layer the state snapshot stored at the chunk's last
-// block position. The cached pages are byte-opaque, so this is pure data
-// movement: every byte is read once from HBM and written once.
+// manages the KV cache of hybrid models", §3.1/§3.2/§4/§7; "When Prefix Cache
+// Meets KDA", Copy-on-Write / Snapshot): one object per (request, chunk or
+// block range, object group); inside it, the group's layers in model order; a
+// paged attention layer contributes the object's blocks, token-major, a KDA
+// layer the state snapshot stored at the object's last block (or one per
+// block). A block copy moves every layer page of one KV group from a source
+// block to a destination block of the same pool. The cached pages are
+// byte-opaque, so this is pure data movement: every byte is read once from
+// HBM and written once.
 //
-// GPU design. The work of one launch is a flat list of equal-sized tiles
-// (each at most kTileBytes, 16-byte multiples, never crossing a page). Tile
-// t resolves to (object group, job, layer, page, piece) with integer math on
-// the launch plan held in kernel parameter space, reads one block id from
-// the caller's block table, and copies one contiguous range: 16-byte
-// vector loads that bypass L1 and streaming (evict-first) stores, several in
-// flight per thread. One CTA per tile, many CTAs resident per SM, so the
-// dependent block-table read of one CTA hides under the copies of others.
+// GPU design. The work of one launch is a flat list of tiles (each at most
+// kTileBytes, 16-byte multiples, never crossing a page). Tile t resolves to
+// (group, job, layer, page, piece) with integer math on the launch plan held
+// in kernel parameter space, reads one block id (or one block pair) from the
+// caller's device arrays, and copies one contiguous range: 16-byte vector
+// loads that bypass L1 and streaming (evict-first) stores, several in flight
+// per thread. One CTA per tile, several CTAs resident per SM, so the dependent
+// block-table read of one CTA hides under the copies of others.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -49,11 +52,17 @@
 #ifndef LMC_BULK_CTAS_PER_SM
 #define LMC_BULK_CTAS_PER_SM 1
 #endif
+#ifndef LMC_LD_HINT
+#define LMC_LD_HINT 0  // 0: .nc.L1::no_allocate, 1: + .L2::256B prefetch, 2: plain
+#endif
+#ifndef LMC_ST_HINT
+#define LMC_ST_HINT 0  // 0: .cs (evict-first), 1: plain write-back, 2: .L1::no_allocate
+#endif
 
 namespace {
 
-constexpr int kMaxEntries = LMC_MAX_LAYERS;  // layers in one launch
-constexpr int kMaxGroups = 16;               // object groups in one launch
+constexpr int kMaxEntries = LMC_MAX_LAYERS;  // layer entries in one launch
+constexpr int kMaxGroups = 64;               // object groups (or KV groups) in one launch
 constexpr int kMaxKv = 64;                   // KV groups (block tables)
 constexpr int kTileBytes = LMC_TILE_BYTES;
 constexpr int kThreads = LMC_THREADS;
@@ -64,7 +73,9 @@ constexpr int kBulkCtasPerSm = LMC_BULK_CTAS_PER_SM;
 static_assert(kEngine != 1 || kBulkCtasPerSm * (kBulkStages * kTileBytes + 1024) <= 228 * 1024,
               "bulk stages must fit the SM's shared memory");
 
-// One layer's run of pages inside an object of one group.
+enum Mode : int32_t { kStore = 0, kLoad = 1, kCopy = 2 };
+
+// One layer's run of pages inside an object (or inside a copied block).
 struct Entry {
     int64_t pool_base;    // pool byte offset of block 0's page
     int64_t pool_stride;  // bytes between consecutive blocks' pages
@@ -73,15 +84,15 @@ struct Entry {
     int32_t tile_bytes;   // bytes per tile of this page (last tile shorter)
     int32_t tiles_per_seg;
     int32_t tile_start;   // tiles of earlier layers in the object
-    int32_t pos_add;      // block position = chunk * m + pos_add + page index
+    int32_t pos_add;      // block position = first + pos_add + page index
     int16_t kv;           // KV group (block table)
-    uint8_t kda;          // 1: a single snapshot page
+    uint8_t kda;          // 1: a KDA state page (a missing one is NO_SNAPSHOT)
     uint8_t pad;
 };
 
 struct Group {
-    const lmc_job *jobs;
-    int64_t num_jobs;
+    const void *items;   // lmc_job[] (store/load) or lmc_block_pair[] (copy)
+    int64_t num_items;
     int64_t tile_begin;  // first launch-wide tile of this group
     int64_t obj_bytes;
     int32_t tiles_per_obj;
@@ -97,28 +108,21 @@ struct Table {
 };
 
 struct Plan {
-    const uint8_t *src_base;  // store: pool; load: arena
-    uint8_t *dst_base;        // store: arena; load: pool
+    const uint8_t *src_base;  // store: pool; load: arena; copy: pool
+    uint8_t *dst_base;        // store: arena; load: pool; copy: pool
     uint32_t *status;
     int64_t arena_bytes;
     int64_t num_blocks;
     int64_t total_tiles;
-    int32_t m;
+    int32_t pos_mul;  // first block position = job.chunk * pos_mul (C/N for chunk jobs, 1 for block jobs)
     int32_t num_requests;
     int32_t num_groups;
-    int32_t store;  // 1: pool -> arena
+    int32_t mode;
     Group groups[kMaxGroups];
     Table tables[kMaxKv];
     Entry entries[kMaxEntries];
 };
 static_assert(sizeof(Plan) <= 32000, "kernel parameter space");
-
-#ifndef LMC_LD_HINT
-#define LMC_LD_HINT 0  // 0: .nc.L1::no_allocate, 1: + .L2::256B prefetch, 2: plain
-#endif
-#ifndef LMC_ST_HINT
-#define LMC_ST_HINT 0  // 0: .cs (evict-first), 1: plain write-back, 2: .L1::no_allocate
-#endif
 
 // Source bytes are read once: bypass L1 (and never alias the destination).
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
@@ -157,12 +161,18 @@ struct Span {
 
 // Resolves tile -> span; returns the status bits to raise (0: copy it).
 __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s) {
-    int g = 0;
-    while (g + 1 < P.num_groups && tile >= P.groups[g + 1].tile_begin)
-        g++;
+    // group: the last one whose first tile is <= tile
+    int g = 0, gh = P.num_groups - 1;
+    while (g < gh) {
+        const int mid = (g + gh + 1) >> 1;
+        if (P.groups[mid].tile_begin <= tile)
+            g = mid;
+        else
+            gh = mid - 1;
+    }
     const Group &G = P.groups[g];
     const int64_t local = tile - G.tile_begin;
-    const int64_t q = local / G.tiles_per_obj;  // job index
+    const int64_t q = local / G.tiles_per_obj;  // job (or pair) index
     const int32_t t = (int32_t)(local - q * G.tiles_per_obj);
 
     // layer entry: the last one whose first tile is <= t
@@ -178,13 +188,27 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
     const int32_t u = t - E.tile_start;
     const int32_t j = u / E.tiles_per_seg;  // page index within the layer
     const int32_t k = u - j * E.tiles_per_seg;
+    const int64_t piece = (int64_t)k * E.tile_bytes;
+    s.bytes = min(E.tile_bytes, (int32_t)(E.seg_bytes - piece));
 
-    const lmc_job job = G.jobs[q];
+    if (P.mode == kCopy) {
+        const lmc_block_pair pr = static_cast<const lmc_block_pair *>(G.items)[q];
+        if (pr.src_block == -1 || pr.dst_block == -1)
+            return LMC_ST_NO_BLOCK;
+        if (pr.src_block < 0 || pr.src_block >= P.num_blocks || pr.dst_block < 0 ||
+            pr.dst_block >= P.num_blocks)
+            return LMC_ST_BLOCK_OOR;
+        s.src = P.src_base + E.pool_base + (int64_t)pr.src_block * E.pool_stride + piece;
+        s.dst = P.dst_base + E.pool_base + (int64_t)pr.dst_block * E.pool_stride + piece;
+        return 0;
+    }
+
+    const lmc_job job = static_cast<const lmc_job *>(G.items)[q];
     if (job.request < 0 || job.request >= P.num_requests || job.chunk < 0 || job.offset < 0 ||
         (job.offset & 15) != 0 || job.offset > P.arena_bytes - G.obj_bytes)
         return LMC_ST_BAD_JOB;
     const Table &T = P.tables[E.kv];
-    const int64_t pos = (int64_t)job.chunk * P.m + E.pos_add + j;
+    const int64_t pos = (int64_t)job.chunk * P.pos_mul + E.pos_add + j;
     if (pos >= T.num_cols)
         return LMC_ST_BAD_JOB;
     const int32_t block = __ldg(T.ptr + (int64_t)job.request * T.row_stride + pos);
@@ -193,12 +217,10 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
     if (block < 0 || block >= P.num_blocks)
         return LMC_ST_BLOCK_OOR;
 
-    const int64_t piece = (int64_t)k * E.tile_bytes;
     const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + piece;
     const int64_t obj = job.offset + E.obj_off + (int64_t)j * E.seg_bytes + piece;
-    s.bytes = min(E.tile_bytes, (int32_t)(E.seg_bytes - piece));
-    s.src = P.src_base + (P.store ? page : obj);
-    s.dst = P.dst_base + (P.store ? obj : page);
+    s.src = P.src_base + (P.mode == kStore ? page : obj);
+    s.dst = P.dst_base + (P.mode == kStore ? obj : page);
     return 0;
 }
 
@@ -237,7 +259,7 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
     }
 }
 
-// Distinct names for the two directions (they share the body; the plan says
+// Distinct names per operation (they share the body; the plan's mode says
 // which side is the pool).
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_store_kernel(const __grid_constant__ Plan P) {
@@ -245,6 +267,10 @@ __global__ void __launch_bounds__(kThreads) lmc_store_kernel(const __grid_consta
 }
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_load_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<kVec>(P);
+}
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) lmc_copy_kernel(const __grid_constant__ Plan P) {
     copy_tiles<kVec>(P);
 }
 
@@ -388,6 +414,10 @@ __global__ void __launch_bounds__(32) lmc_load_bulk_kernel(const __grid_constant
     bulk_tiles<kStages>(P);
 }
 
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
 int sm_count() {
     static std::mutex mu;
     static std::vector<int> cache;
@@ -408,19 +438,74 @@ int sm_count() {
 
 bool aligned16(int64_t x) { return (x & 15) == 0; }
 
-// Host-side validation and launch plan; shared by store and load.
-int build_plan(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_batch *b,
-               const void *arena, int64_t arena_bytes, uint32_t *status, bool store, Plan &P,
-               bool &vec) {
-    if (L == nullptr || b == nullptr || status == nullptr)
+// Appends a layer entry (one page of `d`, `pages` pages per object).
+int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t pos_add, int64_t &obj,
+              int64_t &tiles, bool &vec) {
+    if (ne >= kMaxEntries)
         return LMC_ERR_INVALID_ARG;
-    if (chunk <= 0 || chunk % L->block_size != 0)
-        return LMC_ERR_NOT_MULTIPLE;
+    if (d.real_bytes > INT32_MAX - kTileBytes)
+        return LMC_ERR_INVALID_ARG;  // one page must stay below 2 GiB
+    const int32_t seg = (int32_t)d.real_bytes;
+    const int32_t pieces = (seg + kTileBytes - 1) / kTileBytes;
+    int32_t tb = (seg + pieces - 1) / pieces;
+    tb = (tb + 15) & ~15;  // 16-byte pieces; the last one is shorter
+    Entry &E = P.entries[ne++];
+    E.pool_base = d.base;
+    E.pool_stride = d.stride;
+    E.obj_off = obj;
+    E.seg_bytes = seg;
+    E.tile_bytes = tb;
+    E.tiles_per_seg = (seg + tb - 1) / tb;
+    E.tile_start = (int32_t)tiles;
+    E.kda = d.kind == LMC_LAYER_KDA;
+    E.pos_add = pos_add;
+    E.kv = (int16_t)d.kv_group;
+    int64_t add;
+    if (!lmc::mul_ok(pages, seg, &add) || !lmc::add_ok(obj, add, &obj))
+        return LMC_ERR_OVERFLOW;
+    tiles += pages * E.tiles_per_seg;
+    if (tiles > INT32_MAX)
+        return LMC_ERR_OVERFLOW;
+    vec = vec && aligned16(d.base) && aligned16(d.stride) && aligned16(seg);
+    return LMC_OK;
+}
+
+// Adds a group of `n` items to the plan's tile space.
+int close_group(Plan &P, int ne, int first_entry, const void *items, int64_t n, int64_t obj, int64_t tiles,
+                int64_t &total) {
+    if (P.num_groups >= kMaxGroups)
+        return LMC_ERR_INVALID_ARG;
+    Group &G = P.groups[P.num_groups++];
+    G.items = items;
+    G.num_items = n;
+    G.first_entry = first_entry;
+    G.num_entries = ne - first_entry;
+    G.obj_bytes = obj;
+    G.tiles_per_obj = (int32_t)tiles;
+    G.tile_begin = total;
+    int64_t add;
+    if (!lmc::mul_ok(n, tiles, &add) || !lmc::add_ok(total, add, &total))
+        return LMC_ERR_OVERFLOW;
+    return LMC_OK;
+}
+
+// Object geometry of one call: an object covers `nb` block positions from
+// job.chunk * pos_mul; KDA layers give the last block's snapshot, or one per
+// block with kda_every.
+struct Shape {
+    int64_t nb;
+    int32_t pos_mul;
+    bool kda_every;
+};
+
+// Host-side validation and launch plan of a store or load.
+int build_object_plan(const lmc_layout *L, const Shape &sh, const void *pool, const lmc_batch *b,
+                      const void *arena, int64_t arena_bytes, uint32_t *status, Mode mode, Plan &P,
+                      bool &vec) {
+    if (b == nullptr || status == nullptr)
+        return LMC_ERR_INVALID_ARG;
     if (((uintptr_t)status & 3) != 0)
         return LMC_ERR_ALIGN;
-    const int64_t m64 = chunk / L->block_size;
-    if (m64 > INT32_MAX)
-        return LMC_ERR_OVERFLOW;
     const int nkv = (int)L->kv_group_kind.size();
     const int nog = (int)L->object_group_layers.size();
     if (b->num_requests < 0 || b->num_kv_groups != nkv || b->num_object_groups != nog ||
@@ -431,12 +516,12 @@ int build_plan(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_b
         return LMC_ERR_INVALID_ARG;
 
     std::memset(&P, 0, sizeof(P));
-    P.m = (int32_t)m64;
+    P.pos_mul = sh.pos_mul;
     P.num_requests = b->num_requests;
     P.num_blocks = L->num_blocks;
     P.arena_bytes = arena_bytes;
     P.status = status;
-    P.store = store ? 1 : 0;
+    P.mode = mode;
     for (int k = 0; k < nkv; k++) {
         const lmc_block_table &t = b->tables[k];
         if (t.num_cols < 0 || t.row_stride < t.num_cols ||
@@ -454,69 +539,39 @@ int build_plan(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_b
             return LMC_ERR_INVALID_ARG;
         if (nj == 0)
             continue;
-        Group &G = P.groups[P.num_groups];
-        G.jobs = b->jobs[og];
-        G.num_jobs = nj;
-        G.first_entry = ne;
+        const int first = ne;
         int64_t obj = 0, tiles = 0;
         for (int32_t i : L->object_group_layers[og]) {
             const lmc_layer_desc &d = L->desc[i];
-            if (d.real_bytes > INT32_MAX - kTileBytes)
-                return LMC_ERR_INVALID_ARG;  // one page must stay below 2 GiB
-            const int32_t seg = (int32_t)d.real_bytes;
-            const int32_t pieces = (seg + kTileBytes - 1) / kTileBytes;
-            int32_t tb = (seg + pieces - 1) / pieces;
-            tb = (tb + 15) & ~15;  // 16-byte pieces; the last one is shorter
-            Entry &E = P.entries[ne++];
-            E.pool_base = d.base;
-            E.pool_stride = d.stride;
-            E.obj_off = obj;
-            E.seg_bytes = seg;
-            E.tile_bytes = tb;
-            E.tiles_per_seg = (seg + tb - 1) / tb;
-            E.tile_start = (int32_t)tiles;
-            E.kda = d.kind == LMC_LAYER_KDA;
-            E.pos_add = E.kda ? P.m - 1 : 0;
-            E.kv = (int16_t)d.kv_group;
-            const int64_t pages = E.kda ? 1 : m64;
-            obj += pages * seg;
-            tiles += pages * E.tiles_per_seg;
-            if (tiles > INT32_MAX)
-                return LMC_ERR_OVERFLOW;
-            vec = vec && aligned16(d.base) && aligned16(d.stride) && aligned16(seg);
+            const bool last_only = d.kind == LMC_LAYER_KDA && !sh.kda_every;
+            const int rc = add_entry(P, ne, d, last_only ? 1 : sh.nb, last_only ? (int32_t)(sh.nb - 1) : 0,
+                                     obj, tiles, vec);
+            if (rc != LMC_OK)
+                return rc;
         }
-        G.num_entries = ne - G.first_entry;
-        G.obj_bytes = obj;
-        G.tiles_per_obj = (int32_t)tiles;
-        G.tile_begin = total;
-        int64_t add;
-        if (!lmc::mul_ok(nj, tiles, &add) || !lmc::add_ok(total, add, &total))
-            return LMC_ERR_OVERFLOW;
-        P.num_groups++;
+        const int rc = close_group(P, ne, first, b->jobs[og], nj, obj, tiles, total);
+        if (rc != LMC_OK)
+            return rc;
     }
     P.total_tiles = total;
     if (total > 0 && (pool == nullptr || arena == nullptr))
         return LMC_ERR_INVALID_ARG;
-    P.src_base = static_cast<const uint8_t *>(store ? pool : arena);
-    P.dst_base = static_cast<uint8_t *>(const_cast<void *>(store ? arena : pool));
+    P.src_base = static_cast<const uint8_t *>(mode == kStore ? pool : arena);
+    P.dst_base = static_cast<uint8_t *>(const_cast<void *>(mode == kStore ? arena : pool));
     return LMC_OK;
 }
 
-int launch(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_batch *b,
-           const void *arena, int64_t arena_bytes, uint32_t *status, void *stream, bool store) {
-    Plan P;
-    bool vec = false;
-    int rc = build_plan(L, chunk, pool, b, arena, arena_bytes, status, store, P, vec);
-    if (rc != LMC_OK || P.total_tiles == 0)
-        return rc;
+int launch_plan(const Plan &P, bool vec, void *stream) {
+    if (P.total_tiles == 0)
+        return LMC_OK;
     const int sms = sm_count();
     if (sms <= 0)
         return LMC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec && kEngine == 1) {
+    if (vec && kEngine == 1 && P.mode != kCopy) {
         // persistent: kBulkCtasPerSm CTAs per SM, each a ring of stages
         const size_t smem = (size_t)kBulkStages * kTileBytes;
-        auto kern = store ? lmc_store_bulk_kernel<kBulkStages> : lmc_load_bulk_kernel<kBulkStages>;
+        auto kern = P.mode == kStore ? lmc_store_bulk_kernel<kBulkStages> : lmc_load_bulk_kernel<kBulkStages>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return LMC_ERR_CUDA;
         const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * kBulkCtasPerSm);
@@ -524,12 +579,44 @@ int launch(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_batch
     } else {
         // one CTA per tile, capped; the kernel strides over the rest
         const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * 2048);
-        if (vec)
-            (store ? lmc_store_kernel<true> : lmc_load_kernel<true>)<<<grid, kThreads, 0, s>>>(P);
+        void (*kern)(const Plan);
+        if (P.mode == kStore)
+            kern = vec ? lmc_store_kernel<true> : lmc_store_kernel<false>;
+        else if (P.mode == kLoad)
+            kern = vec ? lmc_load_kernel<true> : lmc_load_kernel<false>;
         else
-            (store ? lmc_store_kernel<false> : lmc_load_kernel<false>)<<<grid, kThreads, 0, s>>>(P);
+            kern = vec ? lmc_copy_kernel<true> : lmc_copy_kernel<false>;
+        kern<<<grid, kThreads, 0, s>>>(P);
     }
     return cudaGetLastError() == cudaSuccess ? LMC_OK : LMC_ERR_CUDA;
+}
+
+int chunk_shape(const lmc_layout *L, int64_t chunk, Shape &sh) {
+    if (L == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    if (chunk <= 0 || chunk % L->block_size != 0)
+        return LMC_ERR_NOT_MULTIPLE;
+    const int64_t m = chunk / L->block_size;
+    if (m > INT32_MAX)
+        return LMC_ERR_OVERFLOW;
+    sh = Shape{m, (int32_t)m, false};
+    return LMC_OK;
+}
+
+int block_shape(const lmc_layout *L, int64_t nb, int32_t kda_mode, Shape &sh) {
+    if (L == nullptr || nb <= 0 || nb > INT32_MAX ||
+        (kda_mode != LMC_KDA_LAST_BLOCK && kda_mode != LMC_KDA_EVERY_BLOCK))
+        return LMC_ERR_INVALID_ARG;
+    sh = Shape{nb, 1, kda_mode == LMC_KDA_EVERY_BLOCK};
+    return LMC_OK;
+}
+
+int run_objects(const lmc_layout *L, const Shape &sh, const void *pool, const lmc_batch *b, const void *arena,
+                int64_t arena_bytes, uint32_t *status, void *stream, Mode mode) {
+    Plan P;
+    bool vec = false;
+    const int rc = build_object_plan(L, sh, pool, b, arena, arena_bytes, status, mode, P, vec);
+    return rc != LMC_OK ? rc : launch_plan(P, vec, stream);
 }
 
 }  // namespace
@@ -537,11 +624,75 @@ int launch(const lmc_layout *L, int64_t chunk, const void *pool, const lmc_batch
 extern "C" int lmc_store(const lmc_layout *layout, int64_t chunk_size, const void *pool,
                          const lmc_batch *batch, void *arena, int64_t arena_bytes, uint32_t *status,
                          void *stream) {
-    return launch(layout, chunk_size, pool, batch, arena, arena_bytes, status, stream, true);
+    Shape sh;
+    const int rc = chunk_shape(layout, chunk_size, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kStore);
 }
 
 extern "C" int lmc_load(const lmc_layout *layout, int64_t chunk_size, void *pool,
                         const lmc_batch *batch, const void *arena, int64_t arena_bytes,
                         uint32_t *status, void *stream) {
-    return launch(layout, chunk_size, pool, batch, arena, arena_bytes, status, stream, false);
+    Shape sh;
+    const int rc = chunk_shape(layout, chunk_size, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kLoad);
+}
+
+extern "C" int lmc_store_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                                const void *pool, const lmc_batch *batch, void *arena, int64_t arena_bytes,
+                                uint32_t *status, void *stream) {
+    Shape sh;
+    const int rc = block_shape(layout, blocks_per_object, kda_mode, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kStore);
+}
+
+extern "C" int lmc_load_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                               void *pool, const lmc_batch *batch, const void *arena, int64_t arena_bytes,
+                               uint32_t *status, void *stream) {
+    Shape sh;
+    const int rc = block_shape(layout, blocks_per_object, kda_mode, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kLoad);
+}
+
+extern "C" int lmc_copy_blocks(const lmc_layout *L, void *pool, const lmc_copy_batch *b, uint32_t *status,
+                               void *stream) {
+    if (L == nullptr || b == nullptr || status == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    if (((uintptr_t)status & 3) != 0)
+        return LMC_ERR_ALIGN;
+    const int nkv = (int)L->kv_group_kind.size();
+    if (b->num_kv_groups != nkv || nkv > kMaxGroups || b->pairs == nullptr || b->num_pairs == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    Plan P;
+    std::memset(&P, 0, sizeof(P));
+    P.num_blocks = L->num_blocks;
+    P.status = status;
+    P.mode = kCopy;
+    bool vec = aligned16((int64_t)(uintptr_t)pool);
+    int64_t total = 0;
+    int ne = 0;
+    for (int g = 0; g < nkv; g++) {
+        const int64_t n = b->num_pairs[g];
+        if (n < 0 || (n > 0 && b->pairs[g] == nullptr))
+            return LMC_ERR_INVALID_ARG;
+        if (n == 0)
+            continue;
+        const int first = ne;
+        int64_t obj = 0, tiles = 0;
+        for (size_t i = 0; i < L->desc.size(); i++) {
+            if (L->desc[i].kv_group != g)
+                continue;
+            const int rc = add_entry(P, ne, L->desc[i], 1, 0, obj, tiles, vec);
+            if (rc != LMC_OK)
+                return rc;
+        }
+        const int rc = close_group(P, ne, first, b->pairs[g], n, obj, tiles, total);
+        if (rc != LMC_OK)
+            return rc;
+    }
+    P.total_tiles = total;
+    if (total > 0 && pool == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    P.src_base = static_cast<const uint8_t *>(pool);
+    P.dst_base = static_cast<uint8_t *>(pool);
+    return launch_plan(P, vec, stream);
 }

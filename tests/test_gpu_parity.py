@@ -324,3 +324,204 @@ def test_full_size_mixed_two_streams(lmc):
         lo, n = int(pg["pool_offset"]), int(pg["bytes"])
         ref[lo:lo + n] = pool[lo:lo + n]
     assert torch.equal(ref, pool)
+
+
+# ---------------------------------------------------------------------------
+# Block-granular objects (tails, every-block snapshots) and in-pool copies
+# ---------------------------------------------------------------------------
+
+def _block_units(inp, kind):
+    """(blocks per object, every-block flag, units per object group)."""
+    L, C = inp.layout, inp.C
+    m = C // L.N
+    og_n = L.num_object_groups
+    if kind == "every":
+        u = [(r, c * m) for r, Lr in enumerate(inp.lengths) for c in range(int(Lr) // C)]
+        return [(m, True, [u] * og_n)]
+    tails = {}
+    for r, Lr in enumerate(inp.lengths):
+        t = int(Lr) // L.N - (int(Lr) // C) * m
+        if t > 0:
+            tails.setdefault(t, []).append((r, (int(Lr) // C) * m))
+    return [(nb, False, [u] * og_n) for nb, u in sorted(tails.items())]
+
+
+def _blocks_exact(lmc, inp, Lp, kind):
+    Lo = inp.layout
+    shapes = _block_units(inp, kind)
+    assert shapes
+    for nb, every, units in shapes:
+        sizes = [Lo.object_bytes_blocks(nb, every, g) for g in range(Lo.num_object_groups)]
+        for g in range(Lo.num_object_groups):
+            assert Lp.object_bytes_blocks(nb, every, g) == sizes[g]
+        jobs, nbytes = W.pack_jobs(units, sizes)
+        mode = lmc.LMC_KDA_EVERY_BLOCK if every else lmc.LMC_KDA_LAST_BLOCK
+        pool_h = W.fill_normal_np(Lo.pool_bytes, 55 + nb)
+        pool = torch.from_numpy(pool_h).to(DEV)
+        arena = torch.full((nbytes,), 0x3C, dtype=torch.uint8, device=DEV)
+        fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+        st = _status()
+        dj = dev_jobs(jobs, DEV)
+        lmc.lmc_store_blocks(Lp, nb, mode, pool, dev_tables(inp.tables_src, DEV), dj, arena, st)
+        lmc.lmc_load_blocks(Lp, nb, mode, fresh, dev_tables(inp.tables_dst, DEV), dj, arena, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        arena_o = np.full(nbytes, 0x3C, dtype=np.uint8)
+        assert oracle.store_blocks(Lo, nb, every, pool_h, inp.tables_src, jobs, arena_o) == 0
+        fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        assert oracle.load_blocks(Lo, nb, every, fresh_o, inp.tables_dst, jobs, arena_o) == 0
+        assert np.array_equal(arena.cpu().numpy(), arena_o), (kind, nb)
+        assert np.array_equal(fresh.cpu().numpy(), fresh_o), (kind, nb)
+
+
+def _tail_cfg(seed, packed):
+    # chunk 150 -> 192 = 3 blocks of 64: the requests leave 1 or 2 tail blocks
+    cfg0 = W.CONFIGS[0]
+    return W.Config(300 + seed, "tails", cfg0.layers, N=64, requested_chunk=150, packed=packed,
+                    num_requests=4, lengths="fixed", fixed_lengths=(300, 517, 640, 1000), seed=seed)
+
+
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("kind", ["tails", "every"])
+def test_block_objects_exact(lmc, packed, kind):
+    inp, Lp = case_inputs(_tail_cfg(7, packed))
+    _blocks_exact(lmc, inp, Lp, kind)
+
+
+@pytest.mark.parametrize("t", range(6))
+def test_block_objects_random_specs(lmc, t):
+    rng = np.random.default_rng(2000 + t)
+    cfg = _random_cfg(rng, t)
+    cfg = W.Config(cfg.index, cfg.name, cfg.layers, N=cfg.N, requested_chunk=3 * cfg.N, packed=cfg.packed,
+                   num_requests=cfg.num_requests, lengths="fixed",
+                   fixed_lengths=tuple(int(x) + 4 * cfg.N for x in cfg.fixed_lengths), snapshot="block",
+                   seed=cfg.seed)
+    inp, Lp = case_inputs(cfg, split=bool(t % 2))
+    _blocks_exact(lmc, inp, Lp, "every")
+    if _block_units(inp, "tails"):
+        _blocks_exact(lmc, inp, Lp, "tails")
+
+
+def test_block_objects_full_size_every_block(lmc):
+    """Kimi-Linear packed, chunk = 2N, objects with one KDA snapshot per block."""
+    cfg = W.CONFIGS[2]
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    nb, every, units = _block_units(inp, "every")[0]
+    sizes = [Lo.object_bytes_blocks(nb, every, g) for g in range(Lo.num_object_groups)]
+    jobs, nbytes = W.pack_jobs(units, sizes)
+    pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, 77)
+    arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    dj = dev_jobs(jobs, DEV)
+    t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+    lmc.lmc_store_blocks(Lp, nb, lmc.LMC_KDA_EVERY_BLOCK, pool, t_src, dj, arena, st)
+    lmc.lmc_load_blocks(Lp, nb, lmc.LMC_KDA_EVERY_BLOCK, fresh, t_dst, dj, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(2)
+    sel = [J[np.sort(rng.choice(len(J), 6, replace=False))] for J in jobs]
+    pages, s0 = oracle.list_pages(Lo, C, inp.tables_src, sel, nbytes, nb=nb, kda_every=True)
+    assert s0 == 0
+    host_pool = np.zeros(Lo.pool_bytes, dtype=np.uint8)
+    for pg in pages:
+        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
+        host_pool[lo:lo + n] = pool[lo:lo + n].cpu().numpy()
+    arena_o = np.zeros(nbytes, dtype=np.uint8)
+    assert oracle.store_blocks(Lo, nb, True, host_pool, inp.tables_src, sel, arena_o) == 0
+    for g, J in enumerate(sel):
+        for job in J:
+            lo, hi = int(job["offset"]), int(job["offset"]) + sizes[g]
+            assert np.array_equal(arena[lo:hi].cpu().numpy(), arena_o[lo:hi])
+    arena2 = torch.empty_like(arena)
+    lmc.lmc_store_blocks(Lp, nb, lmc.LMC_KDA_EVERY_BLOCK, fresh, t_dst, dj, arena2, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(arena, arena2)
+
+
+def _random_pairs(L, rng, per_group, free_from):
+    """Distinct sources below `free_from`, distinct destinations at or above it."""
+    src = rng.permutation(free_from)
+    dst = free_from + rng.permutation(L.num_blocks - free_from)
+    out, k = [], 0
+    for g in range(L.num_kv_groups):
+        n = min(per_group, (L.num_blocks - free_from) // L.num_kv_groups)
+        out.append(np.array(list(zip(src[k:k + n], dst[k:k + n])), dtype=oracle.PAIR_DTYPE).reshape(-1))
+        k += n
+    return out
+
+
+@pytest.mark.parametrize("t", range(8))
+def test_copy_blocks_exact(lmc, t):
+    rng = np.random.default_rng(3000 + t)
+    spec = P.random_spec(rng, int(rng.integers(2, 9)))
+    N = int(rng.choice([4, 16, 64]))
+    packed = bool(t % 2)
+    o = oracle.layout(spec, N, packed, int(rng.integers(2, 8)) << 20)
+    p = lmc.lmc_layout_build(spec, N, packed, int(o.pool_bytes))
+    assert p.num_blocks == o.num_blocks and p.base == o.base
+    pairs = _random_pairs(o, rng, 6, o.num_blocks // 2)
+    if t == 7:  # faults: -1 and an id past the pool are skipped with their bits
+        pairs[0] = np.concatenate([pairs[0], np.array([(-1, 1), (2, o.num_blocks)], dtype=oracle.PAIR_DTYPE)])
+    pool_h = W.fill_normal_np(o.pool_bytes, t)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    st = _status()
+    lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], st)
+    torch.cuda.synchronize()
+    st_o = oracle.copy_blocks(o, pool_h, pairs)
+    assert int(st.item()) == st_o
+    assert np.array_equal(pool.cpu().numpy(), pool_h)
+
+
+def test_copy_blocks_full_size_kda_states(lmc):
+    """Copy-on-write of every KDA snapshot of the Kimi-Linear batch (768
+    pairs over 3 KDA groups, 10 GB) into spare blocks of a larger pool."""
+    cfg = W.CONFIGS[1]
+    inp, _ = case_inputs(cfg)
+    need = inp.layout.num_blocks
+    per_block = inp.layout.pool_bytes // need
+    o = oracle.layout(cfg.layers, cfg.N, cfg.packed, 2 * need * per_block)
+    p = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, 2 * need * per_block)
+    assert p.base == o.base and p.num_blocks == 2 * need
+    pairs = []
+    nxt = need
+    for g, kind in enumerate(o.kv_group_kind):
+        src = inp.tables_src[g][inp.tables_src[g] >= 0] if kind == "KDA" else np.zeros(0, np.int32)
+        pairs.append(np.array([(int(s), nxt + i) for i, s in enumerate(src)], dtype=oracle.PAIR_DTYPE).reshape(-1))
+        nxt += len(src)
+    pool = torch.empty(o.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, 91)
+    before = pool.clone()
+    st = _status()
+    lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # every destination page holds its source page; every other byte is unchanged
+    ref = before
+    for g, P_ in enumerate(pairs):
+        layers = [i for i in range(len(o.kinds)) if o.kv_group[i] == g]
+        for pr in P_:
+            for i in layers:
+                s0 = o.base[i] + int(pr["src_block"]) * o.stride[i]
+                d0 = o.base[i] + int(pr["dst_block"]) * o.stride[i]
+                ref[d0:d0 + o.real_bytes[i]] = before[s0:s0 + o.real_bytes[i]]
+    assert torch.equal(ref, pool)
+    # and a sample matches the oracle run on host copies of the pages involved
+    rng = np.random.default_rng(5)
+    g = o.kv_group_kind.index("KDA")
+    sel = pairs[g][rng.choice(len(pairs[g]), 4, replace=False)]
+    host = np.zeros(o.pool_bytes, dtype=np.uint8)
+    layers = [i for i in range(len(o.kinds)) if o.kv_group[i] == g]
+    for pr in sel:
+        for i in layers:
+            s0 = o.base[i] + int(pr["src_block"]) * o.stride[i]
+            host[s0:s0 + o.real_bytes[i]] = ref[s0:s0 + o.real_bytes[i]].cpu().numpy()
+    only = [np.zeros(0, dtype=oracle.PAIR_DTYPE) for _ in pairs]
+    only[g] = sel
+    assert oracle.copy_blocks(o, host, only) == 0
+    for pr in sel:
+        for i in layers:
+            d0 = o.base[i] + int(pr["dst_block"]) * o.stride[i]
+            assert np.array_equal(pool[d0:d0 + o.real_bytes[i]].cpu().numpy(), host[d0:d0 + o.real_bytes[i]])

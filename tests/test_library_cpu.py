@@ -139,3 +139,57 @@ def test_store_load_host_checks(lmc, fn):
     # nothing to move: returns OK without touching the device
     assert _raw_call(lmc, fn, L, 944, njobs=0) == lmc.LMC_OK
     assert _raw_call(lmc, fn, L, 944, njobs=0, null_jobs=True) == lmc.LMC_OK
+
+
+@pytest.mark.parametrize("cfg_index", [0, 1, 3, 4])
+def test_block_object_sizes_match_oracle(lmc, cfg_index):
+    cfg = W.CONFIGS[cfg_index]
+    for sep in (True, False):
+        p = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, 1 << 36, True, sep)
+        o = oracle.layout(cfg.layers, cfg.N, cfg.packed, 1 << 36, True, sep)
+        for nb in (1, 2, 3, 7):
+            for every in (False, True):
+                for g in range(o.num_object_groups):
+                    assert p.object_bytes_blocks(nb, every, g) == o.object_bytes_blocks(nb, every, g)
+        for g in range(o.num_object_groups):
+            assert p.object_bytes_blocks(2, False, g) == p.object_bytes(2 * cfg.N, g)
+    with pytest.raises(lmc.LmcError):
+        lmc.lmc_object_bytes_blocks(p, 0, lmc.LMC_KDA_LAST_BLOCK, 0)
+    with pytest.raises(lmc.LmcError):
+        lmc.lmc_object_bytes_blocks(p, 2, 7, 0)
+
+
+@pytest.mark.parametrize("fn", ["lmc_store_blocks", "lmc_load_blocks"])
+def test_block_store_load_host_checks(lmc, fn):
+    cfg = W.CONFIGS[1]
+    L = lmc.lmc_layout_build(cfg.layers, cfg.N, False, 1 << 34)
+    buf = (ctypes.c_uint8 * 64)()
+    addr = ctypes.addressof(buf)
+    tables = (lmc.lmc_block_table * L.num_kv_groups)(*[lmc.lmc_block_table(addr, 4, 4)] * L.num_kv_groups)
+    jobs = (ctypes.c_void_p * L.num_object_groups)(*[addr] * L.num_object_groups)
+    counts = (ctypes.c_int64 * L.num_object_groups)(*[0] * L.num_object_groups)
+    b = lmc.lmc_batch(2, L.num_kv_groups, tables, L.num_object_groups, 0, jobs, counts)
+    f = getattr(lmc._lib, fn)
+    assert f(L.handle, 0, 0, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+    assert f(L.handle, 2, 5, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+    assert f(L.handle, 2, 1, addr, ctypes.byref(b), addr, 64, addr + 1, None) == lmc.LMC_ERR_ALIGN
+    assert f(L.handle, 2, 1, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_OK  # nothing to move
+
+
+def test_copy_blocks_host_checks(lmc):
+    cfg = W.CONFIGS[1]
+    L = lmc.lmc_layout_build(cfg.layers, cfg.N, False, 1 << 34)
+    buf = (ctypes.c_uint8 * 64)()
+    addr = ctypes.addressof(buf)
+    g = L.num_kv_groups
+    pairs = (ctypes.c_void_p * g)(*[None] * g)
+    counts = (ctypes.c_int64 * g)(*[0] * g)
+    f = lmc._lib.lmc_copy_blocks
+    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts)), addr, None) == lmc.LMC_OK
+    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g - 1, 0, pairs, counts)), addr, None) \
+        == lmc.LMC_ERR_INVALID_ARG
+    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts)), addr + 2, None) \
+        == lmc.LMC_ERR_ALIGN
+    counts[1] = 3  # pairs given as NULL with a non-zero count
+    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts)), addr, None) \
+        == lmc.LMC_ERR_INVALID_ARG
