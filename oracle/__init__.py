@@ -64,7 +64,7 @@ def build(force: bool = False, out_path: str | None = None, src_path: str | None
     if out_path is not None or stale:
         tmp = out + f".tmp{os.getpid()}"
         subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-Werror",
-                        "-I", _HERE, src, "-o", tmp], check=True)
+                        "-I", _HERE, src, "-o", tmp, "-lm"], check=True)
         os.replace(tmp, out)
     return out
 
@@ -156,6 +156,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, P(_Tables),
                                        P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
     lib.or_copy_blocks.argtypes = [P(_Layout), ctypes.c_void_p, P(_CopyBatch), P(ctypes.c_uint32)]
+    for name in ("or_store_q8", "or_load_q8"):
+        getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, P(_Tables),
+                                       P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
+    lib.or_object_bytes_q8.argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+    lib.or_object_bytes_q8.restype = ctypes.c_int64
     lib.or_unified_block_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P(ctypes.c_int64)]
     return lib
 
@@ -232,6 +237,9 @@ class Layout:
 
     def object_bytes(self, C: int, og: int) -> int:
         return int(self._lib.or_object_bytes(ctypes.byref(self._c), int(C), int(og)))
+
+    def object_bytes_q8(self, C: int, d: int, og: int) -> int:
+        return int(self._lib.or_object_bytes_q8(ctypes.byref(self._c), int(C), int(d), int(og)))
 
     def object_bytes_blocks(self, nb: int, kda_every: bool, og: int) -> int:
         return int(self._lib.or_object_bytes_blocks(ctypes.byref(self._c), int(nb), int(bool(kda_every)), int(og)))
@@ -365,6 +373,30 @@ def load_blocks(L: Layout, nb: int, kda_every: bool, pool: np.ndarray, tables, j
                                ctypes.byref(T), ctypes.byref(J), arena.ctypes.data, arena.size, ctypes.byref(st))
     if rc != OK:
         raise OracleError(rc, "load_blocks")
+    return st.value
+
+
+def store_q8(L: Layout, C: int, d: int, pool: np.ndarray, tables, jobs, arena: np.ndarray) -> int:
+    """Chunk-form store with INT8 records for the KDA recurrent state
+    (rows of d fp32 values). Returns the status bits."""
+    assert pool.dtype == np.uint8 and arena.dtype == np.uint8 and arena.flags.writeable
+    T, J, keep = _marshal(L, tables, jobs)
+    st = ctypes.c_uint32(0)
+    rc = L._lib.or_store_q8(ctypes.byref(L._c), int(C), int(d), pool.ctypes.data, ctypes.byref(T),
+                            ctypes.byref(J), arena.ctypes.data, arena.size, ctypes.byref(st))
+    if rc != OK:
+        raise OracleError(rc, "store_q8")
+    return st.value
+
+
+def load_q8(L: Layout, C: int, d: int, pool: np.ndarray, tables, jobs, arena: np.ndarray) -> int:
+    assert pool.dtype == np.uint8 and arena.dtype == np.uint8 and pool.flags.writeable
+    T, J, keep = _marshal(L, tables, jobs)
+    st = ctypes.c_uint32(0)
+    rc = L._lib.or_load_q8(ctypes.byref(L._c), int(C), int(d), pool.ctypes.data, ctypes.byref(T),
+                           ctypes.byref(J), arena.ctypes.data, arena.size, ctypes.byref(st))
+    if rc != OK:
+        raise OracleError(rc, "load_q8")
     return st.value
 
 

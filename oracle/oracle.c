@@ -36,6 +36,7 @@
  * untouched bytes) and by an independent per-token brute force. The byte
  * order inside an object is a reading, not a value from the pages.
  */
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -301,18 +302,34 @@ int or_layout_build(or_layout *L)
  * group's layers in model order; a paged layer holds all nb pages (the
  * object's tokens), a KDA layer one state snapshot (the last block's), or
  * nb snapshots (one per block) when kda_every is set. */
-static int64_t object_bytes_nb(const or_layout *L, int64_t nb, int kda_every, int og)
+/* Bytes of a KDA page's INT8 record (codec below): conv bytes, one fp32
+ * scale per row of d values, one int8 code per value. */
+static int64_t q8_record_bytes(const or_layer *l, int64_t d)
+{
+    int64_t rows = l->rec_bytes / (4 * d);
+    return l->conv_bytes + 4 * rows + rows * d;
+}
+
+static int64_t object_bytes_q(const or_layout *L, int64_t nb, int kda_every, int64_t q8_row, int og)
 {
     int64_t total = 0;
     for (int i = 0; i < L->num_layers; i++) {
         if (L->object_group[i] != og)
             continue;
+        int64_t page = L->real_bytes[i];
+        if (L->layers[i].kind == OR_KDA && q8_row > 0)
+            page = q8_record_bytes(&L->layers[i], q8_row);
         if (L->layers[i].kind == OR_KDA && !kda_every)
-            total += L->real_bytes[i];
+            total += page;
         else
-            total += nb * L->real_bytes[i];
+            total += nb * page;
     }
     return total;
+}
+
+static int64_t object_bytes_nb(const or_layout *L, int64_t nb, int kda_every, int og)
+{
+    return object_bytes_q(L, nb, kda_every, 0, og);
 }
 
 /* Bytes of one object of group og for chunk size C (C / N blocks). */
@@ -362,6 +379,109 @@ static uint32_t copy_page(const or_layout *L, int layer, int64_t block,
     return 0;
 }
 
+/* ------------------------------------------------------------------ */
+/* INT8 per-channel codec of the KDA recurrent state ([MC] "Compressed  */
+/* Checkpoint Storage": the recurrent state is quantised to INT8 with   */
+/* per-channel parameters, the conv window kept in original precision). */
+/* Readings: the page is conv_state then recurrent_state (fp32, rows of */
+/* d values, row-major); a channel is one row; scale = max|x| / 127;    */
+/* q = x / scale rounded half to even, clamped to [-127, 127]; an      */
+/* all-zero row has scale 0 and codes 0; x' = q * scale. All in fp32.   */
+/* Record of one page: conv bytes, then rows fp32 scales, then         */
+/* rows * d int8 codes.                                                 */
+/* ------------------------------------------------------------------ */
+
+static void q8_encode(const uint8_t *page, uint8_t *rec, const or_layer *l, int64_t d)
+{
+    int64_t rows = l->rec_bytes / (4 * d);
+    memcpy(rec, page, (size_t)l->conv_bytes);
+    const uint8_t *x = page + l->conv_bytes;
+    uint8_t *scales = rec + l->conv_bytes;
+    int8_t *codes = (int8_t *)(rec + l->conv_bytes + 4 * rows);
+    for (int64_t r = 0; r < rows; r++) {
+        float amax = 0.0f;
+        for (int64_t j = 0; j < d; j++) {
+            float v;
+            memcpy(&v, x + 4 * (r * d + j), 4);
+            if (fabsf(v) > amax)
+                amax = fabsf(v);
+        }
+        float scale = amax / 127.0f;
+        memcpy(scales + 4 * r, &scale, 4);
+        for (int64_t j = 0; j < d; j++) {
+            float v;
+            memcpy(&v, x + 4 * (r * d + j), 4);
+            float q = 0.0f;
+            if (scale != 0.0f) {
+                q = rintf(v / scale);
+                if (q > 127.0f)
+                    q = 127.0f;
+                if (q < -127.0f)
+                    q = -127.0f;
+            }
+            codes[r * d + j] = (int8_t)q;
+        }
+    }
+}
+
+static void q8_decode(const uint8_t *rec, uint8_t *page, const or_layer *l, int64_t d)
+{
+    int64_t rows = l->rec_bytes / (4 * d);
+    memcpy(page, rec, (size_t)l->conv_bytes);
+    const uint8_t *scales = rec + l->conv_bytes;
+    const int8_t *codes = (const int8_t *)(rec + l->conv_bytes + 4 * rows);
+    uint8_t *x = page + l->conv_bytes;
+    for (int64_t r = 0; r < rows; r++) {
+        float scale;
+        memcpy(&scale, scales + 4 * r, 4);
+        for (int64_t j = 0; j < d; j++) {
+            float v = (float)codes[r * d + j] * scale;
+            memcpy(x + 4 * (r * d + j), &v, 4);
+        }
+    }
+}
+
+/* One KDA snapshot page <-> its compressed record (same checks as copy_page). */
+static uint32_t q8_page(const or_layout *L, int layer, int64_t block, uint8_t *pool, uint8_t *rec,
+                        int to_object, int64_t d, or_page_list *list, int64_t obj_offset)
+{
+    if (block == -1)
+        return OR_ST_NO_SNAPSHOT;
+    if (block < 0 || block >= L->num_blocks)
+        return OR_ST_BLOCK_OOR;
+    uint8_t *page = pool == NULL ? NULL : pool + L->base[layer] + block * L->stride[layer];
+    if (list != NULL) {
+        if (list->count < list->capacity) {
+            or_page *pg = &list->pages[list->count];
+            pg->pool_offset = L->base[layer] + block * L->stride[layer];
+            pg->object_offset = obj_offset;
+            pg->bytes = L->real_bytes[layer];
+            pg->layer = layer;
+            pg->block = (int32_t)block;
+        }
+        list->count++;
+        return 0;
+    }
+    if (to_object)
+        q8_encode(page, rec, &L->layers[layer], d);
+    else
+        q8_decode(rec, page, &L->layers[layer], d);
+    return 0;
+}
+
+/* Row length d accepted by the codec: 4 <= d <= 512, d % 4 == 0, and every
+ * KDA layer's recurrent state a whole number of rows. */
+static int q8_check(const or_layout *L, int64_t d)
+{
+    if (d < 4 || d > 512 || d % 4 != 0)
+        return OR_ERR_INVALID_ARG;
+    for (int i = 0; i < L->num_layers; i++)
+        if (L->layers[i].kind == OR_KDA &&
+            (L->layers[i].rec_bytes % (4 * d) != 0 || L->layers[i].conv_bytes % 16 != 0))
+            return OR_ERR_INVALID_ARG;
+    return OR_OK;
+}
+
 static int check_tables(const or_layout *L, const or_tables *T)
 {
     if (T == NULL || T->num_kv_groups != L->num_kv_groups || T->num_requests < 0)
@@ -380,6 +500,7 @@ typedef struct {
     int64_t nb;
     int first_is_block;
     int kda_every;
+    int64_t q8_row; /* > 0: KDA snapshots as INT8 records with rows of q8_row values */
 } obj_shape;
 
 /* Moves every object of every job, in either direction. */
@@ -398,7 +519,7 @@ static int move_objects(const or_layout *L, const obj_shape *sh, uint8_t *pool,
     int64_t nb = sh->nb;
 
     for (int og = 0; og < L->num_object_groups; og++) {
-        int64_t obj_size = object_bytes_nb(L, nb, sh->kda_every, og);
+        int64_t obj_size = object_bytes_q(L, nb, sh->kda_every, sh->q8_row, og);
         for (int64_t q = 0; q < J->num_jobs[og]; q++) {
             const or_job *job = &J->jobs[og][q];
             int64_t r = job->request;
@@ -426,11 +547,15 @@ static int move_objects(const or_layout *L, const obj_shape *sh, uint8_t *pool,
                     int64_t pos = first + nb - 1;
                     if (pos >= T->num_cols[k])
                         *status |= OR_ST_BAD_JOB;
+                    else if (sh->q8_row > 0)
+                        *status |= q8_page(L, i, row[pos], pool, obj + cursor, to_object,
+                                           sh->q8_row, list, job->offset + cursor);
                     else
                         *status |= copy_page(L, i, row[pos], pool, obj + cursor,
                                              to_object, OR_ST_NO_SNAPSHOT, list,
                                              job->offset + cursor);
-                    cursor += L->real_bytes[i];
+                    cursor += sh->q8_row > 0 ? q8_record_bytes(&L->layers[i], sh->q8_row)
+                                             : L->real_bytes[i];
                 } else if (L->layers[i].kind == OR_KDA) {
                     /* One snapshot per block boundary ([VB] §7, "all"-style
                      * snapshots kept per object). */
@@ -472,6 +597,7 @@ static int chunk_shape(const or_layout *L, int64_t C, obj_shape *sh)
     sh->nb = C / L->N;
     sh->first_is_block = 0;
     sh->kda_every = 0;
+    sh->q8_row = 0;
     return OR_OK;
 }
 
@@ -482,6 +608,7 @@ static int block_shape(int64_t nb, int kda_every, obj_shape *sh)
     sh->nb = nb;
     sh->first_is_block = 1;
     sh->kda_every = kda_every;
+    sh->q8_row = 0;
     return OR_OK;
 }
 
@@ -565,6 +692,49 @@ int or_list_pages(const or_layout *L, int64_t C, const or_tables *T, const or_jo
                   int64_t arena_bytes, uint32_t *status, or_page_list *list)
 {
     return or_list_pages_any(L, C, 0, 0, T, J, arena_bytes, status, list);
+}
+
+/* Chunk-form store/load with every KDA snapshot held as its INT8 record
+ * (paged layers unchanged). d = values per recurrent-state row. */
+int or_store_q8(const or_layout *L, int64_t C, int64_t d, const uint8_t *pool,
+                const or_tables *T, const or_jobs *J,
+                uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    obj_shape sh;
+    int rc = chunk_shape(L, C, &sh);
+    if (rc == OR_OK)
+        rc = q8_check(L, d);
+    if (rc != OR_OK)
+        return rc;
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    sh.q8_row = d;
+    return move_objects(L, &sh, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1, NULL);
+}
+
+int or_load_q8(const or_layout *L, int64_t C, int64_t d, uint8_t *pool,
+               const or_tables *T, const or_jobs *J,
+               const uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    obj_shape sh;
+    int rc = chunk_shape(L, C, &sh);
+    if (rc == OR_OK)
+        rc = q8_check(L, d);
+    if (rc != OR_OK)
+        return rc;
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    sh.q8_row = d;
+    return move_objects(L, &sh, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0, NULL);
+}
+
+/* Bytes of one chunk object of group og with compressed KDA records, or -1
+ * when d is not accepted. */
+int64_t or_object_bytes_q8(const or_layout *L, int64_t C, int64_t d, int og)
+{
+    if (q8_check(L, d) != OR_OK || C <= 0 || C % L->N != 0)
+        return -1;
+    return object_bytes_q(L, C / L->N, 0, d, og);
 }
 
 /* In-pool block copies ([MC] "Copy-on-Write", "Snapshot": a shared

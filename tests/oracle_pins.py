@@ -526,9 +526,147 @@ def check_copy_blocks(lib):
         assert np.array_equal(out, ref), "a bad pair must skip only itself"
 
 
+def _q8_case(lib, rows_x, d):
+    """A one-layer KDA layout whose single page holds `rows_x` (fp32) after a
+    16-byte conv part; returns (layout, pool, tables, jobs, arena size)."""
+    rows_x = np.asarray(rows_x, dtype=np.float32).reshape(-1, d)
+    spec = [{"kind": "KDA", "token_bytes": 0, "conv_bytes": 16, "rec_bytes": rows_x.size * 4, "window": 0},
+            W.mla(16)]
+    L = oracle.layout(spec, 1, True, 1 << 20, _lib=lib)
+    pool = np.zeros(L.pool_bytes, dtype=np.uint8)
+    b = 3
+    lo = L.base[0] + b * L.stride[0]
+    pool[lo:lo + 16] = np.arange(16, dtype=np.uint8)
+    pool[lo + 16:lo + 16 + rows_x.size * 4] = rows_x.view(np.uint8).reshape(-1)
+    kda_g, mla_g = L.kv_group[0], L.kv_group[1]
+    tables = [None, None]
+    tables[kda_g] = np.array([[b]], dtype=np.int32)
+    tables[mla_g] = np.array([[5]], dtype=np.int32)
+    size = L.object_bytes_q8(1, d, L.object_group[0])
+    jobs = [np.zeros(0, dtype=W.JOB_DTYPE) for _ in range(L.num_object_groups)]
+    jobs[L.object_group[0]] = np.array([(0, 0, 0)], dtype=W.JOB_DTYPE)
+    return L, pool, tables, jobs, size, rows_x, lo
+
+
+def check_q8_golden(lib):
+    """Worked rows: half-to-even ties, clamping at 127, zero rows, exact
+    round trips when the scale is a power of two."""
+    lines = [l.split("#")[0].strip() for l in open(os.path.join(GOLDEN, "q8_rows.txt"))]
+    lines = [l for l in lines if l]
+    for k in range(0, len(lines), 3):
+        x = np.array(lines[k].split(":")[1].split(), dtype=np.float32)
+        q = np.array(lines[k + 1].split(":")[1].split(), dtype=np.int8)
+        sc = np.float32(lines[k + 2].split(":")[1])
+        L, pool, tables, jobs, size, rows_x, lo = _q8_case(lib, x, 8)
+        assert size == 16 + 4 + 8
+        arena = np.zeros(size, dtype=np.uint8)
+        assert oracle.store_q8(L, 1, 8, pool, tables, jobs, arena) == 0
+        assert np.array_equal(arena[:16], np.arange(16, dtype=np.uint8)), "conv part must stay raw"
+        assert arena[16:20].view(np.float32)[0] == sc, (x, arena[16:20].view(np.float32))
+        assert np.array_equal(arena[20:28].view(np.int8), q), (x, arena[20:28].view(np.int8))
+        back = np.zeros_like(pool)
+        assert oracle.load_q8(L, 1, 8, back, tables, jobs, arena) == 0
+        got = back[lo + 16:lo + 48].view(np.float32)
+        assert np.array_equal(got, q.astype(np.float32) * sc)
+
+
+def q8_numpy(x, d):
+    """Independent float32 restatement of the codec for the pins."""
+    x = np.asarray(x, dtype=np.float32).reshape(-1, d)
+    amax = np.max(np.abs(x), axis=1)
+    scale = (amax / np.float32(127)).astype(np.float32)
+    safe = np.where(scale == 0, np.float32(1), scale).astype(np.float32)
+    q = np.rint((x / safe[:, None]).astype(np.float32))
+    q = np.where(scale[:, None] == 0, 0, np.clip(q, -127, 127)).astype(np.int8)
+    return scale, q
+
+
+def check_q8_random(lib):
+    """Random N(0,1) states (plus scaled and sparse rows): the C codec equals
+    the numpy restatement bit for bit, and every decoded value lies within
+    half a step of its input."""
+    rng = np.random.default_rng(31)
+    for d in (4, 8, 64, 128, 512):
+        rows = int(rng.integers(1, 40))
+        x = rng.standard_normal((rows, d)).astype(np.float32)
+        x[0] *= np.float32(1e-30)
+        x[-1, : d // 2] = 0
+        # a subnormal row: its scale (max/127) rounds coarsely, so x/scale can
+        # exceed 127.5 and the clamp to [-127, 127] decides the code
+        sub = np.zeros(d, dtype=np.float32)
+        sub[0] = np.float32(190 * 2.0 ** -149)
+        sub[1] = -np.float32(189 * 2.0 ** -149)
+        sub[2] = np.float32(37 * 2.0 ** -149)
+        x = np.vstack([x, sub[None, :]]).astype(np.float32)
+        rows += 1
+        if rows > 2:
+            x[1] = 0
+        L, pool, tables, jobs, size, rows_x, lo = _q8_case(lib, x, d)
+        arena = np.zeros(size, dtype=np.uint8)
+        assert oracle.store_q8(L, 1, d, pool, tables, jobs, arena) == 0
+        scale = arena[16:16 + 4 * rows].view(np.float32)
+        codes = arena[16 + 4 * rows:16 + 4 * rows + rows * d].view(np.int8).reshape(rows, d)
+        s_np, q_np = q8_numpy(x, d)
+        assert np.array_equal(scale, s_np) and np.array_equal(codes, q_np)
+        back = np.zeros_like(pool)
+        assert oracle.load_q8(L, 1, d, back, tables, jobs, arena) == 0
+        y = back[lo + 16:lo + 16 + 4 * rows * d].view(np.float32).reshape(rows, d)
+        err = np.abs(y.astype(np.float64) - x.astype(np.float64))
+        bound = scale.astype(np.float64)[:, None] * (0.5 + 1e-6) + 1e-45
+        assert (err[:-1] <= bound[:-1]).all()
+        assert (np.abs(codes) <= 127).all()
+        assert codes[-1, 0] == 127 and codes[-1, 1] == -127  # clamped (190 and -189 steps)
+    # a d that is not accepted is an argument error
+    L, pool, tables, jobs, size, rows_x, lo = _q8_case(lib, np.zeros(24, np.float32), 8)
+    for bad in (6, 0, 1024, 16):
+        try:
+            oracle.store_q8(L, 1, bad, pool, tables, jobs, np.zeros(4096, np.uint8))
+            raise AssertionError(f"row length {bad} accepted")
+        except oracle.OracleError as e:
+            assert e.code == oracle.ERR_INVALID_ARG
+
+
+def check_q8_objects(lib):
+    """In whole objects the codec touches only KDA pages: paged layers are
+    byte-identical to the plain store and objects shrink by the codec's
+    ratio; store_q8 then load_q8 restores conv bytes exactly and state
+    values within half a step."""
+    case = tiny_case(lib, 0)
+    L, C = case["L"], case["C"]
+    d = 64
+    sizes = [L.object_bytes_q8(C, d, g) for g in range(L.num_object_groups)]
+    kda_og = L.object_group[0]
+    rows = (4 * 64 * 64 * 4) // (4 * d)
+    assert sizes[kda_og] == 3 * (4608 + 4 * rows + rows * d)
+    jobs, nbytes = W.pack_jobs(W.store_units(case["lengths"], C, L.num_object_groups), sizes)
+    arena = np.zeros(nbytes, dtype=np.uint8)
+    assert oracle.store_q8(L, C, d, case["pool"], case["t_src"], jobs, arena) == 0
+    plain = np.zeros(case["arena_bytes"], dtype=np.uint8)
+    oracle.store(L, C, case["pool"], case["t_src"], case["jobs"], plain)
+    mla_og = 1 - kda_og
+    for a, b in zip(jobs[mla_og], case["jobs"][mla_og]):
+        n = sizes[mla_og]
+        assert np.array_equal(arena[int(a["offset"]):int(a["offset"]) + n], plain[int(b["offset"]):int(b["offset"]) + n])
+    dst = np.zeros(L.pool_bytes, dtype=np.uint8)
+    assert oracle.load_q8(L, C, d, dst, case["t_dst"], jobs, arena) == 0
+    m = C // L.N
+    for r, Lr in enumerate(case["lengths"]):
+        for c in range(int(Lr) // C):
+            for i in range(3):
+                g = L.kv_group[i]
+                src = L.base[i] + int(case["t_src"][g][r, (c + 1) * m - 1]) * L.stride[i]
+                out = L.base[i] + int(case["t_dst"][g][r, (c + 1) * m - 1]) * L.stride[i]
+                assert np.array_equal(dst[out:out + 4608], case["pool"][src:src + 4608])
+                x = case["pool"][src + 4608:src + 70144].view(np.float32).reshape(-1, d)
+                y = dst[out + 4608:out + 70144].view(np.float32).reshape(-1, d)
+                s_np, q_np = q8_numpy(x, d)
+                assert np.array_equal(y, q_np.astype(np.float32) * s_np[:, None])
+
+
 ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",
        "check_budget", "check_page_formulas", "check_unified_block_size", "check_k3_groups", "check_closed_forms",
-       "check_non_overlap", "check_store_load_cases", "check_block_objects", "check_copy_blocks"]
+       "check_non_overlap", "check_store_load_cases", "check_block_objects", "check_copy_blocks",
+       "check_q8_golden", "check_q8_random", "check_q8_objects"]
 
 
 def check_store_load_cases(lib):

@@ -35,13 +35,19 @@ MUTANTS = [
      "memmove(pool + L->base[i] + src * L->stride[i],\n                        pool + L->base[i] + dst * L->stride[i]"),
     ("copy skips a group's last layer", "                if (L->kv_group[i] != g)\n                    continue;\n                memmove",
      "                if (L->kv_group[i] != g || i == L->num_layers - 1)\n                    continue;\n                memmove"),
+    ("codec rounds half away from zero", "q = rintf(v / scale);", "q = roundf(v / scale);"),
+    ("codec scales by 128", "float scale = amax / 127.0f;", "float scale = amax / 128.0f;"),
+    ("codec does not clamp", "                if (q > 127.0f)\n                    q = 127.0f;", "                if (0)\n                    q = 127.0f;"),
+    ("codec drops the conv window", "    memcpy(rec, page, (size_t)l->conv_bytes);", "    memset(rec, 0, (size_t)l->conv_bytes);"),
+    ("codec record has no scales", "    return l->conv_bytes + 4 * rows + rows * d;", "    return l->conv_bytes + rows * d;"),
+    ("decoder ignores the scale", "float v = (float)codes[r * d + j] * scale;", "float v = (float)codes[r * d + j];"),
     ("copy accepts block ids past the pool", "dst < 0 || dst >= L->num_blocks", "dst < 0 || dst > L->num_blocks + 1000000"),
     ("page copy one byte short", "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer]);",
      "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer] - 1);"),
     ("misaligned object offsets accepted", "job->offset % 16 != 0 ||", ""),
     ("block id upper bound off by one", "block >= L->num_blocks", "block > L->num_blocks"),
-    ("object size counts KDA per block", "        if (L->layers[i].kind == OR_KDA && !kda_every)\n            total += L->real_bytes[i];",
-     "        if (0)\n            total += L->real_bytes[i];"),
+    ("object size counts KDA per block", "        if (L->layers[i].kind == OR_KDA && !kda_every)\n            total += page;",
+     "        if (0)\n            total += page;"),
 ]
 
 
