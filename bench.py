@@ -249,6 +249,15 @@ class PagingStep:
         C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
         build = functools.partial(lmc.lmc_layout_build, cfg.layers, cfg.N, cfg.packed)
         inp = W.make_inputs(cfg, build, C, ids)
+        if op == "q8":
+            # the same chunks with every KDA snapshot as an INT8 record
+            self.q8_row = W.state_row_elems(cfg)
+            full = [inp.layout.object_bytes(C, g) for g in range(inp.layout.num_object_groups)]
+            units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
+            inp.object_bytes = [inp.layout.object_bytes_q8(C, self.q8_row, g)
+                                for g in range(inp.layout.num_object_groups)]
+            self.full_payload = sum(full[g] * len(u) for g, u in enumerate(units))
+            inp.jobs, inp.arena_bytes = W.pack_jobs(units, inp.object_bytes)
         if op == "blocks":
             # the same chunks as block-granular objects holding one KDA
             # snapshot per block (every block boundary of the chunk)
@@ -288,13 +297,20 @@ class PagingStep:
             self.chunks = int(sum(int(x) // C for x in inp.lengths))
             self.launches_per_step = 2
         # every payload byte is read once and written once, by the store and by the load
-        self.bytes_per_step = 2 * (self.load_payload + self.store_payload)
+        self.store_bytes = 2 * self.store_payload
+        self.load_bytes = 2 * self.load_payload
+        if op == "q8":
+            # the store reads full pages and writes records; the load the reverse
+            self.store_bytes = self.load_bytes = self.full_payload + inp.payload_bytes
+        self.bytes_per_step = self.store_bytes + self.load_bytes
 
     def _store(self, pool, tables, jobs):
         lmc = self.lmc
         if self.op == "blocks":
             lmc.lmc_store_blocks(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, pool, tables, jobs, self.arena,
                                  self.status, self.main)
+        elif self.op == "q8":
+            lmc.lmc_store_q8(self.L, self.C, self.q8_row, pool, tables, jobs, self.arena, self.status, self.main)
         else:
             lmc.lmc_store(self.L, self.C, pool, tables, jobs, self.arena, self.status, self.main)
 
@@ -303,6 +319,8 @@ class PagingStep:
         if self.op == "blocks":
             lmc.lmc_load_blocks(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, pool, tables, jobs, self.arena,
                                 self.status, stream)
+        elif self.op == "q8":
+            lmc.lmc_load_q8(self.L, self.C, self.q8_row, pool, tables, jobs, self.arena, self.status, stream)
         else:
             lmc.lmc_load(self.L, self.C, pool, tables, jobs, self.arena, self.status, stream)
 
@@ -460,6 +478,7 @@ class CopyStep:
         self.pairs = [lmc.pairs_to_device(p, dev) for p in pairs]
         self.h_pairs = pairs
         self.store_payload, self.load_payload = moved, 0
+        self.store_bytes, self.load_bytes = 2 * moved, 0
         self.bytes_per_step = 2 * moved
         self.chunks = sum(len(p) for p in pairs)
 
@@ -568,9 +587,9 @@ def run_gpu(args):
         # the two kernels share HBM concurrently: the roofline is the step's
         dominant, dom_bytes, dom_ms = "store+load (concurrent)", S.bytes_per_step, ms_per_step
     elif st_avg >= ld_avg:
-        dominant, dom_bytes, dom_ms = "store", 2 * S.store_payload, st_avg
+        dominant, dom_bytes, dom_ms = "store", S.store_bytes, st_avg
     else:
-        dominant, dom_bytes, dom_ms = "load", 2 * S.load_payload, ld_avg
+        dominant, dom_bytes, dom_ms = "load", S.load_bytes, ld_avg
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -585,8 +604,8 @@ def run_gpu(args):
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "chunks_per_s": round(S.chunks * world / (ms_per_step * 1e-3), 1),
-        "store": {"ms": round(st_avg, 4), "gbs": _gbs(2 * S.store_payload, st_avg)},
-        "load": {"ms": round(ld_avg, 4), "gbs": _gbs(2 * S.load_payload, ld_avg)},
+        "store": {"ms": round(st_avg, 4), "gbs": _gbs(S.store_bytes, st_avg)},
+        "load": {"ms": round(ld_avg, 4), "gbs": _gbs(S.load_bytes, ld_avg)},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -615,9 +634,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--impl", choices=["lmc", "reference"], default="lmc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["paging", "blocks", "copy"], default="paging",
+    ap.add_argument("--op", choices=["paging", "blocks", "copy", "q8"], default="paging",
                     help="paging: store + load by chunk; blocks: block-granular objects with one KDA "
-                         "snapshot per block; copy: in-pool copy of every KDA snapshot")
+                         "snapshot per block; copy: in-pool copy of every KDA snapshot; q8: store + load "
+                         "with KDA snapshots as INT8 records")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -297,6 +297,35 @@ typedef struct {
 int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy_batch *batch, uint32_t *status,
                     void *stream);
 
+/* ---- INT8 per-channel codec of the KDA recurrent state ------------------- */
+
+/* Chunk-form store/load that keeps every KDA snapshot as an INT8 record
+ * ([MC] "Compressed Checkpoint Storage": inactive recurrent states are
+ * compressed to INT8 with per-channel parameters; the convolution window
+ * keeps its original precision; a hit is decoded back to full precision).
+ * The page is read as conv_state (conv_bytes, copied as is) followed by the
+ * fp32 recurrent state in rows of `row_elems` values (heads * d rows of d for
+ * a (heads, d, d) state). Per row: scale = max|x| / 127; code = x / scale
+ * rounded half to even, clamped to [-127, 127]; an all-zero row has scale 0;
+ * decoded value = code * scale; all IEEE binary32. A KDA layer's record in the
+ * object: conv bytes, then one fp32 scale per row, then the int8 codes, row
+ * by row. Paged layers are stored exactly as by lmc_store. Lossy: a decoded
+ * value lies within half a step (scale / 2) of the original.
+ * Requires 4 <= row_elems <= 512, row_elems % 4 == 0, every KDA layer's
+ * recurrent state a whole number of rows and a multiple of 4 rows, and
+ * conv_bytes a multiple of 16, so records stay multiples of 16 bytes
+ * (INVALID_ARG otherwise), and 16-byte aligned pool and arena (ALIGN).
+ * Other arguments, status bits and errors as lmc_store / lmc_load. */
+int lmc_store_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, const void *pool,
+                 const lmc_batch *batch, void *arena, int64_t arena_bytes, uint32_t *status, void *stream);
+int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, void *pool,
+                const lmc_batch *batch, const void *arena, int64_t arena_bytes, uint32_t *status,
+                void *stream);
+
+/* Bytes of one chunk object of `object_group` as lmc_store_q8 writes it. */
+int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, int32_t object_group,
+                        int64_t *out);
+
 /* Static description of a code ("LMC_OK", ...); never NULL. */
 const char *lmc_strerror(int code);
 

@@ -469,15 +469,18 @@ static uint32_t q8_page(const or_layout *L, int layer, int64_t block, uint8_t *p
     return 0;
 }
 
-/* Row length d accepted by the codec: 4 <= d <= 512, d % 4 == 0, and every
- * KDA layer's recurrent state a whole number of rows. */
+/* Row length d accepted by the codec: 4 <= d <= 512, d % 4 == 0, every KDA
+ * layer's recurrent state a whole number of rows, a multiple of 4 rows, and
+ * conv bytes a multiple of 16, so that every record (and every object) stays
+ * a multiple of 16 bytes. */
 static int q8_check(const or_layout *L, int64_t d)
 {
     if (d < 4 || d > 512 || d % 4 != 0)
         return OR_ERR_INVALID_ARG;
     for (int i = 0; i < L->num_layers; i++)
         if (L->layers[i].kind == OR_KDA &&
-            (L->layers[i].rec_bytes % (4 * d) != 0 || L->layers[i].conv_bytes % 16 != 0))
+            (L->layers[i].rec_bytes % (4 * d) != 0 || (L->layers[i].rec_bytes / (4 * d)) % 4 != 0 ||
+             L->layers[i].conv_bytes % 16 != 0))
             return OR_ERR_INVALID_ARG;
     return OR_OK;
 }

@@ -125,6 +125,10 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
                                       ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p]
     so.lmc_copy_blocks.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(lmc_copy_batch), ctypes.c_void_p,
                                    ctypes.c_void_p]
+    for name in ("lmc_store_q8", "lmc_load_q8"):
+        getattr(so, name).argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
+                                      _i64, ctypes.c_void_p, ctypes.c_void_p]
+    so.lmc_object_bytes_q8.argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_int32, _P(_i64)]
     so.lmc_strerror.argtypes = [ctypes.c_int]
     so.lmc_strerror.restype = ctypes.c_char_p
     return so
@@ -213,6 +217,9 @@ class Layout:
 
     def object_bytes(self, chunk: int, object_group: int) -> int:
         return lmc_object_bytes(self, chunk, object_group)
+
+    def object_bytes_q8(self, chunk: int, row_elems: int, object_group: int) -> int:
+        return lmc_object_bytes_q8(self, chunk, row_elems, object_group)
 
     def object_bytes_blocks(self, blocks_per_object: int, kda_every: bool, object_group: int) -> int:
         return lmc_object_bytes_blocks(self, blocks_per_object,
@@ -340,6 +347,32 @@ def lmc_load_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool,
     _check(_lib.lmc_load_blocks(layout.handle, int(blocks_per_object), int(kda_mode), pool.data_ptr(),
                                 ctypes.byref(b), arena.data_ptr(), arena.numel() * arena.element_size(),
                                 status.data_ptr(), _stream_ptr(stream)), "lmc_load_blocks")
+
+
+def lmc_object_bytes_q8(layout: Layout, chunk: int, row_elems: int, object_group: int) -> int:
+    out = _i64(0)
+    _check(_lib.lmc_object_bytes_q8(layout.handle, int(chunk), int(row_elems), int(object_group),
+                                    ctypes.byref(out)), "lmc_object_bytes_q8")
+    return out.value
+
+
+def lmc_store_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, arena, status,
+                 stream=None) -> None:
+    """Chunk store with KDA snapshots as INT8 records (rows of `row_elems`)."""
+    _check_pool(layout, pool)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_store_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
+                             arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
+                             _stream_ptr(stream)), "lmc_store_q8")
+
+
+def lmc_load_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, arena, status,
+                stream=None) -> None:
+    _check_pool(layout, pool)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_load_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
+                            arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
+                            _stream_ptr(stream)), "lmc_load_q8")
 
 
 def pairs_to_device(pairs: np.ndarray, device):

@@ -87,7 +87,9 @@ struct Entry {
     int32_t pos_add;      // block position = first + pos_add + page index
     int16_t kv;           // KV group (block table)
     uint8_t kda;          // 1: a KDA state page (a missing one is NO_SNAPSHOT)
-    uint8_t pad;
+    uint8_t codec;        // 1: INT8 record of the recurrent state (see below)
+    int32_t rows;         // codec: state rows of the page; tile_bytes holds rows per tile
+    int32_t pad;
 };
 
 struct Group {
@@ -118,6 +120,8 @@ struct Plan {
     int32_t num_requests;
     int32_t num_groups;
     int32_t mode;
+    int32_t q8_row;  // codec: values per recurrent-state row (0: no codec)
+    int32_t pad;
     Group groups[kMaxGroups];
     Table tables[kMaxKv];
     Entry entries[kMaxEntries];
@@ -156,10 +160,14 @@ __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
 struct Span {
     const uint8_t *src;
     uint8_t *dst;
-    int32_t bytes;
+    int32_t bytes;   // plain copy: bytes; codec: rows
+    int32_t codec;   // 0: plain copy, 1: encode (store), 2: decode (load)
+    uint8_t *scales; // codec: the rows' fp32 scales (written on encode, read on decode)
 };
 
 // Resolves tile -> span; returns the status bits to raise (0: copy it).
+// kCodec compiles in the codec entries (only the INT8 kernels carry them).
+template <bool kCodec>
 __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s) {
     // group: the last one whose first tile is <= tile
     int g = 0, gh = P.num_groups - 1;
@@ -190,6 +198,8 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
     const int32_t k = u - j * E.tiles_per_seg;
     const int64_t piece = (int64_t)k * E.tile_bytes;
     s.bytes = min(E.tile_bytes, (int32_t)(E.seg_bytes - piece));
+    s.codec = 0;
+    s.scales = nullptr;
 
     if (P.mode == kCopy) {
         const lmc_block_pair pr = static_cast<const lmc_block_pair *>(G.items)[q];
@@ -217,6 +227,29 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
     if (block < 0 || block >= P.num_blocks)
         return LMC_ST_BLOCK_OOR;
 
+    if (kCodec && E.codec) {
+        // rows [k * R, k * R + n) of the page's recurrent state, which starts
+        // after the conv bytes (seg_bytes); the record holds the scales at
+        // obj_off and the codes after all the scales
+        const int64_t row0 = (int64_t)k * E.tile_bytes;
+        const int32_t n = min(E.tile_bytes, (int32_t)(E.rows - row0));
+        const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + E.seg_bytes + row0 * 4 * P.q8_row;
+        const int64_t rec = job.offset + E.obj_off;
+        const int64_t codes = rec + 4 * (int64_t)E.rows + row0 * P.q8_row;
+        s.bytes = n;
+        if (P.mode == kStore) {
+            s.codec = 1;
+            s.src = P.src_base + page;
+            s.dst = P.dst_base + codes;
+            s.scales = P.dst_base + rec + 4 * row0;
+        } else {
+            s.codec = 2;
+            s.src = P.src_base + codes;
+            s.dst = P.dst_base + page;
+            s.scales = const_cast<uint8_t *>(P.src_base) + rec + 4 * row0;
+        }
+        return 0;
+    }
     const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + piece;
     const int64_t obj = job.offset + E.obj_off + (int64_t)j * E.seg_bytes + piece;
     s.src = P.src_base + (P.mode == kStore ? page : obj);
@@ -224,19 +257,91 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
     return 0;
 }
 
+// INT8 per-channel codec of the KDA recurrent state ("When Prefix Cache
+// Meets KDA", Compressed Checkpoint Storage): one warp per row of d fp32
+// values; scale = max|x| / 127, code = x / scale rounded half to even and
+// clamped to [-127, 127] (IEEE binary32 division), zero rows give scale 0
+// and codes 0; decode = code * scale. d % 4 == 0 and d <= 512, so a lane
+// holds at most 4 float4 of a row.
+constexpr int kMaxRowVec = 4;
+
+__device__ __forceinline__ void encode_rows(const Span &s, int d) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nvec = d >> 2;
+    for (int r = warp; r < s.bytes; r += kThreads / 32) {
+        const float4 *x = reinterpret_cast<const float4 *>(s.src) + (int64_t)r * nvec;
+        float4 v[kMaxRowVec];
+        float amax = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kMaxRowVec; w++) {
+            const int e = lane + 32 * w;
+            if (e < nvec) {
+                v[w] = __ldg(x + e);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[w].x), fabsf(v[w].y)), fmaxf(fabsf(v[w].z), fabsf(v[w].w))));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float scale = __fdiv_rn(amax, 127.0f);
+        if (lane == 0)
+            reinterpret_cast<float *>(s.scales)[r] = scale;
+        uint32_t *q = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d);
+#pragma unroll
+        for (int w = 0; w < kMaxRowVec; w++) {
+            const int e = lane + 32 * w;
+            if (e < nvec) {
+                const float c[4] = {v[w].x, v[w].y, v[w].z, v[w].w};
+                uint32_t packed = 0;
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    int qi = 0;
+                    if (scale != 0.0f)
+                        qi = max(-127, min(127, __float2int_rn(__fdiv_rn(c[t], scale))));
+                    packed |= (uint32_t)(uint8_t)(int8_t)qi << (8 * t);
+                }
+                q[e] = packed;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void decode_rows(const Span &s, int d) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nvec = d >> 2;
+    for (int r = warp; r < s.bytes; r += kThreads / 32) {
+        const float scale = __ldg(reinterpret_cast<const float *>(s.scales) + r);
+        const uint32_t *q = reinterpret_cast<const uint32_t *>(s.src + (int64_t)r * d);
+        float4 *x = reinterpret_cast<float4 *>(s.dst) + (int64_t)r * nvec;
+        for (int e = lane; e < nvec; e += 32) {
+            const uint32_t p = __ldg(q + e);
+            float4 o;
+            o.x = (float)(int8_t)(p & 0xffu) * scale;
+            o.y = (float)(int8_t)((p >> 8) & 0xffu) * scale;
+            o.z = (float)(int8_t)((p >> 16) & 0xffu) * scale;
+            o.w = (float)(int8_t)(p >> 24) * scale;
+            x[e] = o;
+        }
+    }
+}
+
 // Vector engine: every thread of the CTA copies 16-byte vectors of the tile,
 // kUnroll loads in flight before the matching stores.
-template <bool kVec>
+template <bool kVec, bool kCodec>
 __device__ __forceinline__ void copy_tiles(const Plan &P) {
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
         Span s;
-        const uint32_t bad = resolve(P, tile, s);
+        const uint32_t bad = resolve<kCodec>(P, tile, s);
         if (bad) {
             if (threadIdx.x == 0)
                 atomicOr(P.status, bad);
             continue;
         }
-        if (kVec) {
+        if (kCodec && s.codec == 1) {
+            encode_rows(s, P.q8_row);
+        } else if (kCodec && s.codec == 2) {
+            decode_rows(s, P.q8_row);
+        } else if (kVec) {
             const uint4 *src = reinterpret_cast<const uint4 *>(s.src);
             uint4 *dst = reinterpret_cast<uint4 *>(s.dst);
             const int n = s.bytes >> 4;
@@ -263,15 +368,21 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
 // which side is the pool).
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_store_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<kVec>(P);
+    copy_tiles<kVec, false>(P);
 }
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_load_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<kVec>(P);
+    copy_tiles<kVec, false>(P);
 }
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_copy_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<kVec>(P);
+    copy_tiles<kVec, false>(P);
+}
+__global__ void __launch_bounds__(kThreads) lmc_store_q8_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<true, true>(P);
+}
+__global__ void __launch_bounds__(kThreads) lmc_load_q8_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<true, true>(P);
 }
 
 // ---------------------------------------------------------------------------
@@ -359,7 +470,7 @@ __device__ __forceinline__ void bulk_tiles(const Plan &P) {
             state[s] = -1;
             return;
         }
-        const uint32_t bad = resolve(P, next, span[s]);
+        const uint32_t bad = resolve<false>(P, next, span[s]);
         next += gridDim.x;
         if (bad) {
             atomicOr(P.status, bad);
@@ -470,6 +581,36 @@ int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t 
     return LMC_OK;
 }
 
+// Appends the codec entry of a KDA layer: the recurrent state after the conv
+// bytes, encoded as an INT8 record (scales, then codes) at the object's
+// current offset; `rows_per_tile` rows per tile.
+int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_spec &spec, int32_t pos_add,
+                    int64_t &obj, int64_t &tiles) {
+    if (ne >= kMaxEntries)
+        return LMC_ERR_INVALID_ARG;
+    const int64_t row = P.q8_row;
+    const int64_t rows = spec.rec_bytes / (4 * row);
+    if (rows > INT32_MAX || spec.conv_bytes > INT32_MAX)
+        return LMC_ERR_INVALID_ARG;
+    const int32_t per_tile = (int32_t)std::max<int64_t>(1, kTileBytes / (4 * row));
+    Entry &E = P.entries[ne++];
+    E.pool_base = d.base;
+    E.pool_stride = d.stride;
+    E.obj_off = obj;
+    E.seg_bytes = (int32_t)spec.conv_bytes;  // the state starts after the conv bytes
+    E.tile_bytes = per_tile;
+    E.rows = (int32_t)rows;
+    E.tiles_per_seg = (int32_t)((rows + per_tile - 1) / per_tile);
+    E.tile_start = (int32_t)tiles;
+    E.kda = 1;
+    E.codec = 1;
+    E.pos_add = pos_add;
+    E.kv = (int16_t)d.kv_group;
+    obj += 4 * rows + rows * row;
+    tiles += E.tiles_per_seg;
+    return tiles > INT32_MAX ? LMC_ERR_OVERFLOW : LMC_OK;
+}
+
 // Adds a group of `n` items to the plan's tile space.
 int close_group(Plan &P, int ne, int first_entry, const void *items, int64_t n, int64_t obj, int64_t tiles,
                 int64_t &total) {
@@ -496,6 +637,7 @@ struct Shape {
     int64_t nb;
     int32_t pos_mul;
     bool kda_every;
+    int32_t q8_row;  // > 0: KDA snapshots as INT8 records with rows of q8_row values
 };
 
 // Host-side validation and launch plan of a store or load.
@@ -517,6 +659,7 @@ int build_object_plan(const lmc_layout *L, const Shape &sh, const void *pool, co
 
     std::memset(&P, 0, sizeof(P));
     P.pos_mul = sh.pos_mul;
+    P.q8_row = sh.q8_row;
     P.num_requests = b->num_requests;
     P.num_blocks = L->num_blocks;
     P.arena_bytes = arena_bytes;
@@ -544,8 +687,19 @@ int build_object_plan(const lmc_layout *L, const Shape &sh, const void *pool, co
         for (int32_t i : L->object_group_layers[og]) {
             const lmc_layer_desc &d = L->desc[i];
             const bool last_only = d.kind == LMC_LAYER_KDA && !sh.kda_every;
-            const int rc = add_entry(P, ne, d, last_only ? 1 : sh.nb, last_only ? (int32_t)(sh.nb - 1) : 0,
-                                     obj, tiles, vec);
+            int rc;
+            if (d.kind == LMC_LAYER_KDA && sh.q8_row > 0) {
+                // the conv window is copied as is, the state goes through the codec
+                lmc_layer_desc conv = d;
+                conv.real_bytes = L->specs[i].conv_bytes;
+                rc = conv.real_bytes > 0 ? add_entry(P, ne, conv, 1, (int32_t)(sh.nb - 1), obj, tiles, vec)
+                                         : LMC_OK;
+                if (rc == LMC_OK)
+                    rc = add_codec_entry(P, ne, d, L->specs[i], (int32_t)(sh.nb - 1), obj, tiles);
+            } else {
+                rc = add_entry(P, ne, d, last_only ? 1 : sh.nb, last_only ? (int32_t)(sh.nb - 1) : 0, obj, tiles,
+                               vec);
+            }
             if (rc != LMC_OK)
                 return rc;
         }
@@ -568,7 +722,7 @@ int launch_plan(const Plan &P, bool vec, void *stream) {
     if (sms <= 0)
         return LMC_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec && kEngine == 1 && P.mode != kCopy) {
+    if (vec && kEngine == 1 && P.mode != kCopy && P.q8_row == 0) {
         // persistent: kBulkCtasPerSm CTAs per SM, each a ring of stages
         const size_t smem = (size_t)kBulkStages * kTileBytes;
         auto kern = P.mode == kStore ? lmc_store_bulk_kernel<kBulkStages> : lmc_load_bulk_kernel<kBulkStages>;
@@ -580,7 +734,9 @@ int launch_plan(const Plan &P, bool vec, void *stream) {
         // one CTA per tile, capped; the kernel strides over the rest
         const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * 2048);
         void (*kern)(const Plan);
-        if (P.mode == kStore)
+        if (P.q8_row > 0)
+            kern = P.mode == kStore ? lmc_store_q8_kernel : lmc_load_q8_kernel;
+        else if (P.mode == kStore)
             kern = vec ? lmc_store_kernel<true> : lmc_store_kernel<false>;
         else if (P.mode == kLoad)
             kern = vec ? lmc_load_kernel<true> : lmc_load_kernel<false>;
@@ -599,7 +755,7 @@ int chunk_shape(const lmc_layout *L, int64_t chunk, Shape &sh) {
     const int64_t m = chunk / L->block_size;
     if (m > INT32_MAX)
         return LMC_ERR_OVERFLOW;
-    sh = Shape{m, (int32_t)m, false};
+    sh = Shape{m, (int32_t)m, false, 0};
     return LMC_OK;
 }
 
@@ -607,7 +763,7 @@ int block_shape(const lmc_layout *L, int64_t nb, int32_t kda_mode, Shape &sh) {
     if (L == nullptr || nb <= 0 || nb > INT32_MAX ||
         (kda_mode != LMC_KDA_LAST_BLOCK && kda_mode != LMC_KDA_EVERY_BLOCK))
         return LMC_ERR_INVALID_ARG;
-    sh = Shape{nb, 1, kda_mode == LMC_KDA_EVERY_BLOCK};
+    sh = Shape{nb, 1, kda_mode == LMC_KDA_EVERY_BLOCK, 0};
     return LMC_OK;
 }
 
@@ -616,7 +772,29 @@ int run_objects(const lmc_layout *L, const Shape &sh, const void *pool, const lm
     Plan P;
     bool vec = false;
     const int rc = build_object_plan(L, sh, pool, b, arena, arena_bytes, status, mode, P, vec);
-    return rc != LMC_OK ? rc : launch_plan(P, vec, stream);
+    if (rc != LMC_OK)
+        return rc;
+    if (sh.q8_row > 0 && !vec)
+        return LMC_ERR_ALIGN;  // the codec reads and writes rows as 16-byte vectors
+    return launch_plan(P, vec, stream);
+}
+
+// Row lengths the codec accepts: 4 <= d <= 512, d % 4 == 0, every KDA
+// layer's recurrent state a whole number of rows and a multiple of 4 rows,
+// and its conv bytes a multiple of 16: every record stays a multiple of 16
+// bytes, so the rows behind it remain 16-byte aligned.
+int q8_shape(const lmc_layout *L, int64_t chunk, int64_t d, Shape &sh) {
+    const int rc = chunk_shape(L, chunk, sh);
+    if (rc != LMC_OK)
+        return rc;
+    if (d < 4 || d > 4 * 32 * kMaxRowVec || d % 4 != 0)
+        return LMC_ERR_INVALID_ARG;
+    for (const lmc_layer_spec &spec : L->specs)
+        if (spec.kind == LMC_LAYER_KDA && (spec.rec_bytes % (4 * d) != 0 || (spec.rec_bytes / (4 * d)) % 4 != 0 ||
+                                           spec.conv_bytes % 16 != 0))
+            return LMC_ERR_INVALID_ARG;
+    sh.q8_row = (int32_t)d;
+    return LMC_OK;
 }
 
 }  // namespace
@@ -695,4 +873,45 @@ extern "C" int lmc_copy_blocks(const lmc_layout *L, void *pool, const lmc_copy_b
     P.src_base = static_cast<const uint8_t *>(pool);
     P.dst_base = static_cast<uint8_t *>(pool);
     return launch_plan(P, vec, stream);
+}
+
+extern "C" int lmc_store_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, const void *pool,
+                            const lmc_batch *batch, void *arena, int64_t arena_bytes, uint32_t *status,
+                            void *stream) {
+    Shape sh;
+    const int rc = q8_shape(layout, chunk_size, row_elems, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kStore);
+}
+
+extern "C" int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, void *pool,
+                           const lmc_batch *batch, const void *arena, int64_t arena_bytes, uint32_t *status,
+                           void *stream) {
+    Shape sh;
+    const int rc = q8_shape(layout, chunk_size, row_elems, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kLoad);
+}
+
+extern "C" int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems,
+                                   int32_t object_group, int64_t *out) {
+    Shape sh;
+    int rc = q8_shape(layout, chunk_size, row_elems, sh);
+    if (rc != LMC_OK)
+        return rc;
+    if (out == nullptr || object_group < 0 || (size_t)object_group >= layout->object_group_layers.size())
+        return LMC_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int32_t i : layout->object_group_layers[object_group]) {
+        const lmc_layer_spec &spec = layout->specs[i];
+        int64_t part;
+        if (spec.kind == LMC_LAYER_KDA) {
+            const int64_t rows = spec.rec_bytes / (4 * row_elems);
+            part = spec.conv_bytes + 4 * rows + rows * row_elems;
+        } else if (!lmc::mul_ok(sh.nb, layout->desc[i].real_bytes, &part)) {
+            return LMC_ERR_OVERFLOW;
+        }
+        if (!lmc::add_ok(total, part, &total))
+            return LMC_ERR_OVERFLOW;
+    }
+    *out = total;
+    return LMC_OK;
 }

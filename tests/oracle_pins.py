@@ -553,21 +553,25 @@ def check_q8_golden(lib):
     round trips when the scale is a power of two."""
     lines = [l.split("#")[0].strip() for l in open(os.path.join(GOLDEN, "q8_rows.txt"))]
     lines = [l for l in lines if l]
+    xs, qs, ss = [], [], []
     for k in range(0, len(lines), 3):
-        x = np.array(lines[k].split(":")[1].split(), dtype=np.float32)
-        q = np.array(lines[k + 1].split(":")[1].split(), dtype=np.int8)
-        sc = np.float32(lines[k + 2].split(":")[1])
-        L, pool, tables, jobs, size, rows_x, lo = _q8_case(lib, x, 8)
-        assert size == 16 + 4 + 8
-        arena = np.zeros(size, dtype=np.uint8)
-        assert oracle.store_q8(L, 1, 8, pool, tables, jobs, arena) == 0
-        assert np.array_equal(arena[:16], np.arange(16, dtype=np.uint8)), "conv part must stay raw"
-        assert arena[16:20].view(np.float32)[0] == sc, (x, arena[16:20].view(np.float32))
-        assert np.array_equal(arena[20:28].view(np.int8), q), (x, arena[20:28].view(np.int8))
-        back = np.zeros_like(pool)
-        assert oracle.load_q8(L, 1, 8, back, tables, jobs, arena) == 0
-        got = back[lo + 16:lo + 48].view(np.float32)
-        assert np.array_equal(got, q.astype(np.float32) * sc)
+        xs.append(np.array(lines[k].split(":")[1].split(), dtype=np.float32))
+        qs.append(np.array(lines[k + 1].split(":")[1].split(), dtype=np.int8))
+        ss.append(np.float32(lines[k + 2].split(":")[1]))
+    n = len(xs)
+    assert n % 4 == 0  # records keep whole groups of 4 rows
+    x, q, sc = np.stack(xs), np.stack(qs), np.array(ss, dtype=np.float32)
+    L, pool, tables, jobs, size, rows_x, lo = _q8_case(lib, x, 8)
+    assert size == 16 + 4 * n + 8 * n
+    arena = np.zeros(size, dtype=np.uint8)
+    assert oracle.store_q8(L, 1, 8, pool, tables, jobs, arena) == 0
+    assert np.array_equal(arena[:16], np.arange(16, dtype=np.uint8)), "conv part must stay raw"
+    assert np.array_equal(arena[16:16 + 4 * n].view(np.float32), sc), arena[16:16 + 4 * n].view(np.float32)
+    assert np.array_equal(arena[16 + 4 * n:].view(np.int8).reshape(n, 8), q), arena[16 + 4 * n:].view(np.int8)
+    back = np.zeros_like(pool)
+    assert oracle.load_q8(L, 1, 8, back, tables, jobs, arena) == 0
+    got = back[lo + 16:lo + 16 + 32 * n].view(np.float32).reshape(n, 8)
+    assert np.array_equal(got, q.astype(np.float32) * sc[:, None])
 
 
 def q8_numpy(x, d):
@@ -587,7 +591,7 @@ def check_q8_random(lib):
     half a step of its input."""
     rng = np.random.default_rng(31)
     for d in (4, 8, 64, 128, 512):
-        rows = int(rng.integers(1, 40))
+        rows = 4 * int(rng.integers(1, 10)) - 1  # plus the subnormal row below: a multiple of 4
         x = rng.standard_normal((rows, d)).astype(np.float32)
         x[0] *= np.float32(1e-30)
         x[-1, : d // 2] = 0
@@ -617,8 +621,8 @@ def check_q8_random(lib):
         assert (np.abs(codes) <= 127).all()
         assert codes[-1, 0] == 127 and codes[-1, 1] == -127  # clamped (190 and -189 steps)
     # a d that is not accepted is an argument error
-    L, pool, tables, jobs, size, rows_x, lo = _q8_case(lib, np.zeros(24, np.float32), 8)
-    for bad in (6, 0, 1024, 16):
+    L, pool, tables, jobs, size, rows_x, lo = _q8_case(lib, np.zeros(96, np.float32), 8)
+    for bad in (6, 0, 1024, 16, 32, 36):  # 16, 32: 6 and 3 rows (not 4k); 36: not whole rows
         try:
             oracle.store_q8(L, 1, bad, pool, tables, jobs, np.zeros(4096, np.uint8))
             raise AssertionError(f"row length {bad} accepted")

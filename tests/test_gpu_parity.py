@@ -525,3 +525,119 @@ def test_copy_blocks_full_size_kda_states(lmc):
         for i in layers:
             d0 = o.base[i] + int(pr["dst_block"]) * o.stride[i]
             assert np.array_equal(pool[d0:d0 + o.real_bytes[i]].cpu().numpy(), host[d0:d0 + o.real_bytes[i]])
+
+
+# ---------------------------------------------------------------------------
+# INT8 per-channel codec of the KDA recurrent state
+# ---------------------------------------------------------------------------
+
+def _q8_exact(lmc, inp, Lp, d, pool_h):
+    Lo, C = inp.layout, inp.C
+    sizes = [Lo.object_bytes_q8(C, d, g) for g in range(Lo.num_object_groups)]
+    for g in range(Lo.num_object_groups):
+        assert Lp.object_bytes_q8(C, d, g) == sizes[g]
+    units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
+    jobs, nbytes = W.pack_jobs(units, sizes)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    arena = torch.full((nbytes,), 0x3C, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    dj = dev_jobs(jobs, DEV)
+    lmc.lmc_store_q8(Lp, C, d, pool, dev_tables(inp.tables_src, DEV), dj, arena, st)
+    lmc.lmc_load_q8(Lp, C, d, fresh, dev_tables(inp.tables_dst, DEV), dj, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    arena_o = np.full(nbytes, 0x3C, dtype=np.uint8)
+    assert oracle.store_q8(Lo, C, d, pool_h, inp.tables_src, jobs, arena_o) == 0
+    fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    assert oracle.load_q8(Lo, C, d, fresh_o, inp.tables_dst, jobs, arena_o) == 0
+    a = arena.cpu().numpy()
+    if not np.array_equal(a, arena_o):
+        bad = np.flatnonzero(a != arena_o)
+        raise AssertionError(f"{bad.size} record bytes differ, first at {bad[:8]}")
+    assert np.array_equal(fresh.cpu().numpy(), fresh_o)
+
+
+def test_q8_tiny_workload_exact(lmc):
+    """The tiny workload: (4, 64, 64) fp32 states as 256 rows of 64 values."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    _q8_exact(lmc, inp, Lp, 64, W.fill_normal_np(inp.layout.pool_bytes, 61))
+
+
+def test_q8_special_rows_exact(lmc):
+    """Rows that decide the corner cases: all zero, subnormal (the clamp
+    decides), ties at half steps, huge and tiny magnitudes."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    Lo = inp.layout
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 62)
+    rng = np.random.default_rng(9)
+    f = pool_h[: (Lo.pool_bytes // 4) * 4].view(np.float32)
+    for i in range(len(Lo.kinds)):
+        if Lo.kinds[i] != "KDA":
+            continue
+        for b in range(Lo.num_blocks):
+            lo = (Lo.base[i] + b * Lo.stride[i] + 4608) // 4
+            rows = f[lo:lo + 256 * 64].reshape(256, 64)
+            rows[0] = 0
+            rows[1] = 0
+            rows[1, :3] = np.array([190, -189, 37], dtype=np.float32) * np.float32(2.0 ** -149)
+            rows[2] = np.arange(64, dtype=np.float32) - np.float32(31.5)  # ties at scale 32/127...
+            rows[3] = rows[3] * np.float32(1e30)
+            rows[4] = rows[4] * np.float32(1e-35)
+            rows[5, :] = np.float32(127)
+            rows[5, 1::2] = np.float32(2.5)
+            rows[6] = rng.choice([-3.5, -2.5, -0.5, 0.5, 1.5, 2.5], 64).astype(np.float32)
+            rows[6, 0] = 127
+    _q8_exact(lmc, inp, Lp, 64, pool_h)
+
+
+@pytest.mark.parametrize("d", [4, 16, 128])
+def test_q8_row_lengths_exact(lmc, d):
+    spec = [W.kda(48, 3, 2, 32), W.mla(32), W.kda(48, 3, 2, 32), W.mla(32)]
+    cfg = W.Config(400 + d, "q8", spec, N=8, requested_chunk=16, packed=bool(d % 8), num_requests=3,
+                   lengths="fixed", fixed_lengths=(40, 77, 23), seed=d)
+    inp, Lp = case_inputs(cfg)
+    _q8_exact(lmc, inp, Lp, d, W.fill_normal_np(inp.layout.pool_bytes, d))
+
+
+def test_q8_full_size_kimi_linear(lmc):
+    """Kimi-Linear full size, d = 128: sampled records and decoded pages
+    against the oracle; decoded values within half a step everywhere sampled."""
+    cfg = W.CONFIGS[1]
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    d = W.state_row_elems(cfg)
+    sizes = [Lo.object_bytes_q8(C, d, g) for g in range(Lo.num_object_groups)]
+    units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
+    jobs, nbytes = W.pack_jobs(units, sizes)
+    pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, 63)
+    arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    dj = dev_jobs(jobs, DEV)
+    t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+    lmc.lmc_store_q8(Lp, C, d, pool, t_src, dj, arena, st)
+    lmc.lmc_load_q8(Lp, C, d, fresh, t_dst, dj, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(8)
+    sel = [J[np.sort(rng.choice(len(J), 5, replace=False))] for J in jobs]
+    pages, s0 = oracle.list_pages(Lo, C, inp.tables_src, sel, nbytes)
+    assert s0 == 0
+    host = np.zeros(Lo.pool_bytes, dtype=np.uint8)
+    for pg in pages:
+        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
+        host[lo:lo + n] = pool[lo:lo + n].cpu().numpy()
+    arena_o = np.zeros(nbytes, dtype=np.uint8)
+    assert oracle.store_q8(Lo, C, d, host, inp.tables_src, sel, arena_o) == 0
+    for g, J in enumerate(sel):
+        for job in J:
+            lo, hi = int(job["offset"]), int(job["offset"]) + sizes[g]
+            assert np.array_equal(arena[lo:hi].cpu().numpy(), arena_o[lo:hi])
+    back = np.zeros(Lo.pool_bytes, dtype=np.uint8)
+    assert oracle.load_q8(Lo, C, d, back, inp.tables_dst, sel, arena_o) == 0
+    pages_d, _ = oracle.list_pages(Lo, C, inp.tables_dst, sel, nbytes)
+    for pg in pages_d:
+        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
+        assert np.array_equal(fresh[lo:lo + n].cpu().numpy(), back[lo:lo + n])

@@ -193,3 +193,37 @@ def test_copy_blocks_host_checks(lmc):
     counts[1] = 3  # pairs given as NULL with a non-zero count
     assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts)), addr, None) \
         == lmc.LMC_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("cfg_index", [0, 1, 3])
+def test_q8_object_sizes_match_oracle(lmc, cfg_index):
+    cfg = W.CONFIGS[cfg_index]
+    p = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, 1 << 36)
+    o = oracle.layout(cfg.layers, cfg.N, cfg.packed, 1 << 36)
+    for d in (4, 16, 64, 128, 256, 512, 6, 1024, 0):
+        for C in (cfg.N, 2 * cfg.N):
+            for g in range(o.num_object_groups):
+                want = o.object_bytes_q8(C, d, g)
+                if want < 0:
+                    with pytest.raises(lmc.LmcError) as e:
+                        p.object_bytes_q8(C, d, g)
+                    assert e.value.code == lmc.LMC_ERR_INVALID_ARG
+                else:
+                    assert p.object_bytes_q8(C, d, g) == want
+
+
+def test_q8_host_checks(lmc):
+    cfg = W.CONFIGS[1]
+    L = lmc.lmc_layout_build(cfg.layers, cfg.N, False, 1 << 34)
+    buf = (ctypes.c_uint8 * 256)()
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+    tables = (lmc.lmc_block_table * L.num_kv_groups)(*[lmc.lmc_block_table(addr, 4, 4)] * L.num_kv_groups)
+    jobs = (ctypes.c_void_p * L.num_object_groups)(*[addr] * L.num_object_groups)
+    counts = (ctypes.c_int64 * L.num_object_groups)(*[1] * L.num_object_groups)
+    b = lmc.lmc_batch(2, L.num_kv_groups, tables, L.num_object_groups, 0, jobs, counts)
+    for fn in (lmc._lib.lmc_store_q8, lmc._lib.lmc_load_q8):
+        assert fn(L.handle, 944, 100, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+        assert fn(L.handle, 944, 1024, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+        assert fn(L.handle, 900, 128, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_NOT_MULTIPLE
+        # the codec moves 16-byte vectors: an unaligned arena is refused before launch
+        assert fn(L.handle, 944, 128, addr, ctypes.byref(b), addr + 4, 64, addr, None) == lmc.LMC_ERR_ALIGN

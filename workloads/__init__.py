@@ -83,7 +83,7 @@ CONFIGS = {
     0: Config(0, "tiny: 4 layers (KDA,KDA,KDA,MLA), N=64, 2 requests (300, 517 tokens), padded",
               [kda(768, 3, 4, 64), kda(768, 3, 4, 64), kda(768, 3, 4, 64), mla(1152)],
               N=64, requested_chunk=100, packed=False, num_requests=2, lengths="fixed",
-              fixed_lengths=(300, 517), snapshot="block", pool_blocks=64, seed=0),
+              fixed_lengths=(300, 517), snapshot="block", pool_blocks=64, seed=0, extra={"state_d": 64}),
     1: Config(1, "kimi-linear 24L (18 KDA + 6 MLA), N=944, 32 x 8192 tokens, padded, chunk=N",
               _kimi_linear_layers(), N=944, requested_chunk=944, packed=False, num_requests=32,
               lengths="fixed", fixed_lengths=(8192,) * 32, snapshot="block", seed=1),
@@ -97,6 +97,11 @@ CONFIGS = {
               _mixed_layers(), N=944, requested_chunk=944, packed=True, num_requests=256,
               lengths="lognormal", snapshot="block", seed=4, mixed=True),
 }
+
+
+def state_row_elems(cfg: Config) -> int:
+    """Values per row of the KDA recurrent state (heads, d, d): d."""
+    return int(cfg.extra.get("state_d", 128))
 
 
 def request_lengths(cfg: Config) -> np.ndarray:
