@@ -310,7 +310,8 @@ int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy_batch *
  * decoded value = code * scale; all IEEE binary32. A KDA layer's record in the
  * object: conv bytes, then one fp32 scale per row, then the int8 codes, row
  * by row. Paged layers are stored exactly as by lmc_store. Lossy: a decoded
- * value lies within half a step (scale / 2) of the original.
+ * value lies within half a step (scale / 2) of the original. States holding
+ * NaN or infinity are outside the codec's domain (the output is unspecified).
  * Requires 4 <= row_elems <= 512, row_elems % 4 == 0, every KDA layer's
  * recurrent state a whole number of rows and a multiple of 4 rows, and
  * conv_bytes a multiple of 16, so records stay multiples of 16 bytes
