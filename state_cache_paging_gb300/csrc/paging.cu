@@ -258,70 +258,133 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 }
 
 // INT8 per-channel codec of the KDA recurrent state ("When Prefix Cache
-// Meets KDA", Compressed Checkpoint Storage): one warp per row of d fp32
-// values; scale = max|x| / 127, code = x / scale rounded half to even and
-// clamped to [-127, 127] (IEEE binary32 division), zero rows give scale 0
-// and codes 0; decode = code * scale. d % 4 == 0 and d <= 512, so a lane
-// holds at most 4 float4 of a row.
-constexpr int kMaxRowVec = 4;
+// Meets KDA", Compressed Checkpoint Storage): per row of d fp32 values,
+// scale = max|x| / 127, code = x / scale rounded half to even and clamped to
+// [-127, 127] (IEEE binary32 division), zero rows give scale 0 and codes 0;
+// decode = code * scale.
+//
+// Work split: a row's d / 4 float4 vectors are spread over `lpr` lanes of a
+// warp, kRowVec consecutive vectors per lane, so 32 / lpr rows share a warp
+// and every lane has kRowVec 16-byte loads in flight; the row maximum is a
+// shuffle reduction inside each aligned group of lpr lanes. This needs
+// d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two <= 32
+// (d = 16 .. 512 in powers of two); other row lengths take one row per warp.
+constexpr int kRowVec = 4;
+
+__device__ __forceinline__ uint32_t pack_codes(const float4 &v, float scale) {
+    const float c[4] = {v.x, v.y, v.z, v.w};
+    uint32_t packed = 0;
+#pragma unroll
+    for (int t = 0; t < 4; t++) {
+        int qi = 0;
+        if (scale != 0.0f)
+            qi = max(-127, min(127, __float2int_rn(__fdiv_rn(c[t], scale))));
+        packed |= (uint32_t)(uint8_t)(int8_t)qi << (8 * t);
+    }
+    return packed;
+}
+
+__device__ __forceinline__ float4 unpack_codes(uint32_t p, float scale) {
+    float4 o;
+    o.x = (float)(int8_t)(p & 0xffu) * scale;
+    o.y = (float)(int8_t)((p >> 8) & 0xffu) * scale;
+    o.z = (float)(int8_t)((p >> 16) & 0xffu) * scale;
+    o.w = (float)(int8_t)(p >> 24) * scale;
+    return o;
+}
+
+__device__ __forceinline__ float absmax4(const float4 &v) {
+    return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+
+__device__ __forceinline__ bool grouped_rows(int d, int &lpr) {
+    const int nvec = d >> 2;
+    if (nvec % kRowVec != 0)
+        return false;
+    lpr = nvec / kRowVec;
+    return lpr <= 32 && (lpr & (lpr - 1)) == 0;
+}
 
 __device__ __forceinline__ void encode_rows(const Span &s, int d) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWarps = kThreads / 32;
     const int nvec = d >> 2;
-    for (int r = warp; r < s.bytes; r += kThreads / 32) {
-        const float4 *x = reinterpret_cast<const float4 *>(s.src) + (int64_t)r * nvec;
-        float4 v[kMaxRowVec];
-        float amax = 0.0f;
+    int lpr;
+    if (grouped_rows(d, lpr)) {
+        const int per_warp = 32 / lpr, sub = lane / lpr, l = lane % lpr;
+        for (int base = warp * per_warp; base < s.bytes; base += kWarps * per_warp) {
+            const int r = base + sub;
+            const bool live = r < s.bytes;
+            float4 v[kRowVec];
+            float amax = 0.0f;
+            if (live) {
+                const float4 *x = reinterpret_cast<const float4 *>(s.src) + (int64_t)r * nvec + l * kRowVec;
 #pragma unroll
-        for (int w = 0; w < kMaxRowVec; w++) {
-            const int e = lane + 32 * w;
-            if (e < nvec) {
-                v[w] = __ldg(x + e);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[w].x), fabsf(v[w].y)), fmaxf(fabsf(v[w].z), fabsf(v[w].w))));
+                for (int w = 0; w < kRowVec; w++)
+                    v[w] = __ldg(x + w);
+#pragma unroll
+                for (int w = 0; w < kRowVec; w++)
+                    amax = fmaxf(amax, absmax4(v[w]));
+            }
+            for (int o = lpr >> 1; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (live) {
+                const float scale = __fdiv_rn(amax, 127.0f);
+                if (l == 0)
+                    reinterpret_cast<float *>(s.scales)[r] = scale;
+                uint4 q;
+                q.x = pack_codes(v[0], scale);
+                q.y = pack_codes(v[1], scale);
+                q.z = pack_codes(v[2], scale);
+                q.w = pack_codes(v[3], scale);
+                reinterpret_cast<uint4 *>(s.dst + (int64_t)r * d)[l] = q;
             }
         }
-#pragma unroll
+        return;
+    }
+    for (int r = warp; r < s.bytes; r += kWarps) {  // one row per warp
+        const float4 *x = reinterpret_cast<const float4 *>(s.src) + (int64_t)r * nvec;
+        float amax = 0.0f;
+        for (int e = lane; e < nvec; e += 32)
+            amax = fmaxf(amax, absmax4(__ldg(x + e)));
         for (int o = 16; o > 0; o >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float scale = __fdiv_rn(amax, 127.0f);
         if (lane == 0)
             reinterpret_cast<float *>(s.scales)[r] = scale;
         uint32_t *q = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d);
-#pragma unroll
-        for (int w = 0; w < kMaxRowVec; w++) {
-            const int e = lane + 32 * w;
-            if (e < nvec) {
-                const float c[4] = {v[w].x, v[w].y, v[w].z, v[w].w};
-                uint32_t packed = 0;
-#pragma unroll
-                for (int t = 0; t < 4; t++) {
-                    int qi = 0;
-                    if (scale != 0.0f)
-                        qi = max(-127, min(127, __float2int_rn(__fdiv_rn(c[t], scale))));
-                    packed |= (uint32_t)(uint8_t)(int8_t)qi << (8 * t);
-                }
-                q[e] = packed;
-            }
-        }
+        for (int e = lane; e < nvec; e += 32)
+            q[e] = pack_codes(__ldg(x + e), scale);
     }
 }
 
 __device__ __forceinline__ void decode_rows(const Span &s, int d) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWarps = kThreads / 32;
     const int nvec = d >> 2;
-    for (int r = warp; r < s.bytes; r += kThreads / 32) {
+    int lpr;
+    if (grouped_rows(d, lpr)) {
+        const int per_warp = 32 / lpr, sub = lane / lpr, l = lane % lpr;
+        for (int base = warp * per_warp; base < s.bytes; base += kWarps * per_warp) {
+            const int r = base + sub;
+            if (r >= s.bytes)
+                continue;
+            const float scale = __ldg(reinterpret_cast<const float *>(s.scales) + r);
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(s.src + (int64_t)r * d) + l);
+            float4 *x = reinterpret_cast<float4 *>(s.dst) + (int64_t)r * nvec + l * kRowVec;
+            x[0] = unpack_codes(q.x, scale);
+            x[1] = unpack_codes(q.y, scale);
+            x[2] = unpack_codes(q.z, scale);
+            x[3] = unpack_codes(q.w, scale);
+        }
+        return;
+    }
+    for (int r = warp; r < s.bytes; r += kWarps) {  // one row per warp
         const float scale = __ldg(reinterpret_cast<const float *>(s.scales) + r);
         const uint32_t *q = reinterpret_cast<const uint32_t *>(s.src + (int64_t)r * d);
         float4 *x = reinterpret_cast<float4 *>(s.dst) + (int64_t)r * nvec;
-        for (int e = lane; e < nvec; e += 32) {
-            const uint32_t p = __ldg(q + e);
-            float4 o;
-            o.x = (float)(int8_t)(p & 0xffu) * scale;
-            o.y = (float)(int8_t)((p >> 8) & 0xffu) * scale;
-            o.z = (float)(int8_t)((p >> 16) & 0xffu) * scale;
-            o.w = (float)(int8_t)(p >> 24) * scale;
-            x[e] = o;
-        }
+        for (int e = lane; e < nvec; e += 32)
+            x[e] = unpack_codes(__ldg(q + e), scale);
     }
 }
 
@@ -787,7 +850,7 @@ int q8_shape(const lmc_layout *L, int64_t chunk, int64_t d, Shape &sh) {
     const int rc = chunk_shape(L, chunk, sh);
     if (rc != LMC_OK)
         return rc;
-    if (d < 4 || d > 4 * 32 * kMaxRowVec || d % 4 != 0)
+    if (d < 4 || d > 512 || d % 4 != 0)
         return LMC_ERR_INVALID_ARG;
     for (const lmc_layer_spec &spec : L->specs)
         if (spec.kind == LMC_LAYER_KDA && (spec.rec_bytes % (4 * d) != 0 || (spec.rec_bytes / (4 * d)) % 4 != 0 ||
