@@ -271,16 +271,29 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // (d = 16 .. 512 in powers of two); other row lengths take one row per warp.
 constexpr int kRowVec = 4;
 
+// One code: rint(x / scale) clamped. x * inv (inv = 1 / scale rounded) is
+// within a few ulps of x / scale; when that product is more than 1e-4 away
+// from a half-integer both round to the same integer, so the IEEE division
+// runs only near ties (and for subnormal scales, whose reciprocal may not be
+// finite). |x / scale| <= ~127 here, so 1e-4 is far above the products' error.
+__device__ __forceinline__ int code_of(float x, float scale, float inv, bool exact_only) {
+    float y = x * inv;
+    const float frac = fabsf(y - truncf(y));
+    if (exact_only || fabsf(frac - 0.5f) < 1e-4f)
+        y = __fdiv_rn(x, scale);
+    return max(-127, min(127, __float2int_rn(y)));
+}
+
 __device__ __forceinline__ uint32_t pack_codes(const float4 &v, float scale) {
+    if (scale == 0.0f)
+        return 0u;
+    const bool exact_only = scale < 1.17549435e-38f;  // subnormal scale
+    const float inv = __frcp_rn(scale);
     const float c[4] = {v.x, v.y, v.z, v.w};
     uint32_t packed = 0;
 #pragma unroll
-    for (int t = 0; t < 4; t++) {
-        int qi = 0;
-        if (scale != 0.0f)
-            qi = max(-127, min(127, __float2int_rn(__fdiv_rn(c[t], scale))));
-        packed |= (uint32_t)(uint8_t)(int8_t)qi << (8 * t);
-    }
+    for (int t = 0; t < 4; t++)
+        packed |= (uint32_t)(uint8_t)(int8_t)code_of(c[t], scale, inv, exact_only) << (8 * t);
     return packed;
 }
 
@@ -390,19 +403,19 @@ __device__ __forceinline__ void decode_rows(const Span &s, int d) {
 
 // Vector engine: every thread of the CTA copies 16-byte vectors of the tile,
 // kUnroll loads in flight before the matching stores.
-template <bool kVec, bool kCodec>
+template <bool kVec, int kCodec>
 __device__ __forceinline__ void copy_tiles(const Plan &P) {
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
         Span s;
-        const uint32_t bad = resolve<kCodec>(P, tile, s);
+        const uint32_t bad = resolve<kCodec != 0>(P, tile, s);
         if (bad) {
             if (threadIdx.x == 0)
                 atomicOr(P.status, bad);
             continue;
         }
-        if (kCodec && s.codec == 1) {
+        if (kCodec == 1 && s.codec == 1) {
             encode_rows(s, P.q8_row);
-        } else if (kCodec && s.codec == 2) {
+        } else if (kCodec == 2 && s.codec == 2) {
             decode_rows(s, P.q8_row);
         } else if (kVec) {
             const uint4 *src = reinterpret_cast<const uint4 *>(s.src);
@@ -431,21 +444,21 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
 // which side is the pool).
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_store_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<kVec, false>(P);
+    copy_tiles<kVec, 0>(P);
 }
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_load_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<kVec, false>(P);
+    copy_tiles<kVec, 0>(P);
 }
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_copy_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<kVec, false>(P);
+    copy_tiles<kVec, 0>(P);
 }
 __global__ void __launch_bounds__(kThreads) lmc_store_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, true>(P);
+    copy_tiles<true, 1>(P);
 }
 __global__ void __launch_bounds__(kThreads) lmc_load_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, true>(P);
+    copy_tiles<true, 2>(P);
 }
 
 // ---------------------------------------------------------------------------
