@@ -269,7 +269,13 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // shuffle reduction inside each aligned group of lpr lanes. This needs
 // d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two <= 32
 // (d = 16 .. 512 in powers of two); other row lengths take one row per warp.
-constexpr int kRowVec = 4;
+#ifndef LMC_ROW_VEC
+#define LMC_ROW_VEC 4
+#endif
+#ifndef LMC_Q8_MIN_BLOCKS
+#define LMC_Q8_MIN_BLOCKS 1
+#endif
+constexpr int kRowVec = LMC_ROW_VEC;
 
 // One code: rint(x / scale) clamped. x * inv (inv = 1 / scale rounded) is
 // within a few ulps of x / scale; when that product is more than 1e-4 away
@@ -345,12 +351,17 @@ __device__ __forceinline__ void encode_rows(const Span &s, int d) {
                 const float scale = __fdiv_rn(amax, 127.0f);
                 if (l == 0)
                     reinterpret_cast<float *>(s.scales)[r] = scale;
-                uint4 q;
-                q.x = pack_codes(v[0], scale);
-                q.y = pack_codes(v[1], scale);
-                q.z = pack_codes(v[2], scale);
-                q.w = pack_codes(v[3], scale);
-                reinterpret_cast<uint4 *>(s.dst + (int64_t)r * d)[l] = q;
+                uint32_t q[kRowVec];
+#pragma unroll
+                for (int w = 0; w < kRowVec; w++)
+                    q[w] = pack_codes(v[w], scale);
+                uint32_t *out = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d) + l * kRowVec;
+                if (kRowVec == 4)
+                    *reinterpret_cast<uint4 *>(out) = make_uint4(q[0], q[1], q[2], q[3]);
+                else
+#pragma unroll
+                    for (int w = 0; w < kRowVec; w++)
+                        out[w] = q[w];
             }
         }
         return;
@@ -383,12 +394,20 @@ __device__ __forceinline__ void decode_rows(const Span &s, int d) {
             if (r >= s.bytes)
                 continue;
             const float scale = __ldg(reinterpret_cast<const float *>(s.scales) + r);
-            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(s.src + (int64_t)r * d) + l);
+            const uint32_t *q = reinterpret_cast<const uint32_t *>(s.src + (int64_t)r * d) + l * kRowVec;
+            uint32_t c[kRowVec];
+            if (kRowVec == 4) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(q));
+                c[0] = u.x, c[1] = u.y, c[2] = u.z, c[3] = u.w;
+            } else {
+#pragma unroll
+                for (int w = 0; w < kRowVec; w++)
+                    c[w] = __ldg(q + w);
+            }
             float4 *x = reinterpret_cast<float4 *>(s.dst) + (int64_t)r * nvec + l * kRowVec;
-            x[0] = unpack_codes(q.x, scale);
-            x[1] = unpack_codes(q.y, scale);
-            x[2] = unpack_codes(q.z, scale);
-            x[3] = unpack_codes(q.w, scale);
+#pragma unroll
+            for (int w = 0; w < kRowVec; w++)
+                x[w] = unpack_codes(c[w], scale);
         }
         return;
     }
@@ -454,7 +473,7 @@ template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_copy_kernel(const __grid_constant__ Plan P) {
     copy_tiles<kVec, 0>(P);
 }
-__global__ void __launch_bounds__(kThreads) lmc_store_q8_kernel(const __grid_constant__ Plan P) {
+__global__ void __launch_bounds__(kThreads, LMC_Q8_MIN_BLOCKS) lmc_store_q8_kernel(const __grid_constant__ Plan P) {
     copy_tiles<true, 1>(P);
 }
 __global__ void __launch_bounds__(kThreads) lmc_load_q8_kernel(const __grid_constant__ Plan P) {
