@@ -272,8 +272,11 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 #ifndef LMC_ROW_VEC
 #define LMC_ROW_VEC 4
 #endif
+#ifndef LMC_Q8_THREADS
+#define LMC_Q8_THREADS 256  // codec kernels: more, smaller CTAs per SM than the copies
+#endif
 #ifndef LMC_Q8_MIN_BLOCKS
-#define LMC_Q8_MIN_BLOCKS 1
+#define LMC_Q8_MIN_BLOCKS 6
 #endif
 constexpr int kRowVec = LMC_ROW_VEC;
 
@@ -324,9 +327,10 @@ __device__ __forceinline__ bool grouped_rows(int d, int &lpr) {
     return lpr <= 32 && (lpr & (lpr - 1)) == 0;
 }
 
+template <int kNT>
 __device__ __forceinline__ void encode_rows(const Span &s, int d) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int kWarps = kThreads / 32;
+    constexpr int kWarps = kNT / 32;
     const int nvec = d >> 2;
     int lpr;
     if (grouped_rows(d, lpr)) {
@@ -382,9 +386,10 @@ __device__ __forceinline__ void encode_rows(const Span &s, int d) {
     }
 }
 
+template <int kNT>
 __device__ __forceinline__ void decode_rows(const Span &s, int d) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int kWarps = kThreads / 32;
+    constexpr int kWarps = kNT / 32;
     const int nvec = d >> 2;
     int lpr;
     if (grouped_rows(d, lpr)) {
@@ -422,7 +427,7 @@ __device__ __forceinline__ void decode_rows(const Span &s, int d) {
 
 // Vector engine: every thread of the CTA copies 16-byte vectors of the tile,
 // kUnroll loads in flight before the matching stores.
-template <bool kVec, int kCodec>
+template <bool kVec, int kCodec, int kNT = kThreads>
 __device__ __forceinline__ void copy_tiles(const Plan &P) {
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
         Span s;
@@ -433,27 +438,27 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
             continue;
         }
         if (kCodec == 1 && s.codec == 1) {
-            encode_rows(s, P.q8_row);
+            encode_rows<kNT>(s, P.q8_row);
         } else if (kCodec == 2 && s.codec == 2) {
-            decode_rows(s, P.q8_row);
+            decode_rows<kNT>(s, P.q8_row);
         } else if (kVec) {
             const uint4 *src = reinterpret_cast<const uint4 *>(s.src);
             uint4 *dst = reinterpret_cast<uint4 *>(s.dst);
             const int n = s.bytes >> 4;
             int i = threadIdx.x;
-            for (; i + (kUnroll - 1) * kThreads < n; i += kUnroll * kThreads) {
+            for (; i + (kUnroll - 1) * kNT < n; i += kUnroll * kNT) {
                 uint4 v[kUnroll];
 #pragma unroll
                 for (int w = 0; w < kUnroll; w++)
-                    v[w] = ld_stream(src + i + w * kThreads);
+                    v[w] = ld_stream(src + i + w * kNT);
 #pragma unroll
                 for (int w = 0; w < kUnroll; w++)
-                    st_stream(dst + i + w * kThreads, v[w]);
+                    st_stream(dst + i + w * kNT, v[w]);
             }
-            for (; i < n; i += kThreads)
+            for (; i < n; i += kNT)
                 st_stream(dst + i, ld_stream(src + i));
         } else {
-            for (int i = threadIdx.x; i < s.bytes; i += kThreads)
+            for (int i = threadIdx.x; i < s.bytes; i += kNT)
                 s.dst[i] = s.src[i];
         }
     }
@@ -473,11 +478,12 @@ template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_copy_kernel(const __grid_constant__ Plan P) {
     copy_tiles<kVec, 0>(P);
 }
-__global__ void __launch_bounds__(kThreads, LMC_Q8_MIN_BLOCKS) lmc_store_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 1>(P);
+constexpr int kQ8Threads = LMC_Q8_THREADS;
+__global__ void __launch_bounds__(kQ8Threads, LMC_Q8_MIN_BLOCKS) lmc_store_q8_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<true, 1, kQ8Threads>(P);
 }
-__global__ void __launch_bounds__(kThreads) lmc_load_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 2>(P);
+__global__ void __launch_bounds__(kQ8Threads, LMC_Q8_MIN_BLOCKS) lmc_load_q8_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<true, 2, kQ8Threads>(P);
 }
 
 // ---------------------------------------------------------------------------
@@ -828,10 +834,12 @@ int launch_plan(const Plan &P, bool vec, void *stream) {
     } else {
         // one CTA per tile, capped; the kernel strides over the rest
         const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * 2048);
+        if (P.q8_row > 0) {
+            (P.mode == kStore ? lmc_store_q8_kernel : lmc_load_q8_kernel)<<<grid, kQ8Threads, 0, s>>>(P);
+            return cudaGetLastError() == cudaSuccess ? LMC_OK : LMC_ERR_CUDA;
+        }
         void (*kern)(const Plan);
-        if (P.q8_row > 0)
-            kern = P.mode == kStore ? lmc_store_q8_kernel : lmc_load_q8_kernel;
-        else if (P.mode == kStore)
+        if (P.mode == kStore)
             kern = vec ? lmc_store_kernel<true> : lmc_store_kernel<false>;
         else if (P.mode == kLoad)
             kern = vec ? lmc_load_kernel<true> : lmc_load_kernel<false>;
