@@ -269,14 +269,24 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // shuffle reduction inside each aligned group of lpr lanes. This needs
 // d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two <= 32
 // (d = 16 .. 512 in powers of two); other row lengths take one row per warp.
+// Codec kernel shapes picked by measurement on GB300 (Kimi-Linear, d = 128):
+// two float4 per lane, and more, smaller CTAs than the copies (the encoder's
+// register budget would otherwise cap residency): 128 x 16 for encode, 256 x 8
+// for decode.
 #ifndef LMC_ROW_VEC
-#define LMC_ROW_VEC 4
+#define LMC_ROW_VEC 2
 #endif
-#ifndef LMC_Q8_THREADS
-#define LMC_Q8_THREADS 256  // codec kernels: more, smaller CTAs per SM than the copies
+#ifndef LMC_Q8_ENC_THREADS
+#define LMC_Q8_ENC_THREADS 128
 #endif
-#ifndef LMC_Q8_MIN_BLOCKS
-#define LMC_Q8_MIN_BLOCKS 6
+#ifndef LMC_Q8_ENC_MIN_BLOCKS
+#define LMC_Q8_ENC_MIN_BLOCKS 16
+#endif
+#ifndef LMC_Q8_DEC_THREADS
+#define LMC_Q8_DEC_THREADS 256
+#endif
+#ifndef LMC_Q8_DEC_MIN_BLOCKS
+#define LMC_Q8_DEC_MIN_BLOCKS 8
 #endif
 constexpr int kRowVec = LMC_ROW_VEC;
 
@@ -478,12 +488,15 @@ template <bool kVec>
 __global__ void __launch_bounds__(kThreads) lmc_copy_kernel(const __grid_constant__ Plan P) {
     copy_tiles<kVec, 0>(P);
 }
-constexpr int kQ8Threads = LMC_Q8_THREADS;
-__global__ void __launch_bounds__(kQ8Threads, LMC_Q8_MIN_BLOCKS) lmc_store_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 1, kQ8Threads>(P);
+constexpr int kEncThreads = LMC_Q8_ENC_THREADS;
+constexpr int kDecThreads = LMC_Q8_DEC_THREADS;
+__global__ void __launch_bounds__(kEncThreads, LMC_Q8_ENC_MIN_BLOCKS)
+    lmc_store_q8_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<true, 1, kEncThreads>(P);
 }
-__global__ void __launch_bounds__(kQ8Threads, LMC_Q8_MIN_BLOCKS) lmc_load_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 2, kQ8Threads>(P);
+__global__ void __launch_bounds__(kDecThreads, LMC_Q8_DEC_MIN_BLOCKS)
+    lmc_load_q8_kernel(const __grid_constant__ Plan P) {
+    copy_tiles<true, 2, kDecThreads>(P);
 }
 
 // ---------------------------------------------------------------------------
@@ -835,7 +848,10 @@ int launch_plan(const Plan &P, bool vec, void *stream) {
         // one CTA per tile, capped; the kernel strides over the rest
         const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * 2048);
         if (P.q8_row > 0) {
-            (P.mode == kStore ? lmc_store_q8_kernel : lmc_load_q8_kernel)<<<grid, kQ8Threads, 0, s>>>(P);
+            if (P.mode == kStore)
+                lmc_store_q8_kernel<<<grid, kEncThreads, 0, s>>>(P);
+            else
+                lmc_load_q8_kernel<<<grid, kDecThreads, 0, s>>>(P);
             return cudaGetLastError() == cudaSuccess ? LMC_OK : LMC_ERR_CUDA;
         }
         void (*kern)(const Plan);
