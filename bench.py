@@ -359,13 +359,13 @@ class PagingStep:
         self.main.wait_event(ja)
         self.main.wait_event(jb)
 
-    def setup_e2e(self, parts: int = 8):
+    def setup_e2e(self, parts: int = 16):
         """Pinned host buffers for the end-to-end step: block tables and jobs
         go host -> device each step; objects leave the device for the host
         cache tier (store) and come back from it (load). Plain workloads are
-        pipelined over `parts` request ranges so that a part's device -> host
-        copy overlaps the next part's store and its host -> device copy the
-        previous part's load."""
+        pipelined over `parts` request ranges (at most one per request) so
+        that a part's device -> host copy overlaps the next part's store and
+        its host -> device copy the previous part's load."""
         T, inp = self.torch, self.inp
         pin = lambda a: T.from_numpy(np.ascontiguousarray(a)).pin_memory()
         self.h_tables = [pin(t) for t in inp.tables_src] + ([pin(t) for t in inp.tables_dst] if not self.cfg.mixed else [])
