@@ -363,9 +363,9 @@ class PagingStep:
         """Pinned host buffers for the end-to-end step: block tables and jobs
         go host -> device each step; objects leave the device for the host
         cache tier (store) and come back from it (load). Plain workloads are
-        pipelined over `parts` request ranges (at most one per request) so
-        that a part's device -> host copy overlaps the next part's store and
-        its host -> device copy the previous part's load."""
+        pipelined over `parts` ranges of (request, chunk) units so that a
+        part's device -> host copy overlaps the next part's store and its
+        host -> device copy the previous part's load."""
         T, inp = self.torch, self.inp
         pin = lambda a: T.from_numpy(np.ascontiguousarray(a)).pin_memory()
         self.h_tables = [pin(t) for t in inp.tables_src] + ([pin(t) for t in inp.tables_dst] if not self.cfg.mixed else [])
@@ -382,8 +382,13 @@ class PagingStep:
             self.d_jobs = self.jobs
             self.h_arena = T.empty(inp.arena_bytes, dtype=T.uint8, pin_memory=True)
             objs_in, objs_out = inp.arena_bytes, inp.arena_bytes
-            # request ranges -> (per-group job row ranges, arena byte range)
-            n = len(inp.lengths)
+            # ranges of (request, chunk) units -> (per-group job row ranges,
+            # arena byte range); jobs are packed in (request, chunk, group) order
+            units = sorted({(int(j["request"]), int(j["chunk"])) for J in inp.jobs for j in J})
+            index = {u: k for k, u in enumerate(units)}
+            uid = [np.array([index[(int(j["request"]), int(j["chunk"]))] for j in J], dtype=np.int64)
+                   for J in inp.jobs]
+            n = len(units)
             bounds = [round(k * n / parts) for k in range(parts + 1)]
             self.parts = []
             for a, b in zip(bounds[:-1], bounds[1:]):
@@ -391,7 +396,7 @@ class PagingStep:
                     continue
                 rows, lo, hi = [], None, None
                 for g, J in enumerate(inp.jobs):
-                    sel = np.flatnonzero((J["request"] >= a) & (J["request"] < b))
+                    sel = np.flatnonzero((uid[g] >= a) & (uid[g] < b))
                     r0, r1 = (int(sel[0]), int(sel[-1]) + 1) if sel.size else (0, 0)
                     rows.append((r0, r1))
                     if sel.size:
