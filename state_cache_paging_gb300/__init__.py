@@ -186,6 +186,7 @@ class Layout:
 
     def __init__(self, handle: int):
         self._h = ctypes.c_void_p(handle)
+        self._so = _lib  # the build that allocated the handle also frees it
         info = lmc_layout_info()
         _check(_lib.lmc_layout_query(self._h, ctypes.byref(info)), "lmc_layout_query")
         n, g, o = info.num_layers, info.num_kv_groups, info.num_object_groups
@@ -228,7 +229,7 @@ class Layout:
     def __del__(self):
         h = getattr(self, "_h", None)
         if h is not None and h.value:
-            _lib.lmc_layout_free(h)
+            self._so.lmc_layout_free(h)
             self._h = None
 
 
