@@ -236,6 +236,32 @@ def run_reference(args):
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def split_parts(jobs, object_bytes, parts):
+    """Splits packed jobs (ordered by request, chunk, group) into `parts`
+    ranges of (request, chunk) units: [(per-group (row0, row1), arena lo, hi)]."""
+    units = sorted({(int(j["request"]), int(j["chunk"])) for J in jobs for j in J})
+    index = {u: k for k, u in enumerate(units)}
+    uid = [np.array([index[(int(j["request"]), int(j["chunk"]))] for j in J], dtype=np.int64) for J in jobs]
+    n = len(units)
+    bounds = [round(k * n / parts) for k in range(parts + 1)]
+    out = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if a == b:
+            continue
+        rows, lo, hi = [], None, None
+        for g, J in enumerate(jobs):
+            sel = np.flatnonzero((uid[g] >= a) & (uid[g] < b))
+            r0, r1 = (int(sel[0]), int(sel[-1]) + 1) if sel.size else (0, 0)
+            rows.append((r0, r1))
+            if sel.size:
+                lo = int(J["offset"][r0]) if lo is None else min(lo, int(J["offset"][r0]))
+                end = int(J["offset"][r1 - 1]) + int(object_bytes[g])
+                hi = end if hi is None else max(hi, end)
+        if lo is not None:
+            out.append((rows, lo, hi))
+    return out
+
+
 class PagingStep:
     """Device inputs and one step of the hot path for a workload.
 
@@ -377,34 +403,16 @@ class PagingStep:
             self.h_load.copy_(self.load_arena)
             self.h_store = T.empty(inp.store_arena_bytes, dtype=T.uint8, pin_memory=True)
             objs_in, objs_out = inp.load_arena_bytes, inp.store_arena_bytes
+            self.load_parts = split_parts(inp.load_jobs, inp.object_bytes, parts)
+            self.store_parts = split_parts(inp.store_jobs, inp.object_bytes, parts)
+            self.s_out = T.cuda.Stream(self.dev)
+            self.s_in = T.cuda.Stream(self.dev)
         else:
             self.h_jobs = [pin(j.view(np.uint8)) for j in inp.jobs]
             self.d_jobs = self.jobs
             self.h_arena = T.empty(inp.arena_bytes, dtype=T.uint8, pin_memory=True)
             objs_in, objs_out = inp.arena_bytes, inp.arena_bytes
-            # ranges of (request, chunk) units -> (per-group job row ranges,
-            # arena byte range); jobs are packed in (request, chunk, group) order
-            units = sorted({(int(j["request"]), int(j["chunk"])) for J in inp.jobs for j in J})
-            index = {u: k for k, u in enumerate(units)}
-            uid = [np.array([index[(int(j["request"]), int(j["chunk"]))] for j in J], dtype=np.int64)
-                   for J in inp.jobs]
-            n = len(units)
-            bounds = [round(k * n / parts) for k in range(parts + 1)]
-            self.parts = []
-            for a, b in zip(bounds[:-1], bounds[1:]):
-                if a == b:
-                    continue
-                rows, lo, hi = [], None, None
-                for g, J in enumerate(inp.jobs):
-                    sel = np.flatnonzero((uid[g] >= a) & (uid[g] < b))
-                    r0, r1 = (int(sel[0]), int(sel[-1]) + 1) if sel.size else (0, 0)
-                    rows.append((r0, r1))
-                    if sel.size:
-                        lo = int(J["offset"][r0]) if lo is None else min(lo, int(J["offset"][r0]))
-                        end = int(J["offset"][r1 - 1]) + int(inp.object_bytes[g])
-                        hi = end if hi is None else max(hi, end)
-                if lo is not None:
-                    self.parts.append((rows, lo, hi))
+            self.parts = split_parts(inp.jobs, inp.object_bytes, parts)
             self.s_out = T.cuda.Stream(self.dev)
             self.s_in = T.cuda.Stream(self.dev)
             self.s_load = T.cuda.Stream(self.dev)
@@ -420,9 +428,33 @@ class PagingStep:
         for h, d in zip(self.h_jobs, self.d_jobs):
             d.copy_(h, non_blocking=True)
         if self.cfg.mixed:
-            self.load_arena.copy_(self.h_load, non_blocking=True)
-            self.step()
-            self.h_store.copy_(self.store_arena, non_blocking=True)
+            # cached objects stream in (host -> device) part by part, each part
+            # loaded as it lands; new chunks are stored part by part, each part
+            # streamed out (device -> host) as it is written
+            ready = T.cuda.Event()
+            ready.record(self.main)
+            for st in (self.s_in, self.s_out, self.sa, self.sb):
+                st.wait_event(ready)
+            for rows, lo, hi in self.load_parts:
+                jobs = [j[16 * r0:16 * r1] for j, (r0, r1) in zip(self.load_jobs, rows)]
+                with T.cuda.stream(self.s_in):
+                    self.load_arena[lo:hi].copy_(self.h_load[lo:hi], non_blocking=True)
+                    landed = T.cuda.Event()
+                    landed.record(self.s_in)
+                self.sa.wait_event(landed)
+                lmc.lmc_load(L, C, self.pool, self.t_src, jobs, self.load_arena, self.status, self.sa)
+            for rows, lo, hi in self.store_parts:
+                jobs = [j[16 * r0:16 * r1] for j, (r0, r1) in zip(self.store_jobs, rows)]
+                lmc.lmc_store(L, C, self.pool, self.t_src, jobs, self.store_arena, self.status, self.sb)
+                written = T.cuda.Event()
+                written.record(self.sb)
+                with T.cuda.stream(self.s_out):
+                    self.s_out.wait_event(written)
+                    self.h_store[lo:hi].copy_(self.store_arena[lo:hi], non_blocking=True)
+            for st in (self.sa, self.s_out):
+                done = T.cuda.Event()
+                done.record(st)
+                self.main.wait_event(done)
             self.h_status.copy_(self.status, non_blocking=True)
             return
         ready = T.cuda.Event()
