@@ -155,6 +155,23 @@ int lmc_layout_query(const lmc_layout *layout, lmc_layout_info *out);
 /* Frees a layout (NULL is ignored). No call using it may still be running. */
 void lmc_layout_free(lmc_layout *layout);
 
+/* Backend-eligibility bits of lmc_layout_check_backends. */
+#define LMC_BK_PADDED_ATTENTION 0x1u /* padded path pads an attention page, but the
+                                        attention backend cannot index by block stride */
+#define LMC_BK_PACKED_ATTENTION 0x2u /* packed path, an attention backend cannot stride */
+#define LMC_BK_PACKED_STATE 0x4u     /* packed path, a state (KDA) kernel needs
+                                        contiguous pages */
+
+/* Which kernels can read the layout ([VB] §3.3): padding an attention layer's
+ * page needs an attention backend that indexes pages by the block stride
+ * (vLLM raises otherwise); the packed path needs every backend to address
+ * pages by the block stride, and KDA kernels that assume contiguous pages
+ * (causal_conv1d, chunk_kda) cannot, so such models fall back to the padded
+ * path. *out_bits gets the LMC_BK_* bits of every rule broken (0: readable).
+ * The store/load calls themselves work on any layout. */
+int lmc_layout_check_backends(const lmc_layout *layout, int attn_indexes_by_stride, int state_pages_strided_ok,
+                              uint32_t *out_bits);
+
 /* Bytes of one object of `object_group` for chunk size `chunk` ([HM] object
  * groups): the group's layers in model order, a paged layer contributing its
  * chunk / N pages of real_bytes (the chunk's tokens in order), a KDA layer one

@@ -46,6 +46,10 @@ ST_NO_BLOCK = 0x2
 ST_NO_SNAPSHOT = 0x4
 ST_BAD_JOB = 0x8
 
+BK_PADDED_ATTENTION = 0x1
+BK_PACKED_ATTENTION = 0x2
+BK_PACKED_STATE = 0x4
+
 JOB_DTYPE = np.dtype([("request", "<i4"), ("chunk", "<i4"), ("offset", "<i8")])
 
 
@@ -155,6 +159,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("or_store_blocks", "or_load_blocks"):
         getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, P(_Tables),
                                        P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
+    lib.or_check_backends.argtypes = [P(_Layout), ctypes.c_int, ctypes.c_int]
+    lib.or_check_backends.restype = ctypes.c_uint32
     lib.or_copy_blocks.argtypes = [P(_Layout), ctypes.c_void_p, P(_CopyBatch), P(ctypes.c_uint32)]
     for name in ("or_store_q8", "or_load_q8"):
         getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, P(_Tables),
@@ -237,6 +243,10 @@ class Layout:
 
     def object_bytes(self, C: int, og: int) -> int:
         return int(self._lib.or_object_bytes(ctypes.byref(self._c), int(C), int(og)))
+
+    def check_backends(self, attn_indexes_by_stride: bool, state_pages_strided_ok: bool) -> int:
+        return int(self._lib.or_check_backends(ctypes.byref(self._c), int(bool(attn_indexes_by_stride)),
+                                               int(bool(state_pages_strided_ok))))
 
     def object_bytes_q8(self, C: int, d: int, og: int) -> int:
         return int(self._lib.or_object_bytes_q8(ctypes.byref(self._c), int(C), int(d), int(og)))

@@ -87,6 +87,30 @@ int or_check_step_budget(int64_t N, int64_t max_batched, int separate_object_gro
     return separate_object_groups ? OR_OK : OR_ERR_BUDGET;
 }
 
+/* Which backends can read a layout ([VB] §3.3): padding an attention
+ * layer's page (padded path, its page smaller than the unified page) needs an
+ * attention backend that indexes pages by the block stride; the packed path
+ * needs every backend to address pages by the block stride, and KDA kernels
+ * that assume contiguous pages cannot. Returns the OR_BK_* bits of every
+ * rule the layout breaks (0: readable). */
+uint32_t or_check_backends(const or_layout *L, int attn_indexes_by_stride, int state_pages_strided_ok)
+{
+    uint32_t bad = 0;
+    for (int i = 0; i < L->num_layers; i++) {
+        int attention = L->layers[i].kind != OR_KDA;
+        if (!L->packed) {
+            if (attention && L->page_bytes[i] > L->real_bytes[i] && !attn_indexes_by_stride)
+                bad |= OR_BK_PADDED_ATTENTION;
+        } else {
+            if (attention && !attn_indexes_by_stride)
+                bad |= OR_BK_PACKED_ATTENTION;
+            if (!attention && !state_pages_strided_ok)
+                bad |= OR_BK_PACKED_STATE;
+        }
+    }
+    return bad;
+}
+
 /* ------------------------------------------------------------------ */
 /* Layout ([VB] §2.1, §2.2, §3.1, §3.2, §4; [MC] "Flat KV").            */
 /* ------------------------------------------------------------------ */

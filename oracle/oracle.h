@@ -24,6 +24,11 @@
 #define OR_ST_NO_SNAPSHOT 0x4u /* -1 where a KDA snapshot is needed */
 #define OR_ST_BAD_JOB 0x8u     /* bad request/chunk/offset, or past the table */
 
+/* Backend-eligibility bits. */
+#define OR_BK_PADDED_ATTENTION 0x1u /* an attention page is padded, backend cannot stride */
+#define OR_BK_PACKED_ATTENTION 0x2u /* packed, an attention backend cannot stride */
+#define OR_BK_PACKED_STATE 0x4u     /* packed, a state (KDA) kernel needs contiguous pages */
+
 /* Layer kinds. */
 #define OR_MLA 0
 #define OR_KDA 1
@@ -104,6 +109,7 @@ typedef struct {
 int or_negotiate_chunk(int64_t requested, int64_t N, int strict, int64_t *out);
 int or_check_step_budget(int64_t N, int64_t max_batched, int separate_object_groups);
 int or_layout_build(or_layout *L);
+uint32_t or_check_backends(const or_layout *L, int attn_indexes_by_stride, int state_pages_strided_ok);
 int64_t or_object_bytes(const or_layout *L, int64_t C, int og);
 int or_store(const or_layout *L, int64_t C, const uint8_t *pool,
              const or_tables *T, const or_jobs *J,

@@ -40,6 +40,10 @@ LMC_ST_NO_SNAPSHOT = 0x4
 LMC_ST_BAD_JOB = 0x8
 LMC_ST_TIMEOUT = 0x10
 
+LMC_BK_PADDED_ATTENTION = 0x1
+LMC_BK_PACKED_ATTENTION = 0x2
+LMC_BK_PACKED_STATE = 0x4
+
 LMC_KDA_LAST_BLOCK = 0
 LMC_KDA_EVERY_BLOCK = 1
 
@@ -119,6 +123,8 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("lmc_store", "lmc_load"):
         getattr(so, name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
                                       _i64, ctypes.c_void_p, ctypes.c_void_p]
+    so.lmc_layout_check_backends.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                             _P(ctypes.c_uint32)]
     so.lmc_object_bytes_blocks.argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, ctypes.c_int32, _P(_i64)]
     for name in ("lmc_store_blocks", "lmc_load_blocks"):
         getattr(so, name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, ctypes.c_void_p, _P(lmc_batch),
@@ -219,6 +225,9 @@ class Layout:
     def object_bytes(self, chunk: int, object_group: int) -> int:
         return lmc_object_bytes(self, chunk, object_group)
 
+    def check_backends(self, attn_indexes_by_stride: bool, state_pages_strided_ok: bool) -> int:
+        return lmc_layout_check_backends(self, attn_indexes_by_stride, state_pages_strided_ok)
+
     def object_bytes_q8(self, chunk: int, row_elems: int, object_group: int) -> int:
         return lmc_object_bytes_q8(self, chunk, row_elems, object_group)
 
@@ -246,6 +255,15 @@ def lmc_layout_build(layers, block_size: int, packed: bool, mem_bytes: int, spli
     h = ctypes.c_void_p()
     _check(_lib.lmc_layout_build(ctypes.byref(p), ctypes.byref(h)), "lmc_layout_build")
     return Layout(h.value)
+
+
+def lmc_layout_check_backends(layout: Layout, attn_indexes_by_stride: bool, state_pages_strided_ok: bool) -> int:
+    """LMC_BK_* bits of the eligibility rules the layout breaks (0: readable)."""
+    out = ctypes.c_uint32(0)
+    _check(_lib.lmc_layout_check_backends(layout.handle, int(bool(attn_indexes_by_stride)),
+                                          int(bool(state_pages_strided_ok)), ctypes.byref(out)),
+           "lmc_layout_check_backends")
+    return out.value
 
 
 def lmc_object_bytes(layout: Layout, chunk: int, object_group: int) -> int:

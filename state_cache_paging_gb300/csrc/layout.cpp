@@ -219,6 +219,29 @@ extern "C" int lmc_layout_query(const lmc_layout *L, lmc_layout_info *out) {
 
 extern "C" void lmc_layout_free(lmc_layout *L) { delete L; }
 
+extern "C" int lmc_layout_check_backends(const lmc_layout *L, int attn_indexes_by_stride,
+                                         int state_pages_strided_ok, uint32_t *out_bits) {
+    if (L == nullptr || out_bits == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    uint32_t bits = 0;
+    for (const lmc_layer_desc &d : L->desc) {
+        const bool attention = d.kind != LMC_LAYER_KDA;
+        if (L->mode == LMC_LAYOUT_PADDED) {
+            // vLLM pads a smaller page up to the unified one; for attention
+            // that is only legal when the backend strides by block
+            if (attention && d.page_bytes > d.real_bytes && !attn_indexes_by_stride)
+                bits |= LMC_BK_PADDED_ATTENTION;
+        } else if (attention) {
+            if (!attn_indexes_by_stride)
+                bits |= LMC_BK_PACKED_ATTENTION;
+        } else if (!state_pages_strided_ok) {
+            bits |= LMC_BK_PACKED_STATE;
+        }
+    }
+    *out_bits = bits;
+    return LMC_OK;
+}
+
 extern "C" int lmc_object_bytes(const lmc_layout *L, int64_t chunk, int32_t og, int64_t *out) {
     if (L == nullptr || out == nullptr || og < 0 || (size_t)og >= L->object_group_layers.size())
         return LMC_ERR_INVALID_ARG;

@@ -667,10 +667,35 @@ def check_q8_objects(lib):
                 assert np.array_equal(y, q_np.astype(np.float32) * s_np[:, None])
 
 
+def check_backends(lib):
+    """vLLM's eligibility rule ("How vLLM manages the KV cache of hybrid
+    models", §3.3): Kimi-Linear at its own N pads the KDA page (always
+    allowed); the 24-layer workload (N = 944 with a TP-1 state) pads the MLA
+    page, which needs stride-indexing attention; packed needs every backend to
+    stride, which KDA kernels that assume contiguous pages cannot; a pure
+    attention model packs when its backends stride."""
+    tp2 = [_kimi_linear_state(2), W.mla(1152)]
+    L = oracle.layout(tp2, 944, False, 1 << 40, _lib=lib)
+    assert L.check_backends(False, False) == 0
+    L = oracle.layout(W.CONFIGS[1].layers, 944, False, 1 << 40, _lib=lib)
+    assert L.check_backends(False, False) == oracle.BK_PADDED_ATTENTION
+    assert L.check_backends(True, False) == 0
+    L = oracle.layout(W.CONFIGS[1].layers, 944, True, 1 << 40, _lib=lib)
+    assert L.check_backends(True, False) == oracle.BK_PACKED_STATE
+    assert L.check_backends(False, False) == oracle.BK_PACKED_STATE | oracle.BK_PACKED_ATTENTION
+    assert L.check_backends(True, True) == 0
+    mla_only = [W.mla(1152), W.mla(656), W.mla(1152)]
+    L = oracle.layout(mla_only, 64, True, 1 << 30, _lib=lib)
+    assert L.check_backends(True, False) == 0 and L.check_backends(False, True) == oracle.BK_PACKED_ATTENTION
+    # equal pages: nothing is padded, any backend reads the padded path
+    L = oracle.layout([W.mla(1152), W.mla(1152)], 64, False, 1 << 30, _lib=lib)
+    assert L.check_backends(False, False) == 0
+
+
 ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",
        "check_budget", "check_page_formulas", "check_unified_block_size", "check_k3_groups", "check_closed_forms",
        "check_non_overlap", "check_store_load_cases", "check_block_objects", "check_copy_blocks",
-       "check_q8_golden", "check_q8_random", "check_q8_objects"]
+       "check_q8_golden", "check_q8_random", "check_q8_objects", "check_backends"]
 
 
 def check_store_load_cases(lib):

@@ -227,3 +227,16 @@ def test_q8_host_checks(lmc):
         assert fn(L.handle, 900, 128, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_NOT_MULTIPLE
         # the codec moves 16-byte vectors: an unaligned arena is refused before launch
         assert fn(L.handle, 944, 128, addr, ctypes.byref(b), addr + 4, 64, addr, None) == lmc.LMC_ERR_ALIGN
+
+
+def test_backend_rule_matches_oracle(lmc):
+    rng = np.random.default_rng(17)
+    cases = [(W.CONFIGS[i].layers, W.CONFIGS[i].N) for i in range(5)]
+    cases += [(P.random_spec(rng, int(rng.integers(1, 12))), int(rng.integers(1, 200))) for _ in range(60)]
+    for spec, N in cases:
+        for packed in (False, True):
+            o = oracle.layout(spec, N, packed, 1 << 40)
+            p = lmc.lmc_layout_build(spec, N, packed, 1 << 40)
+            for a in (False, True):
+                for b in (False, True):
+                    assert p.check_backends(a, b) == o.check_backends(a, b), (spec, N, packed, a, b)

@@ -41,6 +41,9 @@ MUTANTS = [
     ("codec drops the conv window", "    memcpy(rec, page, (size_t)l->conv_bytes);", "    memset(rec, 0, (size_t)l->conv_bytes);"),
     ("codec record has no scales", "    return l->conv_bytes + 4 * rows + rows * d;", "    return l->conv_bytes + rows * d;"),
     ("decoder ignores the scale", "float v = (float)codes[r * d + j] * scale;", "float v = (float)codes[r * d + j];"),
+    ("padded attention always allowed", "L->page_bytes[i] > L->real_bytes[i] && !attn_indexes_by_stride",
+     "L->page_bytes[i] > L->real_bytes[i] && !attn_indexes_by_stride && 0"),
+    ("packed state pages always allowed", "if (!attention && !state_pages_strided_ok)", "if (0)"),
     ("copy accepts block ids past the pool", "dst < 0 || dst >= L->num_blocks", "dst < 0 || dst > L->num_blocks + 1000000"),
     ("page copy one byte short", "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer]);",
      "memcpy(obj_bytes, page, (size_t)L->real_bytes[layer] - 1);"),
