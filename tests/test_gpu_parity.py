@@ -250,9 +250,12 @@ def test_full_size_kimi_linear_packed_lognormal(lmc):
     _full_size(lmc, W.CONFIGS[2])
 
 
-def test_full_size_k3_one_wave(lmc):
-    """K3 (93 layers, N = 768, chunk 1536): one request of 131,072 tokens."""
-    _full_size(lmc, W.CONFIGS[3], request_ids=[2], per_group=6)
+@pytest.mark.parametrize("wave", range(4))
+def test_full_size_k3_waves(lmc, wave):
+    """K3 (93 layers, N = 768, chunk 1536), 4 requests of 131,072 tokens in
+    4 waves of one request (a wave's pool, objects and fresh pool fill
+    ~116 GB)."""
+    _full_size(lmc, W.CONFIGS[3], request_ids=[wave], per_group=4)
 
 
 def _mixed_run(lmc, inp, Lp, pool, load_arena):
