@@ -290,30 +290,33 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 #endif
 constexpr int kRowVec = LMC_ROW_VEC;
 
-// One code: rint(x / scale) clamped. x * inv (inv = 1 / scale rounded) is
-// within a few ulps of x / scale; when that product is more than 1e-4 away
-// from a half-integer both round to the same integer, so the IEEE division
-// runs only near ties (and for subnormal scales, whose reciprocal may not be
-// finite). |x / scale| <= ~127 here, so 1e-4 is far above the products' error.
-__device__ __forceinline__ int code_of(float x, float scale, float inv, bool exact_only) {
-    float y = x * inv;
-    const float frac = fabsf(y - truncf(y));
-    if (exact_only || fabsf(frac - 0.5f) < 1e-4f)
-        y = __fdiv_rn(x, scale);
-    return max(-127, min(127, __float2int_rn(y)));
-}
-
+// Four codes rint(x / scale), clamped to [-127, 127], packed little-endian.
+// y = x * RN(1 / scale) is within a few ulps of the quotient x / scale, and
+// |x / scale| <= ~127 for a normal scale, so rint(y) == rint(x / scale)
+// unless y lies within 1e-4 of a half-integer; only then (or for a subnormal
+// scale, whose reciprocal may not be finite) are the four codes recomputed
+// with the IEEE division and the clamp. On the fast path rint(y) already lies
+// in [-127, 127].
 __device__ __forceinline__ uint32_t pack_codes(const float4 &v, float scale) {
     if (scale == 0.0f)
         return 0u;
-    const bool exact_only = scale < 1.17549435e-38f;  // subnormal scale
     const float inv = __frcp_rn(scale);
     const float c[4] = {v.x, v.y, v.z, v.w};
-    uint32_t packed = 0;
+    float r[4];
+    bool near = scale < 1.17549435e-38f;  // subnormal scale
 #pragma unroll
-    for (int t = 0; t < 4; t++)
-        packed |= (uint32_t)(uint8_t)(int8_t)code_of(c[t], scale, inv, exact_only) << (8 * t);
-    return packed;
+    for (int t = 0; t < 4; t++) {
+        const float y = c[t] * inv;
+        r[t] = rintf(y);
+        near |= fabsf(y - r[t]) > 0.4999f;
+    }
+    if (near) {
+#pragma unroll
+        for (int t = 0; t < 4; t++)
+            r[t] = fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(c[t], scale))));
+    }
+    return ((uint32_t)__float2int_rz(r[0]) & 0xffu) | (((uint32_t)__float2int_rz(r[1]) & 0xffu) << 8) |
+           (((uint32_t)__float2int_rz(r[2]) & 0xffu) << 16) | ((uint32_t)__float2int_rz(r[3]) << 24);
 }
 
 __device__ __forceinline__ float4 unpack_codes(uint32_t p, float scale) {
