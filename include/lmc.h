@@ -344,6 +344,16 @@ int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems,
 int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, int32_t object_group,
                         int64_t *out);
 
+/* ---- diagnostics ----------------------------------------------------------- */
+
+/* Self-test of the device-side failure reporting: launches one thread that
+ * polls, with the same bounded wait the bulk-copy engine uses, an mbarrier
+ * that nothing completes, and ORs LMC_ST_TIMEOUT into *status (device)
+ * after `rounds` polls (1 .. 2^22); no copy is in flight, so the context
+ * stays usable. No counterpart on the pages (it tests this library's own
+ * error path). Errors: INVALID_ARG, ALIGN, CUDA. */
+int lmc_selftest_wait(uint32_t *status, int64_t rounds, void *stream);
+
 /* Static description of a code ("LMC_OK", ...); never NULL. */
 const char *lmc_strerror(int code);
 

@@ -135,6 +135,7 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
         getattr(so, name).argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
                                       _i64, ctypes.c_void_p, ctypes.c_void_p]
     so.lmc_object_bytes_q8.argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_int32, _P(_i64)]
+    so.lmc_selftest_wait.argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p]
     so.lmc_strerror.argtypes = [ctypes.c_int]
     so.lmc_strerror.restype = ctypes.c_char_p
     return so
@@ -392,6 +393,11 @@ def lmc_load_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, 
     _check(_lib.lmc_load_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
                             arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
                             _stream_ptr(stream)), "lmc_load_q8")
+
+
+def lmc_selftest_wait(status, rounds: int, stream=None) -> None:
+    """Runs the bounded-wait self-test: LMC_ST_TIMEOUT lands in `status`."""
+    _check(_lib.lmc_selftest_wait(status.data_ptr(), int(rounds), _stream_ptr(stream)), "lmc_selftest_wait")
 
 
 def pairs_to_device(pairs: np.ndarray, device):

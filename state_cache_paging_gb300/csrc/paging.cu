@@ -271,7 +271,7 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // (d = 16 .. 512 in powers of two); other row lengths take one row per warp.
 // Codec kernel shapes picked by measurement on GB300 (Kimi-Linear, d = 128):
 // two float4 per lane, and more, smaller CTAs than the copies (the encoder's
-// register budget would otherwise cap residency): 128 x 16 for encode, 256 x 8
+// register budget would otherwise cap residency): 128 x 12 for encode, 256 x 8
 // for decode.
 #ifndef LMC_ROW_VEC
 #define LMC_ROW_VEC 2
@@ -280,7 +280,7 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 #define LMC_Q8_ENC_THREADS 128
 #endif
 #ifndef LMC_Q8_ENC_MIN_BLOCKS
-#define LMC_Q8_ENC_MIN_BLOCKS 16
+#define LMC_Q8_ENC_MIN_BLOCKS 12
 #endif
 #ifndef LMC_Q8_DEC_THREADS
 #define LMC_Q8_DEC_THREADS 256
@@ -537,11 +537,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t k = 0; k < kWaitLimit; k++)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+    for (uint32_t k = 0; k < limit; k++)
         if (mbar_try_wait(bar, parity))
             return true;
     return false;
+}
+
+// Self-test of the bounded wait: one thread polls an mbarrier that nothing
+// will complete (no arrival is expected, no copy targets it) and, when the
+// limit runs out, reports LMC_ST_TIMEOUT like the bulk engine does.
+__global__ void lmc_selftest_wait_kernel(uint32_t *status, uint32_t rounds) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0)
+        return;
+    mbar_init(&bar);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!mbar_wait(&bar, 0u, rounds))
+        atomicOr(status, LMC_ST_TIMEOUT);
 }
 
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -1036,4 +1049,13 @@ extern "C" int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size,
     }
     *out = total;
     return LMC_OK;
+}
+
+extern "C" int lmc_selftest_wait(uint32_t *status, int64_t rounds, void *stream) {
+    if (status == nullptr || rounds <= 0 || rounds > (int64_t)kWaitLimit)
+        return LMC_ERR_INVALID_ARG;
+    if (((uintptr_t)status & 3) != 0)
+        return LMC_ERR_ALIGN;
+    lmc_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, (uint32_t)rounds);
+    return cudaGetLastError() == cudaSuccess ? LMC_OK : LMC_ERR_CUDA;
 }

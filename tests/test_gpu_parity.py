@@ -648,3 +648,15 @@ def test_q8_full_size_kimi_linear(lmc):
     for pg in pages_d:
         lo, n = int(pg["pool_offset"]), int(pg["bytes"])
         assert np.array_equal(fresh[lo:lo + n].cpu().numpy(), back[lo:lo + n])
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(lmc):
+    """A bounded wait that runs out (an mbarrier nothing completes) sets
+    LMC_ST_TIMEOUT; the context stays usable: a store right after it still
+    matches the oracle."""
+    st = _status()
+    lmc.lmc_selftest_wait(st, 1000)
+    torch.cuda.synchronize()
+    assert int(st.item()) == lmc.LMC_ST_TIMEOUT
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    _full_exact(lmc, inp, Lp)

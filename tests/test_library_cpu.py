@@ -240,3 +240,12 @@ def test_backend_rule_matches_oracle(lmc):
             for a in (False, True):
                 for b in (False, True):
                     assert p.check_backends(a, b) == o.check_backends(a, b), (spec, N, packed, a, b)
+
+
+def test_selftest_wait_host_checks(lmc):
+    buf = (ctypes.c_uint8 * 16)()
+    addr = ctypes.addressof(buf)
+    assert lmc._lib.lmc_selftest_wait(addr, 0, None) == lmc.LMC_ERR_INVALID_ARG
+    assert lmc._lib.lmc_selftest_wait(addr, 1 << 30, None) == lmc.LMC_ERR_INVALID_ARG
+    assert lmc._lib.lmc_selftest_wait(None, 10, None) == lmc.LMC_ERR_INVALID_ARG
+    assert lmc._lib.lmc_selftest_wait((addr + 3) // 4 * 4 + 1, 10, None) == lmc.LMC_ERR_ALIGN
