@@ -660,3 +660,25 @@ def test_bounded_wait_reports_timeout_and_context_survives(lmc):
     assert int(st.item()) == lmc.LMC_ST_TIMEOUT
     inp, Lp = case_inputs(W.CONFIGS[0])
     _full_exact(lmc, inp, Lp)
+
+
+def test_odd_page_sizes_blocks_and_copies_exact(lmc):
+    """Odd page sizes (not 16-byte multiples) take the byte-wise kernels:
+    block-granular objects (tails, every-block snapshots) and in-pool copies."""
+    spec = [W.mla(18), {"kind": "KDA", "token_bytes": 0, "conv_bytes": 6, "rec_bytes": 70001, "window": 0},
+            W.swa(7, 32), W.mla(18)]
+    cfg = W.Config(210, "odd", spec, N=8, requested_chunk=20, packed=True, num_requests=3,
+                   lengths="fixed", fixed_lengths=(50, 97, 33), seed=5)
+    inp, Lp = case_inputs(cfg)
+    _blocks_exact(lmc, inp, Lp, "every")
+    _blocks_exact(lmc, inp, Lp, "tails")
+    o = inp.layout
+    rng = np.random.default_rng(77)
+    pairs = _random_pairs(o, rng, 4, o.num_blocks // 2)
+    pool_h = W.fill_normal_np(o.pool_bytes, 78)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    st = _status()
+    lmc.lmc_copy_blocks(Lp, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == oracle.copy_blocks(o, pool_h, pairs) == 0
+    assert np.array_equal(pool.cpu().numpy(), pool_h)
