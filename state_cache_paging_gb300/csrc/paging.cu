@@ -297,13 +297,27 @@ constexpr int kRowVec = LMC_ROW_VEC;
 // scale, whose reciprocal may not be finite) are the four codes recomputed
 // with the IEEE division and the clamp. On the fast path rint(y) already lies
 // in [-127, 127].
-__device__ __forceinline__ uint32_t pack_codes(const float4 &v, float scale) {
+struct RowScale {
+    float scale;  // max|x| / 127
+    float inv;    // RN(1 / scale)
+    bool exact;   // subnormal scale: always divide
+};
+
+__device__ __forceinline__ RowScale row_scale(float amax) {
+    RowScale rs;
+    rs.scale = __fdiv_rn(amax, 127.0f);
+    rs.inv = rs.scale != 0.0f ? __frcp_rn(rs.scale) : 0.0f;
+    rs.exact = rs.scale < 1.17549435e-38f;
+    return rs;
+}
+
+__device__ __forceinline__ uint32_t pack_codes(const float4 &v, const RowScale &rs) {
+    const float scale = rs.scale, inv = rs.inv;
     if (scale == 0.0f)
         return 0u;
-    const float inv = __frcp_rn(scale);
     const float c[4] = {v.x, v.y, v.z, v.w};
     float r[4];
-    bool near = scale < 1.17549435e-38f;  // subnormal scale
+    bool near = rs.exact;
 #pragma unroll
     for (int t = 0; t < 4; t++) {
         const float y = c[t] * inv;
@@ -365,13 +379,13 @@ __device__ __forceinline__ void encode_rows(const Span &s, int d) {
             for (int o = lpr >> 1; o > 0; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             if (live) {
-                const float scale = __fdiv_rn(amax, 127.0f);
+                const RowScale rs = row_scale(amax);
                 if (l == 0)
-                    reinterpret_cast<float *>(s.scales)[r] = scale;
+                    reinterpret_cast<float *>(s.scales)[r] = rs.scale;
                 uint32_t q[kRowVec];
 #pragma unroll
                 for (int w = 0; w < kRowVec; w++)
-                    q[w] = pack_codes(v[w], scale);
+                    q[w] = pack_codes(v[w], rs);
                 uint32_t *out = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d) + l * kRowVec;
                 if (kRowVec == 4)
                     *reinterpret_cast<uint4 *>(out) = make_uint4(q[0], q[1], q[2], q[3]);
@@ -390,12 +404,12 @@ __device__ __forceinline__ void encode_rows(const Span &s, int d) {
             amax = fmaxf(amax, absmax4(__ldg(x + e)));
         for (int o = 16; o > 0; o >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float scale = __fdiv_rn(amax, 127.0f);
+        const RowScale rs = row_scale(amax);
         if (lane == 0)
-            reinterpret_cast<float *>(s.scales)[r] = scale;
+            reinterpret_cast<float *>(s.scales)[r] = rs.scale;
         uint32_t *q = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d);
         for (int e = lane; e < nvec; e += 32)
-            q[e] = pack_codes(__ldg(x + e), scale);
+            q[e] = pack_codes(__ldg(x + e), rs);
     }
 }
 
