@@ -156,6 +156,29 @@ __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) {
                  : "memory");
 }
 
+#ifndef LMC_VEC32
+#define LMC_VEC32 0  // 1: 32-byte (256-bit) loads/stores for tiles whose ends are 32-byte aligned
+#endif
+
+struct alignas(32) u8x32 {
+    uint4 lo, hi;
+};
+
+__device__ __forceinline__ u8x32 ld_stream32(const u8x32 *p) {
+    u8x32 v;
+    asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y), "=r"(v.hi.z),
+          "=r"(v.hi.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream32(u8x32 *p, const u8x32 &v) {
+    asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.lo.x), "r"(v.lo.y),
+                 "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x), "r"(v.hi.y), "r"(v.hi.z), "r"(v.hi.w)
+                 : "memory");
+}
+
 // A resolved tile: copy `bytes` from src to dst.
 struct Span {
     const uint8_t *src;
@@ -468,6 +491,25 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
             encode_rows<kNT>(s, P.q8_row);
         } else if (kCodec == 2 && s.codec == 2) {
             decode_rows<kNT>(s, P.q8_row);
+        } else if (kVec && LMC_VEC32 &&
+                   ((reinterpret_cast<uintptr_t>(s.src) | reinterpret_cast<uintptr_t>(s.dst) | (uint32_t)s.bytes) &
+                    31) == 0) {
+            const u8x32 *src = reinterpret_cast<const u8x32 *>(s.src);
+            u8x32 *dst = reinterpret_cast<u8x32 *>(s.dst);
+            const int n = s.bytes >> 5;
+            constexpr int kU = kUnroll > 1 ? kUnroll / 2 : 1;
+            int i = threadIdx.x;
+            for (; i + (kU - 1) * kNT < n; i += kU * kNT) {
+                u8x32 v[kU];
+#pragma unroll
+                for (int w = 0; w < kU; w++)
+                    v[w] = ld_stream32(src + i + w * kNT);
+#pragma unroll
+                for (int w = 0; w < kU; w++)
+                    st_stream32(dst + i + w * kNT, v[w]);
+            }
+            for (; i < n; i += kNT)
+                st_stream32(dst + i, ld_stream32(src + i));
         } else if (kVec) {
             const uint4 *src = reinterpret_cast<const uint4 *>(s.src);
             uint4 *dst = reinterpret_cast<uint4 *>(s.dst);
@@ -703,7 +745,8 @@ int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t 
     const int32_t seg = (int32_t)d.real_bytes;
     const int32_t pieces = (seg + kTileBytes - 1) / kTileBytes;
     int32_t tb = (seg + pieces - 1) / pieces;
-    tb = (tb + 15) & ~15;  // 16-byte pieces; the last one is shorter
+    const int32_t align = seg % 32 == 0 ? 32 : 16;  // keep 32-byte pages in 32-byte pieces
+    tb = (tb + align - 1) / align * align;          // the last piece is shorter
     Entry &E = P.entries[ne++];
     E.pool_base = d.base;
     E.pool_stride = d.stride;
