@@ -43,6 +43,13 @@
 
 #include <stdint.h>
 
+/* Only the lmc_* entry points are exported from liblmc.so. */
+#if defined(__GNUC__)
+#define LMC_API __attribute__((visibility("default")))
+#else
+#define LMC_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -146,14 +153,14 @@ typedef struct {
  * largest group total, base = offset, stride = block_stride.
  * *out receives a layout owned by the caller (free with lmc_layout_free).
  * Errors: INVALID_ARG (bad spec), NO_MEMORY (not one whole block), OVERFLOW. */
-int lmc_layout_build(const lmc_layout_params *params, lmc_layout **out);
+LMC_API int lmc_layout_build(const lmc_layout_params *params, lmc_layout **out);
 
 /* Fills *out with the layout's geometry; the arrays point into the layout and
  * live until lmc_layout_free. */
-int lmc_layout_query(const lmc_layout *layout, lmc_layout_info *out);
+LMC_API int lmc_layout_query(const lmc_layout *layout, lmc_layout_info *out);
 
 /* Frees a layout (NULL is ignored). No call using it may still be running. */
-void lmc_layout_free(lmc_layout *layout);
+LMC_API void lmc_layout_free(lmc_layout *layout);
 
 /* Backend-eligibility bits of lmc_layout_check_backends. */
 #define LMC_BK_PADDED_ATTENTION 0x1u /* padded path pads an attention page, but the
@@ -169,7 +176,7 @@ void lmc_layout_free(lmc_layout *layout);
  * (causal_conv1d, chunk_kda) cannot, so such models fall back to the padded
  * path. *out_bits gets the LMC_BK_* bits of every rule broken (0: readable).
  * The store/load calls themselves work on any layout. */
-int lmc_layout_check_backends(const lmc_layout *layout, int attn_indexes_by_stride, int state_pages_strided_ok,
+LMC_API int lmc_layout_check_backends(const lmc_layout *layout, int attn_indexes_by_stride, int state_pages_strided_ok,
                               uint32_t *out_bits);
 
 /* Bytes of one object of `object_group` for chunk size `chunk` ([HM] object
@@ -177,7 +184,7 @@ int lmc_layout_check_backends(const lmc_layout *layout, int attn_indexes_by_stri
  * chunk / N pages of real_bytes (the chunk's tokens in order), a KDA layer one
  * state snapshot of real_bytes. Error NOT_MULTIPLE if chunk is not a positive
  * multiple of N. */
-int lmc_object_bytes(const lmc_layout *layout, int64_t chunk, int32_t object_group,
+LMC_API int lmc_object_bytes(const lmc_layout *layout, int64_t chunk, int32_t object_group,
                      int64_t *out);
 
 /* Chunk-size negotiation ([K3] "Chunk-Size Negotiation"): *out = the smallest
@@ -186,18 +193,18 @@ int lmc_object_bytes(const lmc_layout *layout, int64_t chunk, int32_t object_gro
  * `requested` must already be a positive multiple of block_size, else
  * NOT_MULTIPLE (INVALID_ARG when requested <= 0). Errors: INVALID_ARG when
  * block_size <= 0 or out is NULL, OVERFLOW. */
-int lmc_negotiate_chunk(int64_t requested, int64_t block_size, int strict, int64_t *out);
+LMC_API int lmc_negotiate_chunk(int64_t requested, int64_t block_size, int strict, int64_t *out);
 
 /* Scheduler budget rule ([KL] "Why these settings", [HM] Step 2): OK when
  * N <= max_batched < 2N, or max_batched >= 2N with separate object groups;
  * BUDGET otherwise; INVALID_ARG for non-positive arguments. */
-int lmc_check_step_budget(int64_t block_size, int64_t max_batched, int separate_object_groups);
+LMC_API int lmc_check_step_budget(int64_t block_size, int64_t max_batched, int separate_object_groups);
 
 /* Smallest multiple of `align` tokens whose attention page
  * (N * attn_token_bytes) is at least `state_page_bytes` ([HM] Step 1, [KL]
  * note on N). With Kimi-Linear's 1152-byte MLA entry and align 16 this gives
  * 944 for the TP-2 state page and 1888 for TP 1. */
-int lmc_unified_block_size(int64_t attn_token_bytes, int64_t state_page_bytes, int64_t align,
+LMC_API int lmc_unified_block_size(int64_t attn_token_bytes, int64_t state_page_bytes, int64_t align,
                            int64_t *out);
 
 /* ---- store / load -------------------------------------------------------- */
@@ -241,7 +248,7 @@ typedef struct {
  * pool: device, >= pool_bytes, read only. arena: device, arena_bytes bytes.
  * status: device uint32, 4-byte aligned; bits are OR-ed, never cleared.
  * Errors (host): INVALID_ARG, NOT_MULTIPLE, ALIGN, CUDA (launch failure). */
-int lmc_store(const lmc_layout *layout, int64_t chunk_size, const void *pool,
+LMC_API int lmc_store(const lmc_layout *layout, int64_t chunk_size, const void *pool,
               const lmc_batch *batch, void *arena, int64_t arena_bytes, uint32_t *status,
               void *stream);
 
@@ -250,7 +257,7 @@ int lmc_store(const lmc_layout *layout, int64_t chunk_size, const void *pool,
  * hit's state becomes the initial state; [MC] restore at a checkpoint).
  * Writes only the real bytes of the addressed pages; every other pool byte
  * is left as it was. Same arguments and errors as lmc_store. */
-int lmc_load(const lmc_layout *layout, int64_t chunk_size, void *pool,
+LMC_API int lmc_load(const lmc_layout *layout, int64_t chunk_size, void *pool,
              const lmc_batch *batch, const void *arena, int64_t arena_bytes, uint32_t *status,
              void *stream);
 
@@ -266,7 +273,7 @@ int lmc_load(const lmc_layout *layout, int64_t chunk_size, void *pool,
  * With blocks_per_object = chunk / N and LMC_KDA_LAST_BLOCK this equals
  * lmc_object_bytes. Error INVALID_ARG for blocks_per_object <= 0 or an
  * unknown kda_mode. */
-int lmc_object_bytes_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+LMC_API int lmc_object_bytes_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
                             int32_t object_group, int64_t *out);
 
 /* Block-granular store/load: like lmc_store/lmc_load, but each job's `chunk`
@@ -278,10 +285,10 @@ int lmc_object_bytes_blocks(const lmc_layout *layout, int64_t blocks_per_object,
  * LMC_KDA_EVERY_BLOCK, the snapshots of every block boundary inside an
  * object ([KL] the [N, 2N) regime; [VB] §7). Same arguments, ownership,
  * status bits and errors as lmc_store/lmc_load otherwise. */
-int lmc_store_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+LMC_API int lmc_store_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
                      const void *pool, const lmc_batch *batch, void *arena, int64_t arena_bytes,
                      uint32_t *status, void *stream);
-int lmc_load_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode, void *pool,
+LMC_API int lmc_load_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode, void *pool,
                     const lmc_batch *batch, const void *arena, int64_t arena_bytes, uint32_t *status,
                     void *stream);
 
@@ -311,7 +318,7 @@ typedef struct {
  * pairs are skipped. Destination blocks must be distinct and must not be the
  * source of another pair of the same call (they would race); src == dst is
  * a no-op. Asynchronous on `stream`; errors INVALID_ARG, ALIGN, CUDA. */
-int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy_batch *batch, uint32_t *status,
+LMC_API int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy_batch *batch, uint32_t *status,
                     void *stream);
 
 /* ---- INT8 per-channel codec of the KDA recurrent state ------------------- */
@@ -334,14 +341,14 @@ int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy_batch *
  * conv_bytes a multiple of 16, so records stay multiples of 16 bytes
  * (INVALID_ARG otherwise), and 16-byte aligned pool and arena (ALIGN).
  * Other arguments, status bits and errors as lmc_store / lmc_load. */
-int lmc_store_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, const void *pool,
+LMC_API int lmc_store_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, const void *pool,
                  const lmc_batch *batch, void *arena, int64_t arena_bytes, uint32_t *status, void *stream);
-int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, void *pool,
+LMC_API int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, void *pool,
                 const lmc_batch *batch, const void *arena, int64_t arena_bytes, uint32_t *status,
                 void *stream);
 
 /* Bytes of one chunk object of `object_group` as lmc_store_q8 writes it. */
-int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, int32_t object_group,
+LMC_API int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, int32_t object_group,
                         int64_t *out);
 
 /* ---- diagnostics ----------------------------------------------------------- */
@@ -352,10 +359,10 @@ int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t ro
  * after `rounds` polls (1 .. 2^22); no copy is in flight, so the context
  * stays usable. No counterpart on the pages (it tests this library's own
  * error path). Errors: INVALID_ARG, ALIGN, CUDA. */
-int lmc_selftest_wait(uint32_t *status, int64_t rounds, void *stream);
+LMC_API int lmc_selftest_wait(uint32_t *status, int64_t rounds, void *stream);
 
 /* Static description of a code ("LMC_OK", ...); never NULL. */
-const char *lmc_strerror(int code);
+LMC_API const char *lmc_strerror(int code);
 
 #ifdef __cplusplus
 }

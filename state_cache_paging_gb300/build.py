@@ -29,7 +29,7 @@ CXX = os.environ.get("CXX", "g++")
 def _sources():
     out = []
     for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cpp", ".h")):
+        if name.endswith((".cu", ".cpp", ".h", ".map")):
             out.append(os.path.join(CSRC, name))
     out.append(os.path.join(INCLUDE, "lmc.h"))
     return out
@@ -54,9 +54,10 @@ def build_library(force: bool = False, extra_nvcc=(), out_path: str | None = Non
     cpp_obj = os.path.join(work, "layout.o")
     ptxas_log = os.path.join(BUILD_DIR, "ptxas.log")
     cmds = [
-        [NVCC, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
+        [NVCC, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xptxas", "-v", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC, *extra_nvcc, "-c", os.path.join(CSRC, "paging.cu"), "-o", cu_obj],
-        [CXX, "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE, "-I", CSRC,
+        [CXX, "-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE,
+         "-I", CSRC,
          "-c", os.path.join(CSRC, "layout.cpp"), "-o", cpp_obj],
     ]
     procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True) for c in cmds]
@@ -69,7 +70,8 @@ def build_library(force: bool = False, extra_nvcc=(), out_path: str | None = Non
     if verbose:
         print(logs[0])
     tmp = os.path.join(work, "liblmc.so")
-    link = [NVCC, "-shared", *ARCH, "-o", tmp, cu_obj, cpp_obj]
+    link = [NVCC, "-shared", *ARCH, "-Xlinker", "--version-script=" + os.path.join(CSRC, "liblmc.map"),
+            "-o", tmp, cu_obj, cpp_obj]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout}{r.stderr}")
