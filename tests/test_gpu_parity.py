@@ -682,3 +682,68 @@ def test_odd_page_sizes_blocks_and_copies_exact(lmc):
     torch.cuda.synchronize()
     assert int(st.item()) == oracle.copy_blocks(o, pool_h, pairs) == 0
     assert np.array_equal(pool.cpu().numpy(), pool_h)
+
+
+class _MappedHost:
+    """Pinned, mapped host memory viewed through its device address (the
+    library takes any device-accessible pointer as the arena)."""
+
+    def __init__(self, nbytes):
+        import ctypes
+        torch.zeros(1, device=DEV)
+        path = [l.split()[-1] for l in open("/proc/self/maps") if "libcudart.so" in l][0]
+        self.rt = rt = ctypes.CDLL(path)
+        rt.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+        rt.cudaHostGetDevicePointer.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_uint]
+        rt.cudaFreeHost.argtypes = [ctypes.c_void_p]
+        h, d = ctypes.c_void_p(), ctypes.c_void_p()
+        assert rt.cudaHostAlloc(ctypes.byref(h), nbytes, 2) == 0  # cudaHostAllocMapped
+        assert rt.cudaHostGetDevicePointer(ctypes.byref(d), h, 0) == 0
+        self.h, self.d, self.n = h.value, d.value, nbytes
+        self.host = np.ctypeslib.as_array((ctypes.c_uint8 * nbytes).from_address(self.h))
+
+    def data_ptr(self):
+        return self.d
+
+    def numel(self):
+        return self.n
+
+    def element_size(self):
+        return 1
+
+    def free(self):
+        self.rt.cudaFreeHost(ctypes_void(self.h))
+
+
+def ctypes_void(x):
+    import ctypes
+    return ctypes.c_void_p(x)
+
+
+@pytest.mark.parametrize("cfg_index,ids", [(0, None), (1, [0, 1])])
+def test_host_resident_arena_exact(lmc, cfg_index, ids):
+    """The arena may live in mapped pinned host memory (a host cache tier):
+    the kernels store into and load from it across the host link, with the
+    same bytes as the oracle."""
+    inp, Lp = case_inputs(W.CONFIGS[cfg_index], request_ids=ids)
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 90 + cfg_index)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    host = _MappedHost(inp.arena_bytes)
+    try:
+        host.host[:] = 0x3C
+        fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+        st = _status()
+        jobs = dev_jobs(inp.jobs, DEV)
+        lmc.lmc_store(Lp, C, pool, dev_tables(inp.tables_src, DEV), jobs, host, st)
+        lmc.lmc_load(Lp, C, fresh, dev_tables(inp.tables_dst, DEV), jobs, host, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        arena_o = np.full(inp.arena_bytes, 0x3C, dtype=np.uint8)
+        assert oracle.store(Lo, C, pool_h, inp.tables_src, inp.jobs, arena_o) == 0
+        assert np.array_equal(host.host, arena_o)
+        fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        assert oracle.load(Lo, C, fresh_o, inp.tables_dst, inp.jobs, arena_o) == 0
+        assert np.array_equal(fresh.cpu().numpy(), fresh_o)
+    finally:
+        host.free()
