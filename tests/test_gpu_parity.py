@@ -6,6 +6,8 @@ benchmark times and are checked on oracle-recomputed samples plus properties
 that hold at any size (store after load reproduces the objects; pool bytes
 outside the addressed pages stay untouched).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -689,7 +691,6 @@ class _MappedHost:
     library takes any device-accessible pointer as the arena)."""
 
     def __init__(self, nbytes):
-        import ctypes
         torch.zeros(1, device=DEV)
         path = [l.split()[-1] for l in open("/proc/self/maps") if "libcudart.so" in l][0]
         self.rt = rt = ctypes.CDLL(path)
@@ -712,12 +713,7 @@ class _MappedHost:
         return 1
 
     def free(self):
-        self.rt.cudaFreeHost(ctypes_void(self.h))
-
-
-def ctypes_void(x):
-    import ctypes
-    return ctypes.c_void_p(x)
+        self.rt.cudaFreeHost(ctypes.c_void_p(self.h))
 
 
 @pytest.mark.parametrize("cfg_index,ids", [(0, None), (1, [0, 1])])
