@@ -743,3 +743,41 @@ def test_host_resident_arena_exact(lmc, cfg_index, ids):
         assert np.array_equal(fresh.cpu().numpy(), fresh_o)
     finally:
         host.free()
+
+
+def test_store_load_captured_in_cuda_graph(lmc):
+    """store + load captured into one CUDA graph and replayed: the replay
+    moves the same bytes as the oracle (the entry points enqueue only a
+    kernel launch on the given stream; the first call on a device caches its
+    SM count, so it is made before capture)."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 95)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    arena = torch.zeros(inp.arena_bytes, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+    jobs = dev_jobs(inp.jobs, DEV)
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside capture
+        lmc.lmc_store(Lp, C, pool, t_src, jobs, arena, st, side)
+    torch.cuda.synchronize()
+    arena.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        lmc.lmc_store(Lp, C, pool, t_src, jobs, arena, st, side)
+        lmc.lmc_load(Lp, C, fresh, t_dst, jobs, arena, st, side)
+    torch.cuda.synchronize()
+    assert not arena.any(), "capture must not execute the kernels"
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    arena_o = np.zeros(inp.arena_bytes, dtype=np.uint8)
+    assert oracle.store(Lo, C, pool_h, inp.tables_src, inp.jobs, arena_o) == 0
+    fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    assert oracle.load(Lo, C, fresh_o, inp.tables_dst, inp.jobs, arena_o) == 0
+    assert np.array_equal(arena.cpu().numpy(), arena_o)
+    assert np.array_equal(fresh.cpu().numpy(), fresh_o)
