@@ -778,7 +778,7 @@ int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t 
 // bytes, encoded as an INT8 record (scales, then codes) at the object's
 // current offset; `rows_per_tile` rows per tile.
 int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_spec &spec, int32_t pos_add,
-                    int64_t &obj, int64_t &tiles) {
+                    int64_t &obj, int64_t &tiles, bool &vec) {
     if (ne >= kMaxEntries)
         return LMC_ERR_INVALID_ARG;
     const int64_t row = P.q8_row;
@@ -801,6 +801,8 @@ int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_s
     E.kv = (int16_t)d.kv_group;
     obj += 4 * rows + rows * row;
     tiles += E.tiles_per_seg;
+    // the rows are read and written as 16-byte vectors
+    vec = vec && aligned16(d.base) && aligned16(d.stride) && aligned16(spec.conv_bytes);
     return tiles > INT32_MAX ? LMC_ERR_OVERFLOW : LMC_OK;
 }
 
@@ -888,7 +890,7 @@ int build_object_plan(const lmc_layout *L, const Shape &sh, const void *pool, co
                 rc = conv.real_bytes > 0 ? add_entry(P, ne, conv, 1, (int32_t)(sh.nb - 1), obj, tiles, vec)
                                          : LMC_OK;
                 if (rc == LMC_OK)
-                    rc = add_codec_entry(P, ne, d, L->specs[i], (int32_t)(sh.nb - 1), obj, tiles);
+                    rc = add_codec_entry(P, ne, d, L->specs[i], (int32_t)(sh.nb - 1), obj, tiles, vec);
             } else {
                 rc = add_entry(P, ne, d, last_only ? 1 : sh.nb, last_only ? (int32_t)(sh.nb - 1) : 0, obj, tiles,
                                vec);

@@ -249,3 +249,21 @@ def test_selftest_wait_host_checks(lmc):
     assert lmc._lib.lmc_selftest_wait(addr, 1 << 30, None) == lmc.LMC_ERR_INVALID_ARG
     assert lmc._lib.lmc_selftest_wait(None, 10, None) == lmc.LMC_ERR_INVALID_ARG
     assert lmc._lib.lmc_selftest_wait((addr + 3) // 4 * 4 + 1, 10, None) == lmc.LMC_ERR_ALIGN
+
+
+def test_q8_refuses_unaligned_state_pages(lmc):
+    """A KDA layer without a conv window whose pages sit at odd offsets (an
+    odd-sized attention page pads the padded layout) cannot go through the
+    16-byte codec: the call is refused before launch."""
+    spec = [{"kind": "KDA", "token_bytes": 0, "conv_bytes": 0, "rec_bytes": 4096, "window": 0}, W.mla(17)]
+    L = lmc.lmc_layout_build(spec, 300, False, 1 << 24)  # page = 5100 bytes: not a 16-byte multiple
+    assert L.page_size % 16 != 0
+    buf = (ctypes.c_uint8 * 256)()
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+    tables = (lmc.lmc_block_table * L.num_kv_groups)(*[lmc.lmc_block_table(addr, 4, 4)] * L.num_kv_groups)
+    jobs = (ctypes.c_void_p * L.num_object_groups)(*[addr] * L.num_object_groups)
+    counts = (ctypes.c_int64 * L.num_object_groups)(*[0] * L.num_object_groups)
+    counts[L.object_group[0]] = 1  # only the KDA group has a job
+    b = lmc.lmc_batch(1, L.num_kv_groups, tables, L.num_object_groups, 0, jobs, counts)
+    assert lmc._lib.lmc_store_q8(L.handle, 300, 16, addr, ctypes.byref(b), addr, 4096, addr, None) \
+        == lmc.LMC_ERR_ALIGN
