@@ -656,6 +656,8 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline and args.op == "paging":
         threads = os.cpu_count() or 1
         line["cpu_baseline"] = oracle_sample(args.config, requests=8, reps=20, threads=threads)
+        one = oracle_sample(args.config, requests=2, reps=2, threads=1)
+        line["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
