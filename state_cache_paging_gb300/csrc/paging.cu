@@ -500,38 +500,38 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
         } else if (kVec && LMC_VEC32 &&
                    ((reinterpret_cast<uintptr_t>(s.src) | reinterpret_cast<uintptr_t>(s.dst) | (uint32_t)s.bytes) &
                     31) == 0) {
+            // every load of a round is issued before its stores: up to
+            // LMC_VEC32_UNROLL 32-byte vectors in flight per thread
             const u8x32 *src = reinterpret_cast<const u8x32 *>(s.src);
             u8x32 *dst = reinterpret_cast<u8x32 *>(s.dst);
             const int n = s.bytes >> 5;
             constexpr int kU = LMC_VEC32_UNROLL;
-            int i = threadIdx.x;
-            for (; i + (kU - 1) * kNT < n; i += kU * kNT) {
+            for (int base = threadIdx.x; base < n; base += kU * kNT) {
                 u8x32 v[kU];
 #pragma unroll
                 for (int w = 0; w < kU; w++)
-                    v[w] = ld_stream32(src + i + w * kNT);
+                    if (base + w * kNT < n)
+                        v[w] = ld_stream32(src + base + w * kNT);
 #pragma unroll
                 for (int w = 0; w < kU; w++)
-                    st_stream32(dst + i + w * kNT, v[w]);
+                    if (base + w * kNT < n)
+                        st_stream32(dst + base + w * kNT, v[w]);
             }
-            for (; i < n; i += kNT)
-                st_stream32(dst + i, ld_stream32(src + i));
         } else if (kVec) {
             const uint4 *src = reinterpret_cast<const uint4 *>(s.src);
             uint4 *dst = reinterpret_cast<uint4 *>(s.dst);
             const int n = s.bytes >> 4;
-            int i = threadIdx.x;
-            for (; i + (kUnroll - 1) * kNT < n; i += kUnroll * kNT) {
+            for (int base = threadIdx.x; base < n; base += kUnroll * kNT) {
                 uint4 v[kUnroll];
 #pragma unroll
                 for (int w = 0; w < kUnroll; w++)
-                    v[w] = ld_stream(src + i + w * kNT);
+                    if (base + w * kNT < n)
+                        v[w] = ld_stream(src + base + w * kNT);
 #pragma unroll
                 for (int w = 0; w < kUnroll; w++)
-                    st_stream(dst + i + w * kNT, v[w]);
+                    if (base + w * kNT < n)
+                        st_stream(dst + base + w * kNT, v[w]);
             }
-            for (; i < n; i += kNT)
-                st_stream(dst + i, ld_stream(src + i));
         } else {
             for (int i = threadIdx.x; i < s.bytes; i += kNT)
                 s.dst[i] = s.src[i];
