@@ -32,13 +32,13 @@
 #include "lmc_internal.h"
 
 // Defaults picked by measurement on GB300 (Kimi-Linear and K3 workloads):
-// 32 KB tiles, 512 threads, 4 vectors in flight per thread, i.e. one CTA
-// moves its whole tile with a single round of loads and stores.
+// 32 KB tiles, 256 threads, four 32-byte vectors in flight per thread, i.e.
+// one CTA moves its whole tile with a single round of loads and stores.
 #ifndef LMC_TILE_BYTES
 #define LMC_TILE_BYTES 32768
 #endif
 #ifndef LMC_THREADS
-#define LMC_THREADS 512
+#define LMC_THREADS 256
 #endif
 #ifndef LMC_UNROLL
 #define LMC_UNROLL 4
