@@ -43,6 +43,9 @@
 #ifndef LMC_UNROLL
 #define LMC_UNROLL 4
 #endif
+#ifndef LMC_MIN_BLOCKS
+#define LMC_MIN_BLOCKS 1  // resident CTAs per SM the copy kernels are compiled for
+#endif
 #ifndef LMC_ENGINE
 #define LMC_ENGINE 0  // 0: vector loads/stores, 1: bulk (TMA) copies through shared memory
 #endif
@@ -483,7 +486,9 @@ __device__ __forceinline__ void decode_rows(const Span &s, int d) {
 
 // Vector engine: every thread of the CTA copies 16-byte vectors of the tile,
 // kUnroll loads in flight before the matching stores.
-template <bool kVec, int kCodec, int kNT = kThreads>
+// kU32 / kU16: vectors per thread per round on the 32- / 16-byte paths (the
+// codec kernels, which run under a tight register budget, copy with one).
+template <bool kVec, int kCodec, int kNT = kThreads, int kU32 = LMC_VEC32_UNROLL, int kU16 = kUnroll>
 __device__ __forceinline__ void copy_tiles(const Plan &P) {
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
         Span s;
@@ -505,7 +510,7 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
             const u8x32 *src = reinterpret_cast<const u8x32 *>(s.src);
             u8x32 *dst = reinterpret_cast<u8x32 *>(s.dst);
             const int n = s.bytes >> 5;
-            constexpr int kU = LMC_VEC32_UNROLL;
+            constexpr int kU = kU32;
             for (int base = threadIdx.x; base < n; base += kU * kNT) {
                 u8x32 v[kU];
 #pragma unroll
@@ -521,14 +526,14 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
             const uint4 *src = reinterpret_cast<const uint4 *>(s.src);
             uint4 *dst = reinterpret_cast<uint4 *>(s.dst);
             const int n = s.bytes >> 4;
-            for (int base = threadIdx.x; base < n; base += kUnroll * kNT) {
-                uint4 v[kUnroll];
+            for (int base = threadIdx.x; base < n; base += kU16 * kNT) {
+                uint4 v[kU16];
 #pragma unroll
-                for (int w = 0; w < kUnroll; w++)
+                for (int w = 0; w < kU16; w++)
                     if (base + w * kNT < n)
                         v[w] = ld_stream(src + base + w * kNT);
 #pragma unroll
-                for (int w = 0; w < kUnroll; w++)
+                for (int w = 0; w < kU16; w++)
                     if (base + w * kNT < n)
                         st_stream(dst + base + w * kNT, v[w]);
             }
@@ -542,26 +547,26 @@ __device__ __forceinline__ void copy_tiles(const Plan &P) {
 // Distinct names per operation (they share the body; the plan's mode says
 // which side is the pool).
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) lmc_store_kernel(const __grid_constant__ Plan P) {
+__global__ void __launch_bounds__(kThreads, LMC_MIN_BLOCKS) lmc_store_kernel(const __grid_constant__ Plan P) {
     copy_tiles<kVec, 0>(P);
 }
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) lmc_load_kernel(const __grid_constant__ Plan P) {
+__global__ void __launch_bounds__(kThreads, LMC_MIN_BLOCKS) lmc_load_kernel(const __grid_constant__ Plan P) {
     copy_tiles<kVec, 0>(P);
 }
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) lmc_copy_kernel(const __grid_constant__ Plan P) {
+__global__ void __launch_bounds__(kThreads, LMC_MIN_BLOCKS) lmc_copy_kernel(const __grid_constant__ Plan P) {
     copy_tiles<kVec, 0>(P);
 }
 constexpr int kEncThreads = LMC_Q8_ENC_THREADS;
 constexpr int kDecThreads = LMC_Q8_DEC_THREADS;
 __global__ void __launch_bounds__(kEncThreads, LMC_Q8_ENC_MIN_BLOCKS)
     lmc_store_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 1, kEncThreads>(P);
+    copy_tiles<true, 1, kEncThreads, 1, 1>(P);
 }
 __global__ void __launch_bounds__(kDecThreads, LMC_Q8_DEC_MIN_BLOCKS)
     lmc_load_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 2, kDecThreads>(P);
+    copy_tiles<true, 2, kDecThreads, 1, 1>(P);
 }
 
 // ---------------------------------------------------------------------------
