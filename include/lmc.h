@@ -244,7 +244,8 @@ typedef struct {
  * copied back to back (token-major), a KDA layer's snapshot at position
  * (chunk + 1) * m - 1, the state at the chunk's end ([KL] snapshots at block
  * boundaries; [MC] restores resume only from a boundary checkpoint).
- * Only real bytes are copied; padding is never read.
+ * Only real bytes are copied; padding is never read. A launch handles layouts
+ * of up to 64 KV groups and 64 object groups (INVALID_ARG beyond).
  * pool: device, >= pool_bytes, read only. arena: device, arena_bytes bytes.
  * status: device uint32, 4-byte aligned; bits are OR-ed, never cleared.
  * Errors (host): INVALID_ARG, NOT_MULTIPLE, ALIGN, CUDA (launch failure). */

@@ -781,3 +781,23 @@ def test_store_load_captured_in_cuda_graph(lmc):
     assert oracle.load(Lo, C, fresh_o, inp.tables_dst, inp.jobs, arena_o) == 0
     assert np.array_equal(arena.cpu().numpy(), arena_o)
     assert np.array_equal(fresh.cpu().numpy(), fresh_o)
+
+
+def _max_spec():
+    """256 layers: 62 sliding windows x 4 layers, 4 MLA, 4 KDA; one KV group
+    per spec gives 64 KV groups and 64 object groups (the library's limits)."""
+    spec = [W.mla(48)] * 4 + [{"kind": "KDA", "token_bytes": 0, "conv_bytes": 32, "rec_bytes": 512,
+                               "window": 0}] * 4
+    for k in range(62):
+        spec += [W.swa(16 * (1 + k % 3), 4 * (1 + k))] * 4
+    return [dict(l) for l in spec]
+
+
+def test_maximum_layout_exact(lmc):
+    spec = _max_spec()
+    cfg = W.Config(500, "max", spec, N=4, requested_chunk=8, packed=True, num_requests=3, lengths="fixed",
+                   fixed_lengths=(40, 23, 57), seed=11)
+    inp, Lp = case_inputs(cfg, split=False)
+    assert Lp.num_layers == 256 and Lp.num_kv_groups == 64 and Lp.num_object_groups == 64
+    _full_exact(lmc, inp, Lp)
+    _blocks_exact(lmc, inp, Lp, "every")

@@ -267,3 +267,18 @@ def test_q8_refuses_unaligned_state_pages(lmc):
     b = lmc.lmc_batch(1, L.num_kv_groups, tables, L.num_object_groups, 0, jobs, counts)
     assert lmc._lib.lmc_store_q8(L.handle, 300, 16, addr, ctypes.byref(b), addr, 4096, addr, None) \
         == lmc.LMC_ERR_ALIGN
+
+
+def test_store_refuses_layouts_past_the_launch_limits(lmc):
+    """store/load accept at most 64 KV groups and 64 object groups."""
+    spec = [W.mla(16)] + [W.swa(16, 4 * (1 + k)) for k in range(64)]  # 65 windows classes
+    L = lmc.lmc_layout_build(spec, 4, True, 1 << 30, False)
+    assert L.num_object_groups == 65 and L.num_kv_groups == 65
+    buf = (ctypes.c_uint8 * 64)()
+    addr = ctypes.addressof(buf)
+    g, o = L.num_kv_groups, L.num_object_groups
+    tables = (lmc.lmc_block_table * g)(*[lmc.lmc_block_table(addr, 4, 4)] * g)
+    jobs = (ctypes.c_void_p * o)(*[addr] * o)
+    counts = (ctypes.c_int64 * o)(*[0] * o)
+    b = lmc.lmc_batch(1, g, tables, o, 0, jobs, counts)
+    assert lmc._lib.lmc_store(L.handle, 4, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
