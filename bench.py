@@ -54,15 +54,17 @@ def _kernel_sha():
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel: str, workload_index: int):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+def _traffic(kernel: str, workload_index: int, op: str):
+    """DRAM bytes per launch of `kernel` (its function name) on a workload and
+    operation from the committed ncu summary, or None when none was taken or
+    the kernel source changed since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = t.get(f"config{workload_index}", {}).get(kernel)
+    key = f"config{workload_index}" + ("" if op == "paging" else f"/{op}")
+    entry = t.get(key, {}).get(kernel)
     if not entry or entry.get("kernel_sha") != _kernel_sha():
         return None
     return entry.get("dram_bytes_per_launch")
@@ -618,15 +620,16 @@ def run_gpu(args):
     value = S.bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = _peaks()
     st_avg, ld_avg = statistics.mean(store_ms), statistics.mean(load_ms)
+    suffix = "_q8_kernel" if args.op == "q8" else "_kernel"
     if args.op == "copy":
-        dominant, dom_bytes, dom_ms = "copy", S.bytes_per_step, st_avg
+        dominant, dom_bytes, dom_ms = "lmc_copy_kernel", S.bytes_per_step, st_avg
     elif cfg.mixed:
         # the two kernels share HBM concurrently: the roofline is the step's
-        dominant, dom_bytes, dom_ms = "store+load (concurrent)", S.bytes_per_step, ms_per_step
+        dominant, dom_bytes, dom_ms = "lmc_store_kernel+lmc_load_kernel (concurrent)", S.bytes_per_step, ms_per_step
     elif st_avg >= ld_avg:
-        dominant, dom_bytes, dom_ms = "store", S.store_bytes, st_avg
+        dominant, dom_bytes, dom_ms = "lmc_store" + suffix, S.store_bytes, st_avg
     else:
-        dominant, dom_bytes, dom_ms = "load", S.load_bytes, ld_avg
+        dominant, dom_bytes, dom_ms = "lmc_load" + suffix, S.load_bytes, ld_avg
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -646,7 +649,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic(dominant, cfg.index) if args.requests is None else None,
+                     "traffic": _traffic(dominant, cfg.index, args.op) if args.requests is None else None,
                      "algorithmic_bytes_per_launch": dom_bytes},
         "e2e": {"value": round(S.bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h},

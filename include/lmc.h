@@ -362,6 +362,17 @@ LMC_API int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, in
  * error path). Errors: INVALID_ARG, ALIGN, CUDA. */
 LMC_API int lmc_selftest_wait(uint32_t *status, int64_t rounds, void *stream);
 
+/* Self-test of the INT8 codec's row scale (see lmc_store_q8): for each of
+ * the n fp32 values amax[i] (device, 4-byte aligned), writes the scale the
+ * encoder stores (which must equal amax / 127 in IEEE binary32 division),
+ * the inverse it multiplies by (0 where the encoder divides instead) and,
+ * for comparison, the quotient by CUDA's IEEE division. Only finite,
+ * non-negative amax is meaningful (a row maximum). No counterpart on the
+ * pages (it tests this library's arithmetic). Errors: INVALID_ARG, ALIGN,
+ * CUDA. */
+LMC_API int lmc_selftest_row_scale(const float *amax, float *scale, float *inv, float *ieee, int64_t n,
+                                   void *stream);
+
 /* Static description of a code ("LMC_OK", ...); never NULL. */
 LMC_API const char *lmc_strerror(int code);
 

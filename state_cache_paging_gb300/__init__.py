@@ -136,6 +136,7 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
                                       _i64, ctypes.c_void_p, ctypes.c_void_p]
     so.lmc_object_bytes_q8.argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_int32, _P(_i64)]
     so.lmc_selftest_wait.argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p]
+    so.lmc_selftest_row_scale.argtypes = [ctypes.c_void_p] * 4 + [_i64, ctypes.c_void_p]
     so.lmc_strerror.argtypes = [ctypes.c_int]
     so.lmc_strerror.restype = ctypes.c_char_p
     return so
@@ -398,6 +399,17 @@ def lmc_load_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, 
 def lmc_selftest_wait(status, rounds: int, stream=None) -> None:
     """Runs the bounded-wait self-test: LMC_ST_TIMEOUT lands in `status`."""
     _check(_lib.lmc_selftest_wait(status.data_ptr(), int(rounds), _stream_ptr(stream)), "lmc_selftest_wait")
+
+
+def lmc_selftest_row_scale(amax, scale, inv, ieee, stream=None) -> None:
+    """The codec's row scale and inverse for each value of the float32
+    device tensor `amax`, with CUDA's IEEE quotient amax / 127 beside them."""
+    n = amax.numel()
+    for t in (scale, inv, ieee):
+        if t.numel() != n:
+            raise ValueError("lmc_selftest_row_scale: output sizes differ from amax")
+    _check(_lib.lmc_selftest_row_scale(amax.data_ptr(), scale.data_ptr(), inv.data_ptr(), ieee.data_ptr(), n,
+                                       _stream_ptr(stream)), "lmc_selftest_row_scale")
 
 
 def pairs_to_device(pairs: np.ndarray, device):

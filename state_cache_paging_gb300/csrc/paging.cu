@@ -212,7 +212,9 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
     }
     const Group &G = P.groups[g];
     const int64_t local = tile - G.tile_begin;
-    const int64_t q = local / G.tiles_per_obj;  // job (or pair) index
+    // job (or pair) index; a 32-bit division whenever the offset fits
+    const int64_t q = local <= INT32_MAX ? (int64_t)((uint32_t)local / (uint32_t)G.tiles_per_obj)
+                                         : local / G.tiles_per_obj;
     const int32_t t = (int32_t)(local - q * G.tiles_per_obj);
 
     // layer entry: the last one whose first tile is <= t
@@ -295,16 +297,21 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // [-127, 127] (IEEE binary32 division), zero rows give scale 0 and codes 0;
 // decode = code * scale.
 //
-// Work split: a row's d / 4 float4 vectors are spread over `lpr` lanes of a
-// warp, kRowVec consecutive vectors per lane, so 32 / lpr rows share a warp
-// and every lane has kRowVec 16-byte loads in flight; the row maximum is a
-// shuffle reduction inside each aligned group of lpr lanes. This needs
-// d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two <= 32
-// (d = 16 .. 512 in powers of two); other row lengths take one row per warp.
+// Encode work split: a row's d / 4 float4 vectors are spread over `lpr` lanes
+// of a warp, kRowVec consecutive vectors per lane, so 32 / lpr rows share a
+// warp; the row maximum is a shuffle reduction inside each aligned group of
+// lpr lanes, and each lane loads its vectors of the warp's next rows before it
+// quantises the current ones, so loads stay in flight during the arithmetic.
+// This needs d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two
+// <= 32 (d = 16 .. 512 in powers of two); other row lengths take one row per
+// warp. Decode is flat over the tile's codes: 16 codes (one 16-byte load) per
+// thread per round, kDecUnroll rounds of loads issued before their stores,
+// values written as whole 32-byte sectors.
 // Codec kernel shapes picked by measurement on GB300 (Kimi-Linear, d = 128):
-// two float4 per lane, and more, smaller CTAs than the copies (the encoder's
-// register budget would otherwise cap residency): 128 x 12 for encode, 256 x 8
-// for decode.
+// the encoder is bound by the latency of its per-row chain (loads, maximum,
+// scale, codes), so it wants the most resident warps (128 x 12: 6.73 TB/s;
+// 128 x 10: 6.64; 128 x 9: 6.32; 4 float4 per lane at 128 x 8: 6.65); the
+// decoder runs at 256 x 6 with two rounds in flight (7.02 TB/s).
 #ifndef LMC_ROW_VEC
 #define LMC_ROW_VEC 2
 #endif
@@ -318,64 +325,148 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 #define LMC_Q8_DEC_THREADS 256
 #endif
 #ifndef LMC_Q8_DEC_MIN_BLOCKS
-#define LMC_Q8_DEC_MIN_BLOCKS 8
+#define LMC_Q8_DEC_MIN_BLOCKS 6
+#endif
+#ifndef LMC_Q8_DEC_UNROLL
+#define LMC_Q8_DEC_UNROLL 2
+#endif
+#ifndef LMC_Q8_COPY_UNROLL
+#define LMC_Q8_COPY_UNROLL 1  // vectors per thread per round on the codec kernels' plain pages
+#endif
+#ifndef LMC_Q8_TILE_BYTES
+#define LMC_Q8_TILE_BYTES 32768  // fp32 state bytes per codec tile
 #endif
 constexpr int kRowVec = LMC_ROW_VEC;
+constexpr int kQ8TileBytes = LMC_Q8_TILE_BYTES;
+constexpr int kDecUnroll = LMC_Q8_DEC_UNROLL;
 
-// Four codes rint(x / scale), clamped to [-127, 127], packed little-endian.
-// y = x * RN(1 / scale) is within a few ulps of the quotient x / scale, and
-// |x / scale| <= ~127 for a normal scale, so rint(y) == rint(x / scale)
-// unless y lies within 1e-4 of a half-integer; only then (or for a subnormal
-// scale, whose reciprocal may not be finite) are the four codes recomputed
-// with the IEEE division and the clamp. On the fast path rint(y) already lies
-// in [-127, 127].
+// Rounding by addition: for |y| <= 2^22, RN(y + 1.5 * 2^23) equals
+// 1.5 * 2^23 + rint(y) (ties to even: the floats of [2^23, 2^24) are the
+// integers, and 1.5 * 2^23 is even), and since the bit pattern of 1.5 * 2^23
+// ends in a zero byte, the low byte of the sum's bit pattern is rint(y) as a
+// two's-complement byte.
+constexpr float kRoundAdd = 12582912.0f;  // 1.5 * 2^23
+
 struct RowScale {
-    float scale;  // max|x| / 127
-    float inv;    // RN(1 / scale)
-    bool exact;   // subnormal scale: always divide
+    float scale;  // RN(max|x| / 127)
+    float inv;    // ~1 / scale (relative error <= 2^-22), 0 for a zero row
+    bool exact;   // tiny or huge maximum: every code by the IEEE quotient
 };
 
+// scale = RN(amax / 127) by Markstein's correction of a reciprocal product
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(amax * z)
+// with z = RN(1 / 127) is within an ulp of the quotient, the residual
+// r = amax - 127 * q0 is exact with one FMA, and RN(q0 + r * z) is the
+// correctly rounded quotient (checked against the IEEE division for every
+// finite non-negative amax). Below 2^-100 (subnormal quotients) the IEEE
+// division itself is used. inv = RN(127 * rcp.approx(amax)): within 2^-22
+// of 1 / scale, so |x * inv - x / scale| <= 127 * 2^-22 < 4e-5 for |x| <= amax.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ RowScale row_scale(float amax) {
+    constexpr float kInv127 = 1.0f / 127.0f;
     RowScale rs;
-    rs.scale = __fdiv_rn(amax, 127.0f);
-    rs.inv = rs.scale != 0.0f ? __frcp_rn(rs.scale) : 0.0f;
-    rs.exact = rs.scale < 1.17549435e-38f;
+    if (amax >= 7.88860905e-31f) {  // 2^-100
+        const float q0 = amax * kInv127;
+        rs.scale = fmaf(fmaf(-q0, 127.0f, amax), kInv127, q0);
+    } else {
+        rs.scale = __fdiv_rn(amax, 127.0f);
+    }
+    rs.exact = amax != 0.0f && (amax < 7.88860905e-31f || amax > 4.25352959e37f);  // outside [2^-100, 2^125]
+    rs.inv = (amax == 0.0f || rs.exact) ? 0.0f : 127.0f * rcp_approx(amax);
     return rs;
 }
 
-__device__ __forceinline__ uint32_t pack_codes(const float4 &v, const RowScale &rs) {
-    const float scale = rs.scale, inv = rs.inv;
+// Maximum over each aligned group of `lanes` lanes (a power of two), by a
+// butterfly of shuffles (measured faster here than redux.sync on the bit
+// patterns).
+__device__ __forceinline__ float group_max(float v, int lanes) {
+    for (int o = lanes >> 1; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t pack_low_bytes(float t0, float t1, float t2, float t3) {
+    const uint32_t lo = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040);
+    const uint32_t hi = __byte_perm(__float_as_uint(t2), __float_as_uint(t3), 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
+}
+
+// Four codes, packed little-endian: t = RN(x * inv + 1.5 * 2^23) rounds the
+// exact product x * inv, which lies within 4e-5 of the exact quotient
+// x / scale, and RN(x / scale) lies within 8e-6 of it. So unless the product
+// is within 1e-4 of a half-integer, rint(RN(x / scale)) equals the product's
+// rounding; `worst` collects |x * inv - rint| (one rounding of an exact
+// residual) so the caller can tell. For a zero row (inv = 0) every code is 0;
+// |x * inv| < 127.01 keeps every code inside [-127, 127].
+__device__ __forceinline__ uint32_t quant4(const float4 &v, float inv, float &worst) {
+    const float t0 = fmaf(v.x, inv, kRoundAdd), t1 = fmaf(v.y, inv, kRoundAdd);
+    const float t2 = fmaf(v.z, inv, kRoundAdd), t3 = fmaf(v.w, inv, kRoundAdd);
+    const float e0 = fmaf(v.x, inv, kRoundAdd - t0), e1 = fmaf(v.y, inv, kRoundAdd - t1);
+    const float e2 = fmaf(v.z, inv, kRoundAdd - t2), e3 = fmaf(v.w, inv, kRoundAdd - t3);
+    worst = fmaxf(worst, fmaxf(fmaxf(fabsf(e0), fabsf(e1)), fmaxf(fabsf(e2), fabsf(e3))));
+    return pack_low_bytes(t0, t1, t2, t3);
+}
+
+// The same four codes by the definition: IEEE quotient, rint, clamp.
+__device__ __forceinline__ uint32_t quant4_exact(const float4 &v, float scale) {
     if (scale == 0.0f)
         return 0u;
     const float c[4] = {v.x, v.y, v.z, v.w};
-    float r[4];
-    bool near = rs.exact;
+    float t[4];
 #pragma unroll
-    for (int t = 0; t < 4; t++) {
-        const float y = c[t] * inv;
-        r[t] = rintf(y);
-        near |= fabsf(y - r[t]) > 0.4999f;
-    }
-    if (near) {
-#pragma unroll
-        for (int t = 0; t < 4; t++)
-            r[t] = fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(c[t], scale))));
-    }
-    return ((uint32_t)__float2int_rz(r[0]) & 0xffu) | (((uint32_t)__float2int_rz(r[1]) & 0xffu) << 8) |
-           (((uint32_t)__float2int_rz(r[2]) & 0xffu) << 16) | ((uint32_t)__float2int_rz(r[3]) << 24);
+    for (int k = 0; k < 4; k++)
+        t[k] = fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(c[k], scale)))) + kRoundAdd;
+    return pack_low_bytes(t[0], t[1], t[2], t[3]);
 }
 
+// A lane's share of a row: if any product came within 1e-4 of a half-integer
+// (or the row's maximum is tiny or huge) every code is recomputed by the
+// definition.
+template <int kN>
+__device__ __forceinline__ void quant_lane(const float4 (&v)[kN], const RowScale &rs, uint32_t (&q)[kN]) {
+    float worst = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kN; w++)
+        q[w] = quant4(v[w], rs.inv, worst);
+    if (rs.exact || worst > 0.4999f) {
+#pragma unroll
+        for (int w = 0; w < kN; w++)
+            q[w] = quant4_exact(v[w], rs.scale);
+    }
+}
+
+// Four values from four codes: the bit pattern 0x4B0000nn with nn = code ^ 0x80
+// is the float 2^23 + 128 + code, so one subtraction (exact) recovers the
+// code as a float; then one IEEE product with the scale.
 __device__ __forceinline__ float4 unpack_codes(uint32_t p, float scale) {
+    const uint32_t b = p ^ 0x80808080u;
+    constexpr float kBase = 8388736.0f;  // 2^23 + 128
     float4 o;
-    o.x = (float)(int8_t)(p & 0xffu) * scale;
-    o.y = (float)(int8_t)((p >> 8) & 0xffu) * scale;
-    o.z = (float)(int8_t)((p >> 16) & 0xffu) * scale;
-    o.w = (float)(int8_t)(p >> 24) * scale;
+    o.x = (__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7440)) - kBase) * scale;
+    o.y = (__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7441)) - kBase) * scale;
+    o.z = (__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7442)) - kBase) * scale;
+    o.w = (__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7443)) - kBase) * scale;
     return o;
 }
 
 __device__ __forceinline__ float absmax4(const float4 &v) {
     return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+
+__device__ __forceinline__ float4 ld_stream_f4(const float4 *p) {
+    const uint4 u = ld_stream(reinterpret_cast<const uint4 *>(p));
+    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+
+__device__ __forceinline__ void st_stream_f4(float4 *p, const float4 &v) {
+    st_stream(reinterpret_cast<uint4 *>(p),
+              make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w)));
 }
 
 __device__ __forceinline__ bool grouped_rows(int d, int &lpr) {
@@ -386,108 +477,166 @@ __device__ __forceinline__ bool grouped_rows(int d, int &lpr) {
     return lpr <= 32 && (lpr & (lpr - 1)) == 0;
 }
 
+// A lane's kRowVec consecutive float4 of one row (16-byte loads: measured
+// as fast as 32-byte ones here, with fewer registers).
+__device__ __forceinline__ void load_lane(float4 (&v)[kRowVec], const float4 *p) {
+#pragma unroll
+    for (int w = 0; w < kRowVec; w++)
+        v[w] = ld_stream_f4(p + w);
+}
+
 template <int kNT>
-__device__ __forceinline__ void encode_rows(const Span &s, int d) {
+__device__ __forceinline__ void encode_grouped(const Span &s, int d, int lpr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int kWarps = kNT / 32;
     const int nvec = d >> 2;
+    float *scales = reinterpret_cast<float *>(s.scales);
+    const int per_warp = 32 / lpr, sub = lane / lpr, l = lane % lpr;
+    const int step = kWarps * per_warp;
+    const float4 *src = reinterpret_cast<const float4 *>(s.src) + l * kRowVec;
+    float4 next[kRowVec];
+    int r = warp * per_warp + sub;
+    if (r < s.bytes)
+        load_lane(next, src + (int64_t)r * nvec);
+    for (int base = warp * per_warp; base < s.bytes; base += step, r += step) {
+        const bool live = r < s.bytes;
+        float4 v[kRowVec];
+#pragma unroll
+        for (int w = 0; w < kRowVec; w++)
+            v[w] = next[w];
+        if (r + step < s.bytes)  // the next rows' loads stay in flight during this round
+            load_lane(next, src + (int64_t)(r + step) * nvec);
+        float amax = 0.0f;
+        if (live) {
+#pragma unroll
+            for (int w = 0; w < kRowVec; w++)
+                amax = fmaxf(amax, absmax4(v[w]));
+        }
+        amax = group_max(amax, lpr);
+        if (live) {
+            const RowScale rs = row_scale(amax);
+            if (l == 0)
+                scales[r] = rs.scale;
+            uint32_t q[kRowVec];
+            quant_lane(v, rs, q);
+            uint32_t *out = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d) + l * kRowVec;
+            if (kRowVec == 4)
+                *reinterpret_cast<uint4 *>(out) = make_uint4(q[0], q[1], q[2 % kRowVec], q[3 % kRowVec]);
+            else if (kRowVec == 2)
+                *reinterpret_cast<uint2 *>(out) = make_uint2(q[0], q[1 % kRowVec]);
+            else
+#pragma unroll
+                for (int w = 0; w < kRowVec; w++)
+                    out[w] = q[w];
+        }
+    }
+}
+
+// s.bytes rows of d values at s.src -> codes at s.dst, scales at s.scales.
+template <int kNT>
+__device__ __forceinline__ void encode_rows(const Span &s, int d) {
     int lpr;
     if (grouped_rows(d, lpr)) {
-        const int per_warp = 32 / lpr, sub = lane / lpr, l = lane % lpr;
-        for (int base = warp * per_warp; base < s.bytes; base += kWarps * per_warp) {
-            const int r = base + sub;
-            const bool live = r < s.bytes;
-            float4 v[kRowVec];
-            float amax = 0.0f;
-            if (live) {
-                const float4 *x = reinterpret_cast<const float4 *>(s.src) + (int64_t)r * nvec + l * kRowVec;
-#pragma unroll
-                for (int w = 0; w < kRowVec; w++)
-                    v[w] = __ldg(x + w);
-#pragma unroll
-                for (int w = 0; w < kRowVec; w++)
-                    amax = fmaxf(amax, absmax4(v[w]));
-            }
-            for (int o = lpr >> 1; o > 0; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            if (live) {
-                const RowScale rs = row_scale(amax);
-                if (l == 0)
-                    reinterpret_cast<float *>(s.scales)[r] = rs.scale;
-                uint32_t q[kRowVec];
-#pragma unroll
-                for (int w = 0; w < kRowVec; w++)
-                    q[w] = pack_codes(v[w], rs);
-                uint32_t *out = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d) + l * kRowVec;
-                if (kRowVec == 4)
-                    *reinterpret_cast<uint4 *>(out) = make_uint4(q[0], q[1], q[2], q[3]);
-                else
-#pragma unroll
-                    for (int w = 0; w < kRowVec; w++)
-                        out[w] = q[w];
-            }
-        }
+        encode_grouped<kNT>(s, d, lpr);
         return;
     }
-    for (int r = warp; r < s.bytes; r += kWarps) {  // one row per warp
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWarps = kNT / 32;
+    const int nvec = d >> 2;
+    float *scales = reinterpret_cast<float *>(s.scales);
+    for (int r = warp; r < s.bytes; r += kWarps) {  // other row lengths: one row per warp
         const float4 *x = reinterpret_cast<const float4 *>(s.src) + (int64_t)r * nvec;
         float amax = 0.0f;
         for (int e = lane; e < nvec; e += 32)
-            amax = fmaxf(amax, absmax4(__ldg(x + e)));
-        for (int o = 16; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            amax = fmaxf(amax, absmax4(ld_stream_f4(x + e)));
+        amax = group_max(amax, 32);
         const RowScale rs = row_scale(amax);
         if (lane == 0)
-            reinterpret_cast<float *>(s.scales)[r] = rs.scale;
+            scales[r] = rs.scale;
         uint32_t *q = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d);
-        for (int e = lane; e < nvec; e += 32)
-            q[e] = pack_codes(__ldg(x + e), rs);
+        for (int e = lane; e < nvec; e += 32) {
+            const float4 v[1] = {ld_stream_f4(x + e)};
+            uint32_t c[1];
+            quant_lane(v, rs, c);
+            q[e] = c[0];
+        }
+    }
+}
+
+// Codes at s.src (s.bytes rows of d) and scales at s.scales -> values at
+// s.dst. The tile's rows are a multiple of 4 and d % 4 == 0, so its codes are
+// whole 16-byte vectors, each covering one row (d a power of two >= 16) or up
+// to four. kU rounds of loads are issued before their stores; with kWide the
+// 64 output bytes of a vector go out as two 32-byte stores (whole sectors).
+template <int kNT, bool kOneRow, int kU, bool kWide>
+__device__ __forceinline__ void decode_flat(const Span &s, int d) {
+    const int n = (s.bytes * d) >> 4;
+    const uint4 *codes = reinterpret_cast<const uint4 *>(s.src);
+    const float *scales = reinterpret_cast<const float *>(s.scales);
+    float4 *x = reinterpret_cast<float4 *>(s.dst);
+    const int shift = __ffs(d) - 1;
+    for (int base = threadIdx.x; base < n; base += kU * kNT) {
+        uint4 c[kU];
+        float sc[kU][kOneRow ? 1 : 4];
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int v = base + u * kNT;
+            if (v < n) {
+                c[u] = ld_stream(codes + v);
+                if (kOneRow) {
+                    sc[u][0] = __ldg(scales + ((v << 4) >> shift));
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 4; w++)
+                        sc[u][w] = __ldg(scales + ((v << 4) + 4 * w) / d);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int v = base + u * kNT;
+            if (v < n) {
+                const uint32_t w4[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+                float4 o[4];
+#pragma unroll
+                for (int w = 0; w < 4; w++)
+                    o[w] = unpack_codes(w4[w], sc[u][kOneRow ? 0 : w]);
+                if (kWide) {
+#pragma unroll
+                    for (int w = 0; w < 4; w += 2) {
+                        u8x32 p;
+                        p.lo = make_uint4(__float_as_uint(o[w].x), __float_as_uint(o[w].y), __float_as_uint(o[w].z),
+                                          __float_as_uint(o[w].w));
+                        p.hi = make_uint4(__float_as_uint(o[w + 1].x), __float_as_uint(o[w + 1].y),
+                                          __float_as_uint(o[w + 1].z), __float_as_uint(o[w + 1].w));
+                        st_stream32(reinterpret_cast<u8x32 *>(x + 4 * (int64_t)v + w), p);
+                    }
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 4; w++)
+                        st_stream_f4(x + 4 * (int64_t)v + w, o[w]);
+                }
+            }
+        }
     }
 }
 
 template <int kNT>
 __device__ __forceinline__ void decode_rows(const Span &s, int d) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int kWarps = kNT / 32;
-    const int nvec = d >> 2;
-    int lpr;
-    if (grouped_rows(d, lpr)) {
-        const int per_warp = 32 / lpr, sub = lane / lpr, l = lane % lpr;
-        for (int base = warp * per_warp; base < s.bytes; base += kWarps * per_warp) {
-            const int r = base + sub;
-            if (r >= s.bytes)
-                continue;
-            const float scale = __ldg(reinterpret_cast<const float *>(s.scales) + r);
-            const uint32_t *q = reinterpret_cast<const uint32_t *>(s.src + (int64_t)r * d) + l * kRowVec;
-            uint32_t c[kRowVec];
-            if (kRowVec == 4) {
-                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(q));
-                c[0] = u.x, c[1] = u.y, c[2] = u.z, c[3] = u.w;
-            } else {
-#pragma unroll
-                for (int w = 0; w < kRowVec; w++)
-                    c[w] = __ldg(q + w);
-            }
-            float4 *x = reinterpret_cast<float4 *>(s.dst) + (int64_t)r * nvec + l * kRowVec;
-#pragma unroll
-            for (int w = 0; w < kRowVec; w++)
-                x[w] = unpack_codes(c[w], scale);
-        }
-        return;
-    }
-    for (int r = warp; r < s.bytes; r += kWarps) {  // one row per warp
-        const float scale = __ldg(reinterpret_cast<const float *>(s.scales) + r);
-        const uint32_t *q = reinterpret_cast<const uint32_t *>(s.src + (int64_t)r * d);
-        float4 *x = reinterpret_cast<float4 *>(s.dst) + (int64_t)r * nvec;
-        for (int e = lane; e < nvec; e += 32)
-            x[e] = unpack_codes(__ldg(q + e), scale);
+    if (d >= 16 && (d & (d - 1)) == 0) {
+        if ((reinterpret_cast<uintptr_t>(s.dst) & 31) == 0)
+            decode_flat<kNT, true, kDecUnroll, true>(s, d);
+        else
+            decode_flat<kNT, true, kDecUnroll, false>(s, d);
+    } else {
+        decode_flat<kNT, false, 1, false>(s, d);  // other row lengths: tested, not tuned
     }
 }
 
-// Vector engine: every thread of the CTA copies 16-byte vectors of the tile,
-// kUnroll loads in flight before the matching stores.
+// Vector engine: every thread of the CTA copies 32-byte (or 16-byte) vectors
+// of the tile, all loads of a round issued before the matching stores.
 // kU32 / kU16: vectors per thread per round on the 32- / 16-byte paths (the
-// codec kernels, which run under a tight register budget, copy with one).
+// codec kernels, which run under a tighter register budget, copy with fewer).
 template <bool kVec, int kCodec, int kNT = kThreads, int kU32 = LMC_VEC32_UNROLL, int kU16 = kUnroll>
 __device__ __forceinline__ void copy_tiles(const Plan &P) {
     for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
@@ -562,11 +711,11 @@ constexpr int kEncThreads = LMC_Q8_ENC_THREADS;
 constexpr int kDecThreads = LMC_Q8_DEC_THREADS;
 __global__ void __launch_bounds__(kEncThreads, LMC_Q8_ENC_MIN_BLOCKS)
     lmc_store_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 1, kEncThreads, 1, 1>(P);
+    copy_tiles<true, 1, kEncThreads, LMC_Q8_COPY_UNROLL, LMC_Q8_COPY_UNROLL>(P);
 }
 __global__ void __launch_bounds__(kDecThreads, LMC_Q8_DEC_MIN_BLOCKS)
     lmc_load_q8_kernel(const __grid_constant__ Plan P) {
-    copy_tiles<true, 2, kDecThreads, 1, 1>(P);
+    copy_tiles<true, 2, kDecThreads, LMC_Q8_COPY_UNROLL, LMC_Q8_COPY_UNROLL>(P);
 }
 
 // ---------------------------------------------------------------------------
@@ -622,6 +771,18 @@ __global__ void lmc_selftest_wait_kernel(uint32_t *status, uint32_t rounds) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (!mbar_wait(&bar, 0u, rounds))
         atomicOr(status, LMC_ST_TIMEOUT);
+}
+
+// Self-test of the codec's row scale: for each amax, the scale and inverse
+// the encoder uses, and the IEEE quotient amax / 127 beside them.
+__global__ void lmc_selftest_row_scale_kernel(const float *amax, float *scale, float *inv, float *ieee, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float a = amax[i];
+        const RowScale rs = row_scale(a);
+        scale[i] = rs.scale;
+        inv[i] = rs.inv;
+        ieee[i] = __fdiv_rn(a, 127.0f);
+    }
 }
 
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -790,7 +951,9 @@ int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_s
     const int64_t rows = spec.rec_bytes / (4 * row);
     if (rows > INT32_MAX || spec.conv_bytes > INT32_MAX)
         return LMC_ERR_INVALID_ARG;
-    const int32_t per_tile = (int32_t)std::max<int64_t>(1, kTileBytes / (4 * row));
+    // rows per tile: a multiple of 4, so every tile's codes and scales start
+    // on a 16-byte boundary
+    const int32_t per_tile = (int32_t)std::max<int64_t>(4, kQ8TileBytes / (4 * row) / 4 * 4);
     Entry &E = P.entries[ne++];
     E.pool_base = d.base;
     E.pool_stride = d.stride;
@@ -1119,6 +1282,22 @@ extern "C" int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size,
     }
     *out = total;
     return LMC_OK;
+}
+
+extern "C" int lmc_selftest_row_scale(const float *amax, float *scale, float *inv, float *ieee, int64_t n,
+                                      void *stream) {
+    if (n < 0 || (n > 0 && (amax == nullptr || scale == nullptr || inv == nullptr || ieee == nullptr)))
+        return LMC_ERR_INVALID_ARG;
+    if ((((uintptr_t)amax | (uintptr_t)scale | (uintptr_t)inv | (uintptr_t)ieee) & 3) != 0)
+        return LMC_ERR_ALIGN;
+    if (n == 0)
+        return LMC_OK;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return LMC_ERR_CUDA;
+    const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)sms * 8);
+    lmc_selftest_row_scale_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(amax, scale, inv, ieee, n);
+    return cudaGetLastError() == cudaSuccess ? LMC_OK : LMC_ERR_CUDA;
 }
 
 extern "C" int lmc_selftest_wait(uint32_t *status, int64_t rounds, void *stream) {

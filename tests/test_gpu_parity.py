@@ -569,14 +569,20 @@ def test_q8_tiny_workload_exact(lmc):
     _q8_exact(lmc, inp, Lp, 64, W.fill_normal_np(inp.layout.pool_bytes, 61))
 
 
-def test_q8_special_rows_exact(lmc):
+@pytest.mark.parametrize("d", [64, 128, 16, 4])
+def test_q8_special_rows_exact(lmc, d):
     """Rows that decide the corner cases: all zero, subnormal (the clamp
-    decides), ties at half steps, huge and tiny magnitudes."""
+    decides), exact ties at half steps, products within a few ulps of a half
+    step (the encoder must fall back to the IEEE quotient), huge and tiny
+    magnitudes; for the grouped (d = 16, 64, 128) and one-row-per-warp (d = 4)
+    encoders and both decoder paths."""
     inp, Lp = case_inputs(W.CONFIGS[0])
     Lo = inp.layout
     pool_h = W.fill_normal_np(Lo.pool_bytes, 62)
     rng = np.random.default_rng(9)
     f = pool_h[: (Lo.pool_bytes // 4) * 4].view(np.float32)
+    nrows = 64 * 64 // d  # one (64, 64) head of the tiny workload's state
+    half = np.float32(100) / np.float32(127)
     seen = set()  # layers of different groups share pages in this padded pool: edit each page once
     for i in range(len(Lo.kinds)):
         if Lo.kinds[i] != "KDA":
@@ -586,27 +592,40 @@ def test_q8_special_rows_exact(lmc):
             if lo in seen:
                 continue
             seen.add(lo)
-            rows = f[lo:lo + 256 * 64].reshape(256, 64)
+            rows = f[lo:lo + nrows * d].reshape(nrows, d)
             rows[0] = 0
             rows[1] = 0
             rows[1, :3] = np.array([190, -189, 37], dtype=np.float32) * np.float32(2.0 ** -149)
-            rows[2] = np.arange(64, dtype=np.float32) - np.float32(31.5)  # ties at scale 32/127...
+            rows[2] = np.arange(d, dtype=np.float32) - np.float32((d - 1) / 2)
             rows[3] = rows[3] * np.float32(1e30)  # large but finite (non-finite input is out of domain)
             rows[4] = rows[4] * np.float32(1e-35)
             rows[5, :] = np.float32(127)
             rows[5, 1::2] = np.float32(2.5)
-            rows[6] = rng.choice([-3.5, -2.5, -0.5, 0.5, 1.5, 2.5], 64).astype(np.float32)
+            rows[6] = rng.choice([-3.5, -2.5, -0.5, 0.5, 1.5, 2.5], d).astype(np.float32)
             rows[6, 0] = 127
-    _q8_exact(lmc, inp, Lp, 64, pool_h)
+            # scale 1: half steps moved by one ulp either way
+            k = rng.integers(-120, 120, d).astype(np.float32) + np.float32(0.5)
+            rows[7] = np.nextafter(k, k + rng.choice([-1, 1], d).astype(np.float32))
+            rows[7, 0] = 127
+            # scale 100/127: (k + 1/2) * scale, whose quotients land within a few ulps of k + 1/2
+            rows[8] = (rng.integers(-127, 126, d).astype(np.float32) + np.float32(0.5)) * half
+            rows[8, 0] = 100
+    _q8_exact(lmc, inp, Lp, d, pool_h)
 
 
-@pytest.mark.parametrize("d", [4, 16, 128])
-def test_q8_row_lengths_exact(lmc, d):
-    spec = [W.kda(48, 3, 2, 32), W.mla(32), W.kda(48, 3, 2, 32), W.mla(32)]
+@pytest.mark.parametrize("d,rows", [(4, 16), (16, 128), (128, 16), (4, 2400), (8, 1100), (12, 800),
+                                    (20, 68), (24, 340), (96, 68), (256, 36), (500, 24), (512, 20)])
+def test_q8_row_lengths_exact(lmc, d, rows):
+    """Row lengths of every encoder and decoder path (grouped: 8 .. 256;
+    one row per warp: 4, 12, 20, 24, 96, 500, 512; decoder one scale per
+    vector for powers of two >= 16, four otherwise), pages of one tile and of
+    several with a shorter last tile (4 x 2400, 8 x 1100, 12 x 800)."""
+    state = {"kind": "KDA", "token_bytes": 0, "conv_bytes": 48, "rec_bytes": 4 * d * rows, "window": 0}
+    spec = [state, W.mla(32), dict(state, conv_bytes=64), W.mla(32)]
     cfg = W.Config(400 + d, "q8", spec, N=8, requested_chunk=16, packed=bool(d % 8), num_requests=3,
                    lengths="fixed", fixed_lengths=(40, 77, 23), seed=d)
     inp, Lp = case_inputs(cfg)
-    _q8_exact(lmc, inp, Lp, d, W.fill_normal_np(inp.layout.pool_bytes, d))
+    _q8_exact(lmc, inp, Lp, d, W.fill_normal_np(inp.layout.pool_bytes, d + rows))
 
 
 def test_q8_full_size_kimi_linear(lmc):
@@ -650,6 +669,35 @@ def test_q8_full_size_kimi_linear(lmc):
     for pg in pages_d:
         lo, n = int(pg["pool_offset"]), int(pg["bytes"])
         assert np.array_equal(fresh[lo:lo + n].cpu().numpy(), back[lo:lo + n])
+
+
+def test_q8_row_scale_every_float(lmc):
+    """The encoder's row scale equals the IEEE quotient amax / 127 (CUDA's
+    division) bit for bit for every finite non-negative float, and its inverse
+    is within 3e-7 of 1 / scale wherever the encoder multiplies (so a product
+    x * inv stays within 127.01 * 3e-7 < 4e-5 of x / scale); a random sample
+    also matches numpy's binary32 division."""
+    top = 0x7F7FFFFF + 1  # bit patterns of 0 .. FLT_MAX
+    step = 1 << 27
+    rng = np.random.default_rng(127)
+    for lo in range(0, top, step):
+        hi = min(top, lo + step)
+        amax = torch.arange(lo, hi, dtype=torch.int64, device=DEV).to(torch.int32).view(torch.float32)
+        scale, inv, ieee = (torch.empty_like(amax) for _ in range(3))
+        lmc.lmc_selftest_row_scale(amax, scale, inv, ieee)
+        torch.cuda.synchronize()
+        same = scale.view(torch.int32) == ieee.view(torch.int32)
+        if not bool(same.all()):
+            bad = torch.nonzero(~same)[:4, 0] + lo
+            raise AssertionError(f"row scale differs from the IEEE quotient at bit patterns {bad.tolist()}")
+        mult = inv != 0
+        err = (inv[mult].double() * scale[mult].double() - 1.0).abs().max().item() if bool(mult.any()) else 0.0
+        assert err <= 3e-7, (lo, err)
+        divide = ~mult & (amax != 0)
+        assert bool(((amax[divide] < 2.0 ** -100) | (amax[divide] > 2.0 ** 125)).all())
+        pick = torch.from_numpy(rng.integers(0, hi - lo, 4096)).to(DEV)
+        a_h, s_h = amax[pick].cpu().numpy(), scale[pick].cpu().numpy()
+        assert np.array_equal(s_h.view(np.int32), (a_h / np.float32(127)).astype(np.float32).view(np.int32))
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(lmc):

@@ -251,6 +251,17 @@ def test_selftest_wait_host_checks(lmc):
     assert lmc._lib.lmc_selftest_wait((addr + 3) // 4 * 4 + 1, 10, None) == lmc.LMC_ERR_ALIGN
 
 
+def test_selftest_row_scale_host_checks(lmc):
+    buf = (ctypes.c_uint8 * 64)()
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    f = lmc._lib.lmc_selftest_row_scale
+    assert f(a, a + 16, a + 32, a + 48, -1, None) == lmc.LMC_ERR_INVALID_ARG
+    assert f(None, a + 16, a + 32, a + 48, 4, None) == lmc.LMC_ERR_INVALID_ARG
+    assert f(a, a + 16, None, a + 48, 4, None) == lmc.LMC_ERR_INVALID_ARG
+    assert f(a + 2, a + 16, a + 32, a + 48, 4, None) == lmc.LMC_ERR_ALIGN
+    assert f(a, a + 16, a + 32, a + 48, 0, None) == lmc.LMC_OK  # nothing to do: no launch
+
+
 def test_q8_refuses_unaligned_state_pages(lmc):
     """A KDA layer without a conv window whose pages sit at odd offsets (an
     odd-sized attention page pads the padded layout) cannot go through the
