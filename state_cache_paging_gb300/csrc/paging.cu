@@ -303,8 +303,8 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // lpr lanes, and each lane loads its vectors of the warp's next rows before it
 // quantises the current ones, so loads stay in flight during the arithmetic.
 // This needs d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two
-// <= 32 (d = 16 .. 512 in powers of two); other row lengths take one row per
-// warp. Decode is flat over the tile's codes: 16 codes (one 16-byte load) per
+// <= 32 (two float4 per lane: d = 8 .. 256 in powers of two); other row
+// lengths take one row per warp. Decode is flat over the tile's codes: 16 codes (one 16-byte load) per
 // thread per round, kDecUnroll rounds of loads issued before their stores,
 // values written as whole 32-byte sectors.
 // Codec kernel shapes picked by measurement on GB300 (Kimi-Linear, d = 128):
