@@ -264,6 +264,35 @@ def split_parts(jobs, object_bytes, parts):
     return out
 
 
+def touched_blocks(layout, tables, jobs, m):
+    """Block ids (over all KV groups) whose pages a set of chunk jobs reads or
+    writes: for job (request r, chunk c) and each layer of its object group,
+    positions c*m .. c*m+m-1 of a paged layer's KV group, or position
+    (c+1)*m-1 of a KDA layer's (the chunk-end snapshot)."""
+    out = []
+    for og, J in enumerate(jobs):
+        if len(J) == 0:
+            continue
+        r = J["request"].astype(np.int64)[:, None]
+        c = J["chunk"].astype(np.int64)[:, None]
+        groups = {(layout.kv_group[i], layout.kinds[i] == "KDA")
+                  for i in range(len(layout.kinds)) if layout.object_group[i] == og}
+        for k, kda in sorted(groups):
+            pos = (c + 1) * m - 1 if kda else c * m + np.arange(m)[None, :]
+            out.append(np.asarray(tables[k])[r, pos].ravel())
+    blocks = np.unique(np.concatenate(out)) if out else np.zeros(0, dtype=np.int32)
+    return blocks[blocks >= 0]
+
+
+def check_disjoint(layout, tables, load_jobs, store_jobs, m):
+    """The mixed step runs its load and its store concurrently on one pool:
+    refuses a batch in which they would touch a common block."""
+    common = np.intersect1d(touched_blocks(layout, tables, load_jobs, m),
+                            touched_blocks(layout, tables, store_jobs, m))
+    if common.size:
+        raise RuntimeError(f"mixed step: load and store share {common.size} block(s), e.g. {common[:4].tolist()}")
+
+
 class PagingStep:
     """Device inputs and one step of the hot path for a workload.
 
@@ -304,6 +333,7 @@ class PagingStep:
         self.status = T.zeros(1, dtype=T.int32, device=dev)
         self.t_src = [T.from_numpy(t).to(dev) for t in inp.tables_src]
         if cfg.mixed:
+            check_disjoint(L, inp.tables_src, inp.load_jobs, inp.store_jobs, C // cfg.N)
             sizes = inp.object_bytes
             self.load_payload = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.load_jobs))
             self.store_payload = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.store_jobs))

@@ -1,0 +1,75 @@
+"""The C ABI from C: a plain C11 client (tests/c_abi_client.c) compiled with
+gcc -std=c11 -pedantic against include/lmc.h and linked to liblmc.so runs the
+host-side calls (no GPU); its output matches the Python binding and the
+values the pages give."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import state_cache_paging_gb300 as lmc
+import workloads as W
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+@pytest.fixture(scope="module")
+def client_output(tmp_path_factory):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    out = tmp_path_factory.mktemp("cabi") / "client"
+    libdir = os.path.dirname(lmc._lib._name)
+    subprocess.run(["gcc", "-std=c11", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(HERE, "c_abi_client.c"), "-o", str(out), f"-L{libdir}", "-llmc",
+                    f"-Wl,-rpath,{libdir}"], check=True, capture_output=True, text=True)
+    r = subprocess.run([str(out)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = r.stdout.splitlines()
+    assert lines[-1] == "done"
+    return lines
+
+
+def _value(lines, key):
+    return next(l.split(" ", 1)[1] for l in lines if l.split(" ", 1)[0] == key)
+
+
+def test_host_rules_from_c(client_output):
+    L = client_output
+    # Kimi-Linear's N at TP 2 and TP 1 ("Kimi-Linear" recipe table and note)
+    assert int(_value(L, "unified_tp2")) == 944
+    assert int(_value(L, "unified_tp1")) == 1888
+    assert int(_value(L, "negotiate_100_64")) == 128
+    assert int(_value(L, "strict_100_64")) == lmc.LMC_ERR_NOT_MULTIPLE
+    assert int(_value(L, "negotiate_bad_n")) == lmc.LMC_ERR_INVALID_ARG
+    assert int(_value(L, "budget_944_1887")) == lmc.LMC_OK
+    assert int(_value(L, "budget_944_1888_joint")) == lmc.LMC_ERR_BUDGET
+    assert int(_value(L, "budget_944_1888_separate")) == lmc.LMC_OK
+    assert int(_value(L, "store_without_batch")) == lmc.LMC_ERR_INVALID_ARG
+    assert int(_value(L, "store_bad_chunk")) == lmc.LMC_ERR_NOT_MULTIPLE
+    assert _value(L, "strerror_budget") == lmc.lmc_strerror(lmc.LMC_ERR_BUDGET)
+
+
+def test_layout_from_c_matches_binding(client_output):
+    L = client_output
+    cfg = W.CONFIGS[1]
+    mem = 1056 * 6 * 2170880
+    P = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, mem)
+    assert int(_value(L, "num_kv_groups")) == P.num_kv_groups == 4
+    assert int(_value(L, "num_object_groups")) == P.num_object_groups == 2
+    assert int(_value(L, "num_slabs")) == P.num_slabs == 6
+    assert int(_value(L, "page_size")) == P.page_size == 2170880
+    assert int(_value(L, "num_blocks")) == P.num_blocks == 1056
+    assert int(_value(L, "pool_bytes")) == P.pool_bytes == mem
+    rows = [list(map(int, l.split()[1:])) for l in L if l.startswith("layer ")]
+    assert len(rows) == 24
+    for i, (idx, kind, kv, slot, og, real, page, base, stride) in enumerate(rows):
+        assert idx == i
+        assert lmc.LMC_LAYER_NAME[kind] == P.kinds[i]
+        assert (kv, slot, og, real, page, base, stride) == (P.kv_group[i], P.slot[i], P.object_group[i],
+                                                          P.real_bytes[i], P.page_bytes[i], P.base[i], P.stride[i])
+    sizes = {int(l.split()[1]): int(l.split()[2]) for l in L if l.startswith("object_bytes ")}
+    assert sizes == {g: P.object_bytes(944, g) for g in range(P.num_object_groups)}
+    assert sorted(sizes.values()) == [6 * 1087488, 18 * 2170880]
+    assert int(_value(L, "backends_stride_attention")) == P.check_backends(True, False)
