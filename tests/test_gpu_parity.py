@@ -628,6 +628,58 @@ def test_q8_row_lengths_exact(lmc, d, rows):
     _q8_exact(lmc, inp, Lp, d, W.fill_normal_np(inp.layout.pool_bytes, d + rows))
 
 
+def test_q8_error_paths_match_oracle(lmc):
+    """The codec kernels under the same faults as the plain copies (bad block
+    ids, a missing snapshot, bad jobs): same status bits, same record bytes
+    and same decoded pages as the oracle."""
+    inp, Lp = case_inputs(W.CONFIGS[0])
+    Lo, C, d = inp.layout, inp.C, 64
+    sizes = [Lo.object_bytes_q8(C, d, g) for g in range(Lo.num_object_groups)]
+    units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
+    jobs0, nbytes = W.pack_jobs(units, sizes)
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 5)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    kda_g = Lo.kv_group_kind.index("KDA")
+    mla_g = Lo.kv_group_kind.index("MLA")
+    og_kda = Lo.object_group[Lo.kinds.index("KDA")]
+    m = C // Lo.N
+    for what in ("oor", "snap", "mla", "req", "align", "end", "chunk"):
+        tabs = [t.copy() for t in inp.tables_src]
+        jobs = [j.copy() for j in jobs0]
+        if what == "oor":
+            tabs[kda_g][0, m - 1] = Lo.num_blocks + 3
+        elif what == "snap":
+            tabs[kda_g][1, 2 * m - 1] = -1
+        elif what == "mla":
+            tabs[mla_g][0, 1] = -1
+        elif what == "req":
+            jobs[og_kda][1]["request"] = 2
+        elif what == "align":
+            jobs[og_kda][0]["offset"] += 8
+        elif what == "end":
+            jobs[og_kda][2]["offset"] = nbytes - 16
+        elif what == "chunk":
+            jobs[og_kda][0]["chunk"] = 1000
+        arena = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device=DEV)
+        st = _status()
+        lmc.lmc_store_q8(Lp, C, d, pool, dev_tables(tabs, DEV), dev_jobs(jobs, DEV), arena, st)
+        torch.cuda.synchronize()
+        arena_o = np.full(nbytes, 0x5A, dtype=np.uint8)
+        st_o = oracle.store_q8(Lo, C, d, pool_h, tabs, jobs, arena_o)
+        assert st_o != 0, what
+        assert int(st.item()) == st_o, (what, int(st.item()), st_o)
+        assert np.array_equal(arena.cpu().numpy(), arena_o), what
+        fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+        st = _status()
+        lmc.lmc_load_q8(Lp, C, d, fresh, dev_tables(tabs, DEV), dev_jobs(jobs, DEV),
+                        torch.from_numpy(arena_o).to(DEV), st)
+        torch.cuda.synchronize()
+        fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        assert oracle.load_q8(Lo, C, d, fresh_o, tabs, jobs, arena_o) == st_o
+        assert int(st.item()) == st_o, what
+        assert np.array_equal(fresh.cpu().numpy(), fresh_o), what
+
+
 def test_q8_full_size_kimi_linear(lmc):
     """Kimi-Linear full size, d = 128: sampled records and decoded pages
     against the oracle; decoded values within half a step everywhere sampled."""
