@@ -188,6 +188,10 @@ __device__ __forceinline__ void st_stream32(u8x32 *p, const u8x32 &v) {
                  : "memory");
 }
 
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 // A resolved tile: copy `bytes` from src to dst.
 struct Span {
     const uint8_t *src;
@@ -300,18 +304,21 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // Encode work split: a row's d / 4 float4 vectors are spread over `lpr` lanes
 // of a warp, kRowVec consecutive vectors per lane, so 32 / lpr rows share a
 // warp; the row maximum is a shuffle reduction inside each aligned group of
-// lpr lanes, and each lane loads its vectors of the warp's next rows before it
-// quantises the current ones, so loads stay in flight during the arithmetic.
+// lpr lanes. Each thread stages its vectors of the next kQ8Stages - 1 rounds
+// in shared memory with asynchronous copies (cp.async: no registers held, and
+// each thread waits only on its own copy groups), so loads stay in flight
+// during the arithmetic.
 // This needs d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two
 // <= 32 (two float4 per lane: d = 8 .. 256 in powers of two); other row
 // lengths take one row per warp. Decode is flat over the tile's codes: 16 codes (one 16-byte load) per
 // thread per round, kDecUnroll rounds of loads issued before their stores,
 // values written as whole 32-byte sectors.
 // Codec kernel shapes picked by measurement on GB300 (Kimi-Linear, d = 128):
-// the encoder is bound by the latency of its per-row chain (loads, maximum,
-// scale, codes), so it wants the most resident warps (128 x 12: 6.73 TB/s;
-// 128 x 10: 6.64; 128 x 9: 6.32; 4 float4 per lane at 128 x 8: 6.65); the
-// decoder runs at 256 x 6 with two rounds in flight (7.02 TB/s).
+// encoder 128 threads x 10 CTAs, four stages (three rounds ahead, 16 KB of
+// shared memory per CTA): 7.10 TB/s (3 stages 7.00, 5 stages 7.03, 11 CTAs
+// 6.94, 9 CTAs 6.99; 256-thread CTAs 5.9 since a 64-row tile then runs only
+// two rounds; the next round prefetched in registers instead: 6.70 at
+// 128 x 12); decoder 256 x 6 with two rounds in flight (7.02 TB/s).
 #ifndef LMC_ROW_VEC
 #define LMC_ROW_VEC 2
 #endif
@@ -319,7 +326,7 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 #define LMC_Q8_ENC_THREADS 128
 #endif
 #ifndef LMC_Q8_ENC_MIN_BLOCKS
-#define LMC_Q8_ENC_MIN_BLOCKS 12
+#define LMC_Q8_ENC_MIN_BLOCKS 10
 #endif
 #ifndef LMC_Q8_DEC_THREADS
 #define LMC_Q8_DEC_THREADS 256
@@ -333,12 +340,17 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 #ifndef LMC_Q8_COPY_UNROLL
 #define LMC_Q8_COPY_UNROLL 1  // vectors per thread per round on the codec kernels' plain pages
 #endif
+#ifndef LMC_Q8_STAGES
+#define LMC_Q8_STAGES 4  // encoder: rounds staged in shared memory (kQ8Stages - 1 ahead)
+#endif
 #ifndef LMC_Q8_TILE_BYTES
 #define LMC_Q8_TILE_BYTES 32768  // fp32 state bytes per codec tile
 #endif
 constexpr int kRowVec = LMC_ROW_VEC;
 constexpr int kQ8TileBytes = LMC_Q8_TILE_BYTES;
 constexpr int kDecUnroll = LMC_Q8_DEC_UNROLL;
+constexpr int kQ8Stages = LMC_Q8_STAGES;
+static_assert(kQ8Stages >= 2, "the staged encoder needs at least two stages");
 
 // Rounding by addition: for |y| <= 2^22, RN(y + 1.5 * 2^23) equals
 // 1.5 * 2^23 + rint(y) (ties to even: the floats of [2^23, 2^24) are the
@@ -477,12 +489,43 @@ __device__ __forceinline__ bool grouped_rows(int d, int &lpr) {
     return lpr <= 32 && (lpr & (lpr - 1)) == 0;
 }
 
-// A lane's kRowVec consecutive float4 of one row (16-byte loads: measured
-// as fast as 32-byte ones here, with fewer registers).
-__device__ __forceinline__ void load_lane(float4 (&v)[kRowVec], const float4 *p) {
+// One round of the grouped encoder: the lane's vectors v of row r (live:
+// r is a row of the tile) -> the row's scale (first lane of the group) and
+// the lane's codes.
+__device__ __forceinline__ void encode_round(const Span &s, int d, int lpr, int l, int r, bool live,
+                                             const float4 (&v)[kRowVec]) {
+    float amax = 0.0f;
+    if (live) {
 #pragma unroll
-    for (int w = 0; w < kRowVec; w++)
-        v[w] = ld_stream_f4(p + w);
+        for (int w = 0; w < kRowVec; w++)
+            amax = fmaxf(amax, absmax4(v[w]));
+    }
+    amax = group_max(amax, lpr);
+    if (live) {
+        const RowScale rs = row_scale(amax);
+        if (l == 0)
+            reinterpret_cast<float *>(s.scales)[r] = rs.scale;
+        uint32_t q[kRowVec];
+        quant_lane(v, rs, q);
+        uint32_t *out = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d) + l * kRowVec;
+        if (kRowVec == 4)
+            *reinterpret_cast<uint4 *>(out) = make_uint4(q[0], q[1], q[2 % kRowVec], q[3 % kRowVec]);
+        else if (kRowVec == 2)
+            *reinterpret_cast<uint2 *>(out) = make_uint2(q[0], q[1 % kRowVec]);
+        else
+#pragma unroll
+            for (int w = 0; w < kRowVec; w++)
+                out[w] = q[w];
+    }
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
 template <int kNT>
@@ -490,46 +533,41 @@ __device__ __forceinline__ void encode_grouped(const Span &s, int d, int lpr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int kWarps = kNT / 32;
     const int nvec = d >> 2;
-    float *scales = reinterpret_cast<float *>(s.scales);
     const int per_warp = 32 / lpr, sub = lane / lpr, l = lane % lpr;
     const int step = kWarps * per_warp;
     const float4 *src = reinterpret_cast<const float4 *>(s.src) + l * kRowVec;
-    float4 next[kRowVec];
-    int r = warp * per_warp + sub;
-    if (r < s.bytes)
-        load_lane(next, src + (int64_t)r * nvec);
-    for (int base = warp * per_warp; base < s.bytes; base += step, r += step) {
+    const int r0 = warp * per_warp + sub;
+    // each thread stages its own vectors of the next kQ8Stages - 1 rounds in
+    // shared memory with asynchronous copies (no registers held, no other
+    // thread involved), waiting only on its own copy groups
+    __shared__ __align__(16) float4 stage[kQ8Stages][kNT][kRowVec];
+    const int rounds = (s.bytes - warp * per_warp + step - 1) / step;  // rounds this warp runs
+    auto issue = [&](int k) {
+        const int rr = r0 + k * step;
+        if (k < rounds && rr < s.bytes) {
+#pragma unroll
+            for (int w = 0; w < kRowVec; w++)
+                cp_async16(&stage[k % kQ8Stages][threadIdx.x][w], src + (int64_t)rr * nvec + w);
+        }
+        cp_async_commit();  // one group per round, empty or not
+    };
+#pragma unroll
+    for (int k = 0; k < kQ8Stages - 1; k++)
+        issue(k);
+    for (int k = 0; k < rounds; k++) {
+        issue(k + kQ8Stages - 1);
+        cp_async_wait<kQ8Stages - 1>();  // round k's group has landed
+        const int r = r0 + k * step;
         const bool live = r < s.bytes;
         float4 v[kRowVec];
-#pragma unroll
-        for (int w = 0; w < kRowVec; w++)
-            v[w] = next[w];
-        if (r + step < s.bytes)  // the next rows' loads stay in flight during this round
-            load_lane(next, src + (int64_t)(r + step) * nvec);
-        float amax = 0.0f;
         if (live) {
 #pragma unroll
             for (int w = 0; w < kRowVec; w++)
-                amax = fmaxf(amax, absmax4(v[w]));
+                v[w] = stage[k % kQ8Stages][threadIdx.x][w];
         }
-        amax = group_max(amax, lpr);
-        if (live) {
-            const RowScale rs = row_scale(amax);
-            if (l == 0)
-                scales[r] = rs.scale;
-            uint32_t q[kRowVec];
-            quant_lane(v, rs, q);
-            uint32_t *out = reinterpret_cast<uint32_t *>(s.dst + (int64_t)r * d) + l * kRowVec;
-            if (kRowVec == 4)
-                *reinterpret_cast<uint4 *>(out) = make_uint4(q[0], q[1], q[2 % kRowVec], q[3 % kRowVec]);
-            else if (kRowVec == 2)
-                *reinterpret_cast<uint2 *>(out) = make_uint2(q[0], q[1 % kRowVec]);
-            else
-#pragma unroll
-                for (int w = 0; w < kRowVec; w++)
-                    out[w] = q[w];
-        }
+        encode_round(s, d, lpr, l, r, live, v);
     }
+    cp_async_wait<0>();  // the stages are free for the next tile
 }
 
 // s.bytes rows of d values at s.src -> codes at s.dst, scales at s.scales.
@@ -727,10 +765,6 @@ __global__ void __launch_bounds__(kDecThreads, LMC_Q8_DEC_MIN_BLOCKS)
 // LMC_ST_TIMEOUT, drains its own copies (bounded) and returns.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds (each may suspend)
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
@@ -1097,6 +1131,10 @@ int launch_plan(const Plan &P, bool vec, void *stream) {
         // one CTA per tile, capped; the kernel strides over the rest
         const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * 2048);
         if (P.q8_row > 0) {
+            if (P.mode == kStore &&
+                cudaFuncSetAttribute(lmc_store_q8_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                return LMC_ERR_CUDA;  // the staged encoder wants shared memory rather than L1 (its loads bypass L1)
             if (P.mode == kStore)
                 lmc_store_q8_kernel<<<grid, kEncThreads, 0, s>>>(P);
             else
