@@ -300,6 +300,7 @@ def _batch(layout: Layout, tables, jobs):
     nreq = int(tables[0].shape[0]) if g else 0
     tarr = (lmc_block_table * max(g, 1))()
     for k, t in enumerate(tables):
+        _visible("block table", t)
         if t.dim() != 2 or t.element_size() != 4 or t.stride(1) != 1 or int(t.shape[0]) != nreq:
             raise LmcError(LMC_ERR_INVALID_ARG, "block tables must be int32 [num_requests, cols] with unit column stride")
         tarr[k] = lmc_block_table(t.data_ptr(), int(t.stride(0)), int(t.shape[1]))
@@ -309,6 +310,7 @@ def _batch(layout: Layout, tables, jobs):
     jarr = (ctypes.c_void_p * max(o, 1))()
     narr = (_i64 * max(o, 1))()
     for q, j in enumerate(jobs):
+        _visible("job array", j)
         nbytes = j.numel() * j.element_size()
         if nbytes % 16 or not j.is_contiguous():
             raise LmcError(LMC_ERR_INVALID_ARG, "job arrays hold contiguous 16-byte lmc_job records")
@@ -325,7 +327,17 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check_pool(layout: Layout, pool):
+def _visible(name: str, t) -> None:
+    """Refuses memory the kernels could not address: every buffer handed to a
+    launch must be a CUDA tensor or pinned (page-locked) host memory."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise LmcError(LMC_ERR_INVALID_ARG, f"{name} must be a CUDA tensor or pinned host memory")
+
+
+def _check_launch(layout: Layout, pool, arena, status):
+    for name, t in (("pool", pool), ("arena", arena), ("status", status)):
+        if t is not None:
+            _visible(name, t)
     if pool.numel() * pool.element_size() < layout.pool_bytes:
         raise LmcError(LMC_ERR_INVALID_ARG, f"pool holds {pool.numel() * pool.element_size()} bytes, "
                                             f"the layout addresses {layout.pool_bytes}")
@@ -335,7 +347,7 @@ def lmc_store(layout: Layout, chunk: int, pool, tables, jobs, arena, status, str
     """Gathers the jobs' objects from `pool` into `arena` (device tensors) on
     `stream` (default: torch's current stream). Device errors are OR-ed into
     the 4-byte `status` tensor."""
-    _check_pool(layout, pool)
+    _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
     _check(_lib.lmc_store(layout.handle, int(chunk), pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
                           arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
@@ -344,7 +356,7 @@ def lmc_store(layout: Layout, chunk: int, pool, tables, jobs, arena, status, str
 
 def lmc_load(layout: Layout, chunk: int, pool, tables, jobs, arena, status, stream=None) -> None:
     """Scatters the jobs' objects from `arena` into `pool` (device tensors)."""
-    _check_pool(layout, pool)
+    _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
     _check(_lib.lmc_load(layout.handle, int(chunk), pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
                          arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
@@ -354,7 +366,7 @@ def lmc_load(layout: Layout, chunk: int, pool, tables, jobs, arena, status, stre
 def lmc_store_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool, tables, jobs, arena, status,
                      stream=None) -> None:
     """Block-granular store: each job's `chunk` field is its first block position."""
-    _check_pool(layout, pool)
+    _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
     _check(_lib.lmc_store_blocks(layout.handle, int(blocks_per_object), int(kda_mode), pool.data_ptr(),
                                  ctypes.byref(b), arena.data_ptr(), arena.numel() * arena.element_size(),
@@ -363,7 +375,7 @@ def lmc_store_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool
 
 def lmc_load_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool, tables, jobs, arena, status,
                     stream=None) -> None:
-    _check_pool(layout, pool)
+    _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
     _check(_lib.lmc_load_blocks(layout.handle, int(blocks_per_object), int(kda_mode), pool.data_ptr(),
                                 ctypes.byref(b), arena.data_ptr(), arena.numel() * arena.element_size(),
@@ -380,7 +392,7 @@ def lmc_object_bytes_q8(layout: Layout, chunk: int, row_elems: int, object_group
 def lmc_store_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, arena, status,
                  stream=None) -> None:
     """Chunk store with KDA snapshots as INT8 records (rows of `row_elems`)."""
-    _check_pool(layout, pool)
+    _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
     _check(_lib.lmc_store_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
                              arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
@@ -389,7 +401,7 @@ def lmc_store_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs,
 
 def lmc_load_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, arena, status,
                 stream=None) -> None:
-    _check_pool(layout, pool)
+    _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
     _check(_lib.lmc_load_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
                             arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
@@ -422,13 +434,14 @@ def pairs_to_device(pairs: np.ndarray, device):
 def lmc_copy_blocks(layout: Layout, pool, pairs, status, stream=None) -> None:
     """In-pool copies: `pairs[g]` (device tensor of 8-byte lmc_block_pair
     records) lists (src, dst) blocks of KV group g."""
-    _check_pool(layout, pool)
+    _check_launch(layout, pool, None, status)
     g = layout.num_kv_groups
     if len(pairs) != g:
         raise LmcError(LMC_ERR_INVALID_ARG, f"{g} pair arrays expected, got {len(pairs)}")
     parr = (ctypes.c_void_p * max(g, 1))()
     narr = (_i64 * max(g, 1))()
     for k, p in enumerate(pairs):
+        _visible("pair array", p)
         nbytes = p.numel() * p.element_size()
         if nbytes % 8 or not p.is_contiguous():
             raise LmcError(LMC_ERR_INVALID_ARG, "pair arrays hold contiguous 8-byte lmc_block_pair records")

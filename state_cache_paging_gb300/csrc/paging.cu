@@ -1,5 +1,6 @@
 // paging.cu -- store (gather pages -> chunk objects), load (scatter chunk
-// objects -> pages) and in-pool block copies for sm_103a.
+// objects -> pages), their INT8-codec forms for the KDA recurrent state, and
+// in-pool block copies, for sm_103a.
 //
 // What is moved ("Hybrid Attention Models" (LMCache docs), Object-group
 // separation; "Kimi-Linear" (LMCache recipe), Why these settings; "How vLLM
@@ -19,8 +20,9 @@
 // in kernel parameter space, reads one block id (or one block pair) from the
 // caller's device arrays, and copies one contiguous range: 32-byte (or, for
 // ranges that are only 16-byte aligned, 16-byte) vector loads that bypass L1
-// and streaming (evict-first) stores, several in flight per thread. One CTA per tile, several CTAs resident per SM, so the dependent
-// block-table read of one CTA hides under the copies of others.
+// and streaming (evict-first) stores, several in flight per thread. One CTA
+// per tile, several CTAs resident per SM, so the dependent block-table read
+// of one CTA hides under the copies of others.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -310,9 +312,9 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // during the arithmetic.
 // This needs d % (4 * kRowVec) == 0 and lpr = d / (4 * kRowVec) a power of two
 // <= 32 (two float4 per lane: d = 8 .. 256 in powers of two); other row
-// lengths take one row per warp. Decode is flat over the tile's codes: 16 codes (one 16-byte load) per
-// thread per round, kDecUnroll rounds of loads issued before their stores,
-// values written as whole 32-byte sectors.
+// lengths take one row per warp. Decode is flat over the tile's codes: 16
+// codes (one 16-byte load) per thread per round, kDecUnroll rounds of loads
+// issued before their stores, values written as whole 32-byte sectors.
 // Codec kernel shapes picked by measurement on GB300 (Kimi-Linear, d = 128):
 // encoder 128 threads x 10 CTAs, four stages (three rounds ahead, 16 KB of
 // shared memory per CTA): 7.10 TB/s (3 stages 7.00, 5 stages 7.03, 11 CTAs

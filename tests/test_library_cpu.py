@@ -293,3 +293,25 @@ def test_store_refuses_layouts_past_the_launch_limits(lmc):
     counts = (ctypes.c_int64 * o)(*[0] * o)
     b = lmc.lmc_batch(1, g, tables, o, 0, jobs, counts)
     assert lmc._lib.lmc_store(L.handle, 4, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+
+
+def test_binding_refuses_memory_the_kernels_cannot_address(lmc):
+    """Pageable host tensors are refused with INVALID_ARG before any launch:
+    the kernels address device memory or pinned host memory only."""
+    import torch
+    cfg = W.CONFIGS[0]
+    C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
+    L = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, 1 << 24)
+    pool = torch.zeros(L.pool_bytes, dtype=torch.uint8)
+    arena = torch.zeros(1024, dtype=torch.uint8)
+    status = torch.zeros(1, dtype=torch.int32)
+    tables = [torch.zeros((1, 8), dtype=torch.int32) for _ in range(L.num_kv_groups)]
+    jobs = [torch.zeros(0, dtype=torch.uint8) for _ in range(L.num_object_groups)]
+    for call in (lambda: lmc.lmc_store(L, C, pool, tables, jobs, arena, status),
+                 lambda: lmc.lmc_load(L, C, pool, tables, jobs, arena, status),
+                 lambda: lmc.lmc_store_q8(L, C, 64, pool, tables, jobs, arena, status),
+                 lambda: lmc.lmc_copy_blocks(L, pool, [torch.zeros(0, dtype=torch.uint8)] * L.num_kv_groups,
+                                             status)):
+        with pytest.raises(lmc.LmcError, match="CUDA tensor or pinned host memory") as e:
+            call()
+        assert e.value.code == lmc.LMC_ERR_INVALID_ARG
