@@ -114,6 +114,53 @@ def test_large_pages_exact(lmc):
     _full_exact(lmc, inp, Lp)
 
 
+@pytest.mark.parametrize("packed", [False, True])
+def test_step_boundary_snapshots_exact(lmc, packed):
+    """The >= 2N scheduler regime ("Kimi-Linear" recipe, Why these settings:
+    a step spans several blocks and only its last block gets a KDA
+    snapshot): with C = N and steps of 3 blocks, the KDA tables hold states
+    only at positions 3k + 2. With separate object groups the caller stores
+    every chunk's MLA object and only the step-end chunks' KDA objects: exact
+    against the oracle. A KDA object asked for at a chunk inside a step finds
+    no snapshot: NO_SNAPSHOT, its pages skipped, the same as the oracle."""
+    spec = [W.kda(48, 3, 2, 32), W.kda(48, 3, 2, 32), W.kda(48, 3, 2, 32), W.mla(64)]
+    cfg = W.Config(230 + int(packed), "steps", spec, N=16, requested_chunk=16, packed=packed, num_requests=3,
+                   lengths="fixed", fixed_lengths=(150, 97, 200), seed=23)
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    assert C == cfg.N
+    kda_groups = [k for k, kind in enumerate(Lo.kv_group_kind) if kind == "KDA"]
+    for tables in (inp.tables_src, inp.tables_dst):
+        for k in kda_groups:
+            t = tables[k]
+            cols = np.arange(t.shape[1])
+            t[:, (cols + 1) % 3 != 0] = -1  # states only where a step of 3 blocks ended
+    og_kda = Lo.object_group[Lo.kinds.index("KDA")]
+    step_end = (inp.jobs[og_kda]["chunk"] + 1) % 3 == 0
+    inside = inp.jobs[og_kda][~step_end][:1].copy()
+    units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
+    units[og_kda] = [(int(j["request"]), int(j["chunk"])) for j in inp.jobs[og_kda][step_end]]
+    assert units[og_kda] and inside.size
+    inp.jobs, inp.arena_bytes = W.pack_jobs(units, inp.object_bytes)
+    _full_exact(lmc, inp, Lp)
+    # one KDA object inside a step: no snapshot there
+    jobs = [J.copy() for J in inp.jobs]
+    inside["offset"] = inp.arena_bytes
+    jobs[og_kda] = np.concatenate([jobs[og_kda], inside])
+    nbytes = inp.arena_bytes + inp.object_bytes[og_kda]
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 29)
+    arena = torch.full((nbytes,), 0x3C, dtype=torch.uint8, device=DEV)
+    st = _status()
+    lmc.lmc_store(Lp, C, torch.from_numpy(pool_h).to(DEV), dev_tables(inp.tables_src, DEV), dev_jobs(jobs, DEV),
+                  arena, st)
+    torch.cuda.synchronize()
+    arena_o = np.full(nbytes, 0x3C, dtype=np.uint8)
+    st_o = oracle.store(Lo, C, pool_h, inp.tables_src, jobs, arena_o)
+    assert st_o == lmc.LMC_ST_NO_SNAPSHOT
+    assert int(st.item()) == st_o
+    assert np.array_equal(arena.cpu().numpy(), arena_o)
+
+
 def test_error_paths_match_oracle(lmc):
     """Bad block ids and bad jobs: same status bits and same arena bytes as
     the oracle (the offending page or object is skipped)."""
