@@ -417,7 +417,7 @@ class PagingStep:
         self.main.wait_event(ja)
         self.main.wait_event(jb)
 
-    def setup_e2e(self, parts: int = 16):
+    def setup_e2e(self, parts: int = 64):
         """Pinned host buffers for the end-to-end step: block tables and jobs
         go host -> device each step; objects leave the device for the host
         cache tier (store) and come back from it (load). Plain workloads are
@@ -625,7 +625,10 @@ def run_gpu(args):
     load_ms = [e[2].elapsed_time(e[3]) for e in evs]
     assert int(S.status.item()) == 0
 
-    S.setup_e2e()
+    if args.op == "copy":
+        S.setup_e2e()
+    else:
+        S.setup_e2e(args.e2e_parts)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     for _ in range(2):
         S.e2e_step()
@@ -682,7 +685,8 @@ def run_gpu(args):
                      "traffic": _traffic(dominant, cfg.index, args.op) if args.requests is None else None,
                      "algorithmic_bytes_per_launch": dom_bytes},
         "e2e": {"value": round(S.bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h},
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h,
+                "parts": None if args.op == "copy" else args.e2e_parts},
         "gpu_launches": S.launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -704,6 +708,8 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--requests", type=int, default=None, help="use only the first R requests")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-parts", type=int, default=64,
+                    help="ranges of (request, chunk) units the end-to-end step is pipelined over")
     ap.add_argument("--impl", choices=["lmc", "reference"], default="lmc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["paging", "blocks", "copy", "q8"], default="paging",
