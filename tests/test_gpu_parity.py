@@ -850,6 +850,11 @@ class _MappedHost:
         self.h, self.d, self.n = h.value, d.value, nbytes
         self.host = np.ctypeslib.as_array((ctypes.c_uint8 * nbytes).from_address(self.h))
 
+    is_cuda = False
+
+    def is_pinned(self):
+        return True  # page-locked and mapped: the kernels address it directly
+
     def data_ptr(self):
         return self.d
 
