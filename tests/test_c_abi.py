@@ -73,3 +73,69 @@ def test_layout_from_c_matches_binding(client_output):
     assert sizes == {g: P.object_bytes(944, g) for g in range(P.num_object_groups)}
     assert sorted(sizes.values()) == [6 * 1087488, 18 * 2170880]
     assert int(_value(L, "backends_stride_attention")) == P.check_backends(True, False)
+
+
+def _cuda_home():
+    for d in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if d and os.path.exists(os.path.join(d, "include", "cuda_runtime.h")):
+            return d
+    return None
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg_index,ids", [(0, None), (2, [0])])
+def test_store_load_from_c_match_oracle(tmp_path, cfg_index, ids):
+    """A C11 program (tests/c_abi_gpu_client.c) allocates device memory with
+    the CUDA runtime's C API and calls lmc_store / lmc_load through the C ABI
+    alone; its arena and reloaded pool equal the oracle's byte for byte."""
+    import numpy as np
+
+    import oracle
+    cuda = _cuda_home()
+    if shutil.which("gcc") is None or cuda is None:
+        pytest.skip("gcc or the CUDA toolkit headers not available")
+    exe = tmp_path / "gpu_client"
+    libdir = os.path.dirname(lmc._lib._name)
+    subprocess.run(["gcc", "-std=c11", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(cuda, "include"), os.path.join(HERE, "c_abi_gpu_client.c"), "-o", str(exe),
+                    f"-L{libdir}", "-llmc", f"-L{os.path.join(cuda, 'lib64')}", "-lcudart",
+                    f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}"],
+                   check=True, capture_output=True, text=True)
+    import functools
+    cfg = W.CONFIGS[cfg_index]
+    C = oracle.negotiate_chunk(cfg.requested_chunk, cfg.N)
+    inp = W.make_inputs(cfg, functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed), C, ids)
+    Lo = inp.layout
+    cols = max(t.shape[1] for t in inp.tables_src + inp.tables_dst)
+
+    def widen(t):
+        out = np.full((t.shape[0], cols), -1, dtype=np.int32)
+        out[:, :t.shape[1]] = t
+        return out
+
+    d = tmp_path
+    with open(d / "case.txt", "w") as f:
+        f.write(f"{cfg.N} {int(cfg.packed)} {Lo.pool_bytes} {C} {len(inp.lengths)} {cols} {len(cfg.layers)} "
+                f"{Lo.num_kv_groups} {Lo.num_object_groups}\n")
+        for l in cfg.layers:
+            f.write(f"{lmc.LMC_LAYER[l['kind']]} {int(l.get('token_bytes', 0))} {int(l.get('conv_bytes', 0))} "
+                    f"{int(l.get('rec_bytes', 0))} {int(l.get('window', 0))}\n")
+        for J in inp.jobs:
+            f.write(f"{len(J)}\n")
+        f.write(f"{inp.arena_bytes}\n")
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 71 + cfg_index)
+    pool_h.tofile(d / "pool.bin")
+    for k in range(Lo.num_kv_groups):
+        widen(inp.tables_src[k]).tofile(d / f"src_{k}.bin")
+        widen(inp.tables_dst[k]).tofile(d / f"dst_{k}.bin")
+    for g, J in enumerate(inp.jobs):
+        np.ascontiguousarray(J, dtype=oracle.JOB_DTYPE).tofile(d / f"jobs_{g}.bin")
+    r = subprocess.run([str(exe), str(d)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip() == "done", r.stdout + r.stderr
+    assert int((d / "status.out").read_text()) == 0
+    arena_o = np.full(inp.arena_bytes, 0x3C, dtype=np.uint8)
+    assert oracle.store(Lo, C, pool_h, inp.tables_src, inp.jobs, arena_o) == 0
+    fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    assert oracle.load(Lo, C, fresh_o, inp.tables_dst, inp.jobs, arena_o) == 0
+    assert np.array_equal(np.fromfile(d / "arena.out", dtype=np.uint8), arena_o)
+    assert np.array_equal(np.fromfile(d / "fresh.out", dtype=np.uint8), fresh_o)
