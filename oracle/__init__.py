@@ -116,6 +116,7 @@ class _Page(ctypes.Structure):
 
 PAGE_DTYPE = np.dtype([("pool_offset", "<i8"), ("object_offset", "<i8"), ("bytes", "<i8"),
                        ("layer", "<i4"), ("block", "<i4")])
+assert PAGE_DTYPE.itemsize == ctypes.sizeof(_Page)  # the C oracle fills or_page records in place
 
 
 class _PageList(ctypes.Structure):
