@@ -168,6 +168,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                        P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
     lib.or_object_bytes_q8.argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
     lib.or_object_bytes_q8.restype = ctypes.c_int64
+    for name in ("or_store_blocks_q8", "or_load_blocks_q8"):
+        getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                       P(_Tables), P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
+    lib.or_object_bytes_blocks_q8.argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int]
+    lib.or_object_bytes_blocks_q8.restype = ctypes.c_int64
     lib.or_unified_block_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P(ctypes.c_int64)]
     return lib
 
@@ -254,6 +259,10 @@ class Layout:
 
     def object_bytes_blocks(self, nb: int, kda_every: bool, og: int) -> int:
         return int(self._lib.or_object_bytes_blocks(ctypes.byref(self._c), int(nb), int(bool(kda_every)), int(og)))
+
+    def object_bytes_blocks_q8(self, nb: int, kda_every: bool, d: int, og: int) -> int:
+        return int(self._lib.or_object_bytes_blocks_q8(ctypes.byref(self._c), int(nb), int(bool(kda_every)), int(d),
+                                                       int(og)))
 
 
 def _fill_layout(spec_layers, N, packed, mem_bytes, split_groups, separate_object_groups) -> _Layout:
@@ -408,6 +417,34 @@ def load_q8(L: Layout, C: int, d: int, pool: np.ndarray, tables, jobs, arena: np
                            ctypes.byref(J), arena.ctypes.data, arena.size, ctypes.byref(st))
     if rc != OK:
         raise OracleError(rc, "load_q8")
+    return st.value
+
+
+def store_blocks_q8(L: Layout, nb: int, kda_every: bool, d: int, pool: np.ndarray, tables, jobs,
+                    arena: np.ndarray) -> int:
+    """Block-granular store with INT8 records for every stored KDA snapshot.
+    Returns the status bits."""
+    assert pool.dtype == np.uint8 and arena.dtype == np.uint8 and arena.flags.writeable
+    T, J, keep = _marshal(L, tables, jobs)
+    st = ctypes.c_uint32(0)
+    rc = L._lib.or_store_blocks_q8(ctypes.byref(L._c), int(nb), int(bool(kda_every)), int(d), pool.ctypes.data,
+                                   ctypes.byref(T), ctypes.byref(J), arena.ctypes.data, arena.size,
+                                   ctypes.byref(st))
+    if rc != OK:
+        raise OracleError(rc, "store_blocks_q8")
+    return st.value
+
+
+def load_blocks_q8(L: Layout, nb: int, kda_every: bool, d: int, pool: np.ndarray, tables, jobs,
+                   arena: np.ndarray) -> int:
+    assert pool.dtype == np.uint8 and arena.dtype == np.uint8 and pool.flags.writeable
+    T, J, keep = _marshal(L, tables, jobs)
+    st = ctypes.c_uint32(0)
+    rc = L._lib.or_load_blocks_q8(ctypes.byref(L._c), int(nb), int(bool(kda_every)), int(d), pool.ctypes.data,
+                                  ctypes.byref(T), ctypes.byref(J), arena.ctypes.data, arena.size,
+                                  ctypes.byref(st))
+    if rc != OK:
+        raise OracleError(rc, "load_blocks_q8")
     return st.value
 
 

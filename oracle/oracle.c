@@ -590,11 +590,15 @@ static int move_objects(const or_layout *L, const obj_shape *sh, uint8_t *pool,
                         int64_t pos = first + s;
                         if (pos >= T->num_cols[k])
                             *status |= OR_ST_BAD_JOB;
+                        else if (sh->q8_row > 0)
+                            *status |= q8_page(L, i, row[pos], pool, obj + cursor, to_object,
+                                               sh->q8_row, list, job->offset + cursor);
                         else
                             *status |= copy_page(L, i, row[pos], pool, obj + cursor,
                                                  to_object, OR_ST_NO_SNAPSHOT, list,
                                                  job->offset + cursor);
-                        cursor += L->real_bytes[i];
+                        cursor += sh->q8_row > 0 ? q8_record_bytes(&L->layers[i], sh->q8_row)
+                                                 : L->real_bytes[i];
                     }
                 } else {
                     /* The object's tokens are its nb consecutive blocks. */
@@ -762,6 +766,50 @@ int64_t or_object_bytes_q8(const or_layout *L, int64_t C, int64_t d, int og)
     if (q8_check(L, d) != OR_OK || C <= 0 || C % L->N != 0)
         return -1;
     return object_bytes_q(L, C / L->N, 0, d, og);
+}
+
+/* Block-granular store/load with every KDA snapshot (the last block's, or
+ * one per block with kda_every) held as its INT8 record: the checkpoints of
+ * [MC] "Compressed Checkpoint Storage" taken at block boundaries ([KL]). */
+int or_store_blocks_q8(const or_layout *L, int64_t nb, int kda_every, int64_t d, const uint8_t *pool,
+                       const or_tables *T, const or_jobs *J,
+                       uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    obj_shape sh;
+    int rc = block_shape(nb, kda_every, &sh);
+    if (rc == OR_OK)
+        rc = q8_check(L, d);
+    if (rc != OR_OK)
+        return rc;
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    sh.q8_row = d;
+    return move_objects(L, &sh, (uint8_t *)pool, T, J, arena, arena_bytes, status, 1, NULL);
+}
+
+int or_load_blocks_q8(const or_layout *L, int64_t nb, int kda_every, int64_t d, uint8_t *pool,
+                      const or_tables *T, const or_jobs *J,
+                      const uint8_t *arena, int64_t arena_bytes, uint32_t *status)
+{
+    obj_shape sh;
+    int rc = block_shape(nb, kda_every, &sh);
+    if (rc == OR_OK)
+        rc = q8_check(L, d);
+    if (rc != OR_OK)
+        return rc;
+    if (arena == NULL)
+        return OR_ERR_INVALID_ARG;
+    sh.q8_row = d;
+    return move_objects(L, &sh, pool, T, J, (uint8_t *)arena, arena_bytes, status, 0, NULL);
+}
+
+/* Bytes of one block-granular object of group og with INT8 KDA records, or
+ * -1 when nb, kda_every or d is not accepted. */
+int64_t or_object_bytes_blocks_q8(const or_layout *L, int64_t nb, int kda_every, int64_t d, int og)
+{
+    if (q8_check(L, d) != OR_OK || nb <= 0 || (kda_every != 0 && kda_every != 1))
+        return -1;
+    return object_bytes_q(L, nb, kda_every, d, og);
 }
 
 /* In-pool block copies ([MC] "Copy-on-Write", "Snapshot": a shared

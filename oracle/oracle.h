@@ -152,6 +152,13 @@ int or_load_q8(const or_layout *L, int64_t C, int64_t d, uint8_t *pool,
                const or_tables *T, const or_jobs *J,
                const uint8_t *arena, int64_t arena_bytes, uint32_t *status);
 int64_t or_object_bytes_q8(const or_layout *L, int64_t C, int64_t d, int og);
+int or_store_blocks_q8(const or_layout *L, int64_t nb, int kda_every, int64_t d, const uint8_t *pool,
+                       const or_tables *T, const or_jobs *J,
+                       uint8_t *arena, int64_t arena_bytes, uint32_t *status);
+int or_load_blocks_q8(const or_layout *L, int64_t nb, int kda_every, int64_t d, uint8_t *pool,
+                      const or_tables *T, const or_jobs *J,
+                      const uint8_t *arena, int64_t arena_bytes, uint32_t *status);
+int64_t or_object_bytes_blocks_q8(const or_layout *L, int64_t nb, int kda_every, int64_t d, int og);
 int or_unified_block_size(int64_t attn_token_bytes, int64_t state_page_bytes,
                           int64_t align, int64_t *out);
 

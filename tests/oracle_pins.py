@@ -667,6 +667,89 @@ def check_q8_objects(lib):
                 assert np.array_equal(y, q_np.astype(np.float32) * s_np[:, None])
 
 
+def check_q8_block_objects(lib):
+    """Block-granular objects with INT8 records: (1) nb = C/N blocks from
+    chunk * m with the last-block snapshot are exactly the chunk-form INT8
+    objects; (2) with one snapshot per block, each KDA layer holds nb records
+    in block order, each its page's raw conv bytes then the numpy
+    restatement's scales and codes, while paged layers equal the plain block
+    objects; (3) the load restores conv bytes exactly and states as decoded
+    codes at every block position; (4) row lengths outside the rules are
+    refused."""
+    case = tiny_case(lib, 0)
+    L, C = case["L"], case["C"]
+    m, d = C // L.N, 64
+    og_n = L.num_object_groups
+    pool = case["pool"]
+    units = [[(int(j["request"]), int(j["chunk"]) * m) for j in J] for J in case["jobs"]]
+    # (1)
+    sizes_c = [L.object_bytes_q8(C, d, g) for g in range(og_n)]
+    jobs_c, nbytes = W.pack_jobs(W.store_units(case["lengths"], C, og_n), sizes_c)
+    arena_c = np.zeros(nbytes, dtype=np.uint8)
+    assert oracle.store_q8(L, C, d, pool, case["t_src"], jobs_c, arena_c) == 0
+    sizes_b = [L.object_bytes_blocks_q8(m, False, d, g) for g in range(og_n)]
+    assert sizes_b == sizes_c
+    jobs_b, nbytes_b = W.pack_jobs(units, sizes_b)
+    arena_b = np.zeros(nbytes_b, dtype=np.uint8)
+    assert oracle.store_blocks_q8(L, m, False, d, pool, case["t_src"], jobs_b, arena_b) == 0
+    assert np.array_equal(arena_c, arena_b), "block INT8 form with nb = C/N differs from the chunk form"
+    # (2)
+    sizes = [L.object_bytes_blocks_q8(m, True, d, g) for g in range(og_n)]
+    plain_sizes = [L.object_bytes_blocks(m, True, g) for g in range(og_n)]
+    kda = [i for i in range(len(L.kinds)) if L.kinds[i] == "KDA"]
+    conv, rec = 4608, 4 * 64 * 64 * 4
+    rows = rec // (4 * d)
+    record = conv + 4 * rows + rows * d
+    kda_og = L.object_group[kda[0]]
+    assert sizes[kda_og] == m * len(kda) * record
+    jobs, nbytes = W.pack_jobs(units, sizes)
+    arena = np.zeros(nbytes, dtype=np.uint8)
+    assert oracle.store_blocks_q8(L, m, True, d, pool, case["t_src"], jobs, arena) == 0
+    plain_jobs, plain_bytes = W.pack_jobs(units, plain_sizes)
+    plain = np.zeros(plain_bytes, dtype=np.uint8)
+    assert oracle.store_blocks(L, m, True, pool, case["t_src"], plain_jobs, plain) == 0
+    for g in range(og_n):
+        if g == kda_og:
+            continue
+        for a, b in zip(jobs[g], plain_jobs[g]):
+            n = sizes[g]
+            assert np.array_equal(arena[int(a["offset"]):int(a["offset"]) + n], plain[int(b["offset"]):int(b["offset"]) + n])
+    for job in jobs[kda_og]:
+        r, first, off = int(job["request"]), int(job["chunk"]), int(job["offset"])
+        for k, i in enumerate(kda):
+            for j in range(m):
+                rec_at = off + (k * m + j) * record
+                blk = int(case["t_src"][L.kv_group[i]][r, first + j])
+                page = L.base[i] + blk * L.stride[i]
+                assert np.array_equal(arena[rec_at:rec_at + conv], pool[page:page + conv])
+                s_np, q_np = q8_numpy(pool[page + conv:page + conv + rec].view(np.float32), d)
+                got_s = arena[rec_at + conv:rec_at + conv + 4 * rows].view(np.float32)
+                got_q = arena[rec_at + conv + 4 * rows:rec_at + record].view(np.int8).reshape(rows, d)
+                assert np.array_equal(got_s, s_np) and np.array_equal(got_q, q_np), (r, first, i, j)
+    # (3)
+    dst = np.zeros(L.pool_bytes, dtype=np.uint8)
+    assert oracle.load_blocks_q8(L, m, True, d, dst, case["t_dst"], jobs, arena) == 0
+    for job in jobs[kda_og]:
+        r, first = int(job["request"]), int(job["chunk"])
+        for i in kda:
+            g = L.kv_group[i]
+            for j in range(m):
+                src = L.base[i] + int(case["t_src"][g][r, first + j]) * L.stride[i]
+                out = L.base[i] + int(case["t_dst"][g][r, first + j]) * L.stride[i]
+                assert np.array_equal(dst[out:out + conv], pool[src:src + conv])
+                s_np, q_np = q8_numpy(pool[src + conv:src + conv + rec].view(np.float32), d)
+                y = dst[out + conv:out + conv + rec].view(np.float32).reshape(-1, d)
+                assert np.array_equal(y, q_np.astype(np.float32) * s_np[:, None])
+    # (4)
+    assert L.object_bytes_blocks_q8(m, True, 6, kda_og) == -1
+    assert L.object_bytes_blocks_q8(0, True, d, kda_og) == -1
+    try:
+        oracle.store_blocks_q8(L, m, True, 6, pool, case["t_src"], jobs, np.zeros(nbytes, np.uint8))
+        raise AssertionError("row length 6 accepted")
+    except oracle.OracleError as e:
+        assert e.code == oracle.ERR_INVALID_ARG
+
+
 def check_backends(lib):
     """vLLM's eligibility rule ("How vLLM manages the KV cache of hybrid
     models", §3.3): Kimi-Linear at its own N pads the KDA page (always
@@ -695,7 +778,7 @@ def check_backends(lib):
 ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",
        "check_budget", "check_page_formulas", "check_unified_block_size", "check_k3_groups", "check_closed_forms",
        "check_non_overlap", "check_store_load_cases", "check_block_objects", "check_copy_blocks",
-       "check_q8_golden", "check_q8_random", "check_q8_objects", "check_backends"]
+       "check_q8_golden", "check_q8_random", "check_q8_objects", "check_q8_block_objects", "check_backends"]
 
 
 def check_store_load_cases(lib):

@@ -51,6 +51,12 @@ MUTANTS = [
     ("block id upper bound off by one", "block >= L->num_blocks", "block > L->num_blocks"),
     ("object size counts KDA per block", "        if (L->layers[i].kind == OR_KDA && !kda_every)\n            total += page;",
      "        if (0)\n            total += page;"),
+    ("every-block snapshots stored raw under the codec",
+     "else if (sh->q8_row > 0)\n                            *status |= q8_page(",
+     "else if (0)\n                            *status |= q8_page("),
+    ("every-block INT8 records advance by the raw page",
+     "cursor += sh->q8_row > 0 ? q8_record_bytes(&L->layers[i], sh->q8_row)\n                                                 : L->real_bytes[i];",
+     "cursor += L->real_bytes[i];"),
 ]
 
 
