@@ -315,13 +315,18 @@ class PagingStep:
                                 for g in range(inp.layout.num_object_groups)]
             self.full_payload = sum(full[g] * len(u) for g, u in enumerate(units))
             inp.jobs, inp.arena_bytes = W.pack_jobs(units, inp.object_bytes)
-        if op == "blocks":
+        if op in ("blocks", "blocks_q8"):
             # the same chunks as block-granular objects holding one KDA
-            # snapshot per block (every block boundary of the chunk)
+            # snapshot per block (every block boundary of the chunk); with
+            # blocks_q8 every snapshot is an INT8 record
             m = C // cfg.N
             units = [[(int(j["request"]), int(j["chunk"]) * m) for j in J] for J in inp.jobs]
-            inp.object_bytes = [inp.layout.object_bytes_blocks(m, True, g)
-                                for g in range(inp.layout.num_object_groups)]
+            og = range(inp.layout.num_object_groups)
+            inp.object_bytes = [inp.layout.object_bytes_blocks(m, True, g) for g in og]
+            if op == "blocks_q8":
+                self.q8_row = W.state_row_elems(cfg)
+                self.full_payload = sum(inp.object_bytes[g] * len(u) for g, u in enumerate(units))
+                inp.object_bytes = [inp.layout.object_bytes_blocks_q8(m, True, self.q8_row, g) for g in og]
             inp.jobs, inp.arena_bytes = W.pack_jobs(units, inp.object_bytes)
             self.nb = m
         self.inp, self.L, self.C = inp, inp.layout, C
@@ -357,7 +362,7 @@ class PagingStep:
         # every payload byte is read once and written once, by the store and by the load
         self.store_bytes = 2 * self.store_payload
         self.load_bytes = 2 * self.load_payload
-        if op == "q8":
+        if op in ("q8", "blocks_q8"):
             # the store reads full pages and writes records; the load the reverse
             self.store_bytes = self.load_bytes = self.full_payload + inp.payload_bytes
         self.bytes_per_step = self.store_bytes + self.load_bytes
@@ -367,6 +372,9 @@ class PagingStep:
         if self.op == "blocks":
             lmc.lmc_store_blocks(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, pool, tables, jobs, self.arena,
                                  self.status, self.main)
+        elif self.op == "blocks_q8":
+            lmc.lmc_store_blocks_q8(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, self.q8_row, pool, tables, jobs,
+                                    self.arena, self.status, self.main)
         elif self.op == "q8":
             lmc.lmc_store_q8(self.L, self.C, self.q8_row, pool, tables, jobs, self.arena, self.status, self.main)
         else:
@@ -377,6 +385,9 @@ class PagingStep:
         if self.op == "blocks":
             lmc.lmc_load_blocks(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, pool, tables, jobs, self.arena,
                                 self.status, stream)
+        elif self.op == "blocks_q8":
+            lmc.lmc_load_blocks_q8(self.L, self.nb, lmc.LMC_KDA_EVERY_BLOCK, self.q8_row, pool, tables, jobs,
+                                   self.arena, self.status, stream)
         elif self.op == "q8":
             lmc.lmc_load_q8(self.L, self.C, self.q8_row, pool, tables, jobs, self.arena, self.status, stream)
         else:
@@ -653,7 +664,7 @@ def run_gpu(args):
     value = S.bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = _peaks()
     st_avg, ld_avg = statistics.mean(store_ms), statistics.mean(load_ms)
-    suffix = "_q8_kernel" if args.op == "q8" else "_kernel"
+    suffix = "_q8_kernel" if args.op in ("q8", "blocks_q8") else "_kernel"
     if args.op == "copy":
         dominant, dom_bytes, dom_ms = "lmc_copy_kernel", S.bytes_per_step, st_avg
     elif cfg.mixed:
@@ -712,10 +723,11 @@ def main():
                     help="ranges of (request, chunk) units the end-to-end step is pipelined over")
     ap.add_argument("--impl", choices=["lmc", "reference"], default="lmc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["paging", "blocks", "copy", "q8"], default="paging",
+    ap.add_argument("--op", choices=["paging", "blocks", "copy", "q8", "blocks_q8"], default="paging",
                     help="paging: store + load by chunk; blocks: block-granular objects with one KDA "
                          "snapshot per block; copy: in-pool copy of every KDA snapshot; q8: store + load "
-                         "with KDA snapshots as INT8 records")
+                         "with KDA snapshots as INT8 records; blocks_q8: block-granular objects with every "
+                         "snapshot as an INT8 record")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -352,6 +352,25 @@ LMC_API int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t ro
 LMC_API int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, int32_t object_group,
                         int64_t *out);
 
+/* Block-granular store/load (as lmc_store_blocks / lmc_load_blocks) with
+ * every stored KDA snapshot kept as an INT8 record as lmc_store_q8 does: the
+ * checkpoints taken at block boundaries ([KL] align mode) compressed for
+ * storage ([MC] "Compressed Checkpoint Storage"). With LMC_KDA_EVERY_BLOCK a
+ * KDA layer holds blocks_per_object records, one per block in order, each
+ * conv bytes, scales, codes; with LMC_KDA_LAST_BLOCK one record, that of the
+ * object's last block. Row rules, status bits and errors as lmc_store_q8. */
+LMC_API int lmc_store_blocks_q8(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                                int64_t row_elems, const void *pool, const lmc_batch *batch, void *arena,
+                                int64_t arena_bytes, uint32_t *status, void *stream);
+LMC_API int lmc_load_blocks_q8(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                               int64_t row_elems, void *pool, const lmc_batch *batch, const void *arena,
+                               int64_t arena_bytes, uint32_t *status, void *stream);
+
+/* Bytes of one block-granular object of `object_group` as lmc_store_blocks_q8
+ * writes it. */
+LMC_API int lmc_object_bytes_blocks_q8(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                                       int64_t row_elems, int32_t object_group, int64_t *out);
+
 /* ---- diagnostics ----------------------------------------------------------- */
 
 /* Self-test of the device-side failure reporting: launches one thread that

@@ -135,6 +135,10 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
         getattr(so, name).argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
                                       _i64, ctypes.c_void_p, ctypes.c_void_p]
     so.lmc_object_bytes_q8.argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_int32, _P(_i64)]
+    for name in ("lmc_store_blocks_q8", "lmc_load_blocks_q8"):
+        getattr(so, name).argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, _i64, ctypes.c_void_p,
+                                      _P(lmc_batch), ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p]
+    so.lmc_object_bytes_blocks_q8.argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, _i64, ctypes.c_int32, _P(_i64)]
     so.lmc_selftest_wait.argtypes = [ctypes.c_void_p, _i64, ctypes.c_void_p]
     so.lmc_selftest_row_scale.argtypes = [ctypes.c_void_p] * 4 + [_i64, ctypes.c_void_p]
     so.lmc_strerror.argtypes = [ctypes.c_int]
@@ -236,6 +240,12 @@ class Layout:
     def object_bytes_blocks(self, blocks_per_object: int, kda_every: bool, object_group: int) -> int:
         return lmc_object_bytes_blocks(self, blocks_per_object,
                                        LMC_KDA_EVERY_BLOCK if kda_every else LMC_KDA_LAST_BLOCK, object_group)
+
+    def object_bytes_blocks_q8(self, blocks_per_object: int, kda_every: bool, row_elems: int,
+                               object_group: int) -> int:
+        return lmc_object_bytes_blocks_q8(self, blocks_per_object,
+                                          LMC_KDA_EVERY_BLOCK if kda_every else LMC_KDA_LAST_BLOCK, row_elems,
+                                          object_group)
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -406,6 +416,35 @@ def lmc_load_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, 
     _check(_lib.lmc_load_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
                             arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
                             _stream_ptr(stream)), "lmc_load_q8")
+
+
+def lmc_object_bytes_blocks_q8(layout: Layout, blocks_per_object: int, kda_mode: int, row_elems: int,
+                               object_group: int) -> int:
+    out = _i64(0)
+    _check(_lib.lmc_object_bytes_blocks_q8(layout.handle, int(blocks_per_object), int(kda_mode), int(row_elems),
+                                           int(object_group), ctypes.byref(out)), "lmc_object_bytes_blocks_q8")
+    return out.value
+
+
+def lmc_store_blocks_q8(layout: Layout, blocks_per_object: int, kda_mode: int, row_elems: int, pool, tables, jobs,
+                        arena, status, stream=None) -> None:
+    """Block-granular store with the stored KDA snapshots as INT8 records."""
+    _check_launch(layout, pool, arena, status)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_store_blocks_q8(layout.handle, int(blocks_per_object), int(kda_mode), int(row_elems),
+                                    pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
+                                    arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+           "lmc_store_blocks_q8")
+
+
+def lmc_load_blocks_q8(layout: Layout, blocks_per_object: int, kda_mode: int, row_elems: int, pool, tables, jobs,
+                       arena, status, stream=None) -> None:
+    _check_launch(layout, pool, arena, status)
+    b, keep = _batch(layout, tables, jobs)
+    _check(_lib.lmc_load_blocks_q8(layout.handle, int(blocks_per_object), int(kda_mode), int(row_elems),
+                                   pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
+                                   arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+           "lmc_load_blocks_q8")
 
 
 def lmc_selftest_wait(status, rounds: int, stream=None) -> None:

@@ -94,7 +94,7 @@ struct Entry {
     uint8_t kda;          // 1: a KDA state page (a missing one is NO_SNAPSHOT)
     uint8_t codec;        // 1: INT8 record of the recurrent state (see below)
     int32_t rows;         // codec: state rows of the page; tile_bytes holds rows per tile
-    int32_t pad;
+    int32_t obj_stride;   // bytes between the object's consecutive pages of this entry
 };
 
 struct Group {
@@ -274,7 +274,7 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
         const int64_t row0 = (int64_t)k * E.tile_bytes;
         const int32_t n = min(E.tile_bytes, (int32_t)(E.rows - row0));
         const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + E.seg_bytes + row0 * 4 * P.q8_row;
-        const int64_t rec = job.offset + E.obj_off;
+        const int64_t rec = job.offset + E.obj_off + (int64_t)j * E.obj_stride;
         const int64_t codes = rec + 4 * (int64_t)E.rows + row0 * P.q8_row;
         s.bytes = n;
         if (P.mode == kStore) {
@@ -291,7 +291,7 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
         return 0;
     }
     const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + piece;
-    const int64_t obj = job.offset + E.obj_off + (int64_t)j * E.seg_bytes + piece;
+    const int64_t obj = job.offset + E.obj_off + (int64_t)j * E.obj_stride + piece;
     s.src = P.src_base + (P.mode == kStore ? page : obj);
     s.dst = P.dst_base + (P.mode == kStore ? obj : page);
     return 0;
@@ -943,9 +943,12 @@ int sm_count() {
 
 bool aligned16(int64_t x) { return (x & 15) == 0; }
 
-// Appends a layer entry (one page of `d`, `pages` pages per object).
+// Appends a layer entry: `pages` pages of `d` per object. The pages lie back
+// to back from the object's current offset `obj`, which advances past them;
+// with rec_stride > 0 page j lies at obj + j * rec_stride instead (the page
+// part of interleaved records) and the caller advances obj.
 int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t pos_add, int64_t &obj,
-              int64_t &tiles, bool &vec) {
+              int64_t &tiles, bool &vec, int64_t rec_stride = 0) {
     if (ne >= kMaxEntries)
         return LMC_ERR_INVALID_ARG;
     if (d.real_bytes > INT32_MAX - kTileBytes)
@@ -966,8 +969,9 @@ int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t 
     E.kda = d.kind == LMC_LAYER_KDA;
     E.pos_add = pos_add;
     E.kv = (int16_t)d.kv_group;
+    E.obj_stride = rec_stride > 0 ? (int32_t)rec_stride : seg;
     int64_t add;
-    if (!lmc::mul_ok(pages, seg, &add) || !lmc::add_ok(obj, add, &obj))
+    if (rec_stride > INT32_MAX || (rec_stride == 0 && (!lmc::mul_ok(pages, seg, &add) || !lmc::add_ok(obj, add, &obj))))
         return LMC_ERR_OVERFLOW;
     tiles += pages * E.tiles_per_seg;
     if (tiles > INT32_MAX)
@@ -976,16 +980,16 @@ int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t 
     return LMC_OK;
 }
 
-// Appends the codec entry of a KDA layer: the recurrent state after the conv
-// bytes, encoded as an INT8 record (scales, then codes) at the object's
-// current offset; `rows_per_tile` rows per tile.
-int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_spec &spec, int32_t pos_add,
-                    int64_t &obj, int64_t &tiles, bool &vec) {
+// Appends the codec entry of a KDA layer: for each of `pages` snapshots per
+// object, the recurrent state after the conv bytes, encoded as the scales
+// then the codes of an INT8 record at obj_off + j * rec_stride.
+int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_spec &spec, int64_t pages,
+                    int32_t pos_add, int64_t obj_off, int64_t rec_stride, int64_t &tiles, bool &vec) {
     if (ne >= kMaxEntries)
         return LMC_ERR_INVALID_ARG;
     const int64_t row = P.q8_row;
     const int64_t rows = spec.rec_bytes / (4 * row);
-    if (rows > INT32_MAX || spec.conv_bytes > INT32_MAX)
+    if (rows > INT32_MAX || spec.conv_bytes > INT32_MAX || rec_stride > INT32_MAX)
         return LMC_ERR_INVALID_ARG;
     // rows per tile: a multiple of 4, so every tile's codes and scales start
     // on a 16-byte boundary
@@ -993,7 +997,8 @@ int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_s
     Entry &E = P.entries[ne++];
     E.pool_base = d.base;
     E.pool_stride = d.stride;
-    E.obj_off = obj;
+    E.obj_off = obj_off;
+    E.obj_stride = (int32_t)rec_stride;
     E.seg_bytes = (int32_t)spec.conv_bytes;  // the state starts after the conv bytes
     E.tile_bytes = per_tile;
     E.rows = (int32_t)rows;
@@ -1003,8 +1008,7 @@ int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_s
     E.codec = 1;
     E.pos_add = pos_add;
     E.kv = (int16_t)d.kv_group;
-    obj += 4 * rows + rows * row;
-    tiles += E.tiles_per_seg;
+    tiles += pages * E.tiles_per_seg;
     // the rows are read and written as 16-byte vectors
     vec = vec && aligned16(d.base) && aligned16(d.stride) && aligned16(spec.conv_bytes);
     return tiles > INT32_MAX ? LMC_ERR_OVERFLOW : LMC_OK;
@@ -1088,13 +1092,21 @@ int build_object_plan(const lmc_layout *L, const Shape &sh, const void *pool, co
             const bool last_only = d.kind == LMC_LAYER_KDA && !sh.kda_every;
             int rc;
             if (d.kind == LMC_LAYER_KDA && sh.q8_row > 0) {
-                // the conv window is copied as is, the state goes through the codec
+                // one INT8 record per stored snapshot, back to back: the conv
+                // window as is, then the state's scales and codes
+                const lmc_layer_spec &spec = L->specs[i];
+                const int64_t pages = last_only ? 1 : sh.nb;
+                const int32_t pos_add = last_only ? (int32_t)(sh.nb - 1) : 0;
+                const int64_t rows = spec.rec_bytes / (4 * (int64_t)sh.q8_row);
+                const int64_t record = spec.conv_bytes + 4 * rows + rows * (int64_t)sh.q8_row;
                 lmc_layer_desc conv = d;
-                conv.real_bytes = L->specs[i].conv_bytes;
-                rc = conv.real_bytes > 0 ? add_entry(P, ne, conv, 1, (int32_t)(sh.nb - 1), obj, tiles, vec)
-                                         : LMC_OK;
+                conv.real_bytes = spec.conv_bytes;
+                int64_t at = obj, add = 0;
+                rc = conv.real_bytes > 0 ? add_entry(P, ne, conv, pages, pos_add, at, tiles, vec, record) : LMC_OK;
                 if (rc == LMC_OK)
-                    rc = add_codec_entry(P, ne, d, L->specs[i], (int32_t)(sh.nb - 1), obj, tiles, vec);
+                    rc = add_codec_entry(P, ne, d, spec, pages, pos_add, obj + spec.conv_bytes, record, tiles, vec);
+                if (rc == LMC_OK && (!lmc::mul_ok(pages, record, &add) || !lmc::add_ok(obj, add, &obj)))
+                    rc = LMC_ERR_OVERFLOW;
             } else {
                 rc = add_entry(P, ne, d, last_only ? 1 : sh.nb, last_only ? (int32_t)(sh.nb - 1) : 0, obj, tiles,
                                vec);
@@ -1191,17 +1203,53 @@ int run_objects(const lmc_layout *L, const Shape &sh, const void *pool, const lm
 // layer's recurrent state a whole number of rows and a multiple of 4 rows,
 // and its conv bytes a multiple of 16: every record stays a multiple of 16
 // bytes, so the rows behind it remain 16-byte aligned.
-int q8_shape(const lmc_layout *L, int64_t chunk, int64_t d, Shape &sh) {
-    const int rc = chunk_shape(L, chunk, sh);
-    if (rc != LMC_OK)
-        return rc;
+int q8_check(const lmc_layout *L, int64_t d) {
     if (d < 4 || d > 512 || d % 4 != 0)
         return LMC_ERR_INVALID_ARG;
     for (const lmc_layer_spec &spec : L->specs)
         if (spec.kind == LMC_LAYER_KDA && (spec.rec_bytes % (4 * d) != 0 || (spec.rec_bytes / (4 * d)) % 4 != 0 ||
                                            spec.conv_bytes % 16 != 0))
             return LMC_ERR_INVALID_ARG;
-    sh.q8_row = (int32_t)d;
+    return LMC_OK;
+}
+
+int q8_shape(const lmc_layout *L, int64_t chunk, int64_t d, Shape &sh) {
+    int rc = chunk_shape(L, chunk, sh);
+    if (rc == LMC_OK)
+        rc = q8_check(L, d);
+    sh.q8_row = rc == LMC_OK ? (int32_t)d : 0;
+    return rc;
+}
+
+int q8_block_shape(const lmc_layout *L, int64_t nb, int32_t kda_mode, int64_t d, Shape &sh) {
+    int rc = block_shape(L, nb, kda_mode, sh);
+    if (rc == LMC_OK)
+        rc = q8_check(L, d);
+    sh.q8_row = rc == LMC_OK ? (int32_t)d : 0;
+    return rc;
+}
+
+// Bytes of one object of `og` with INT8 KDA records: a paged layer's nb
+// pages, a KDA layer's one (or, every block, nb) records.
+int object_bytes_q8(const lmc_layout *L, const Shape &sh, int32_t og, int64_t *out) {
+    if (out == nullptr || og < 0 || (size_t)og >= L->object_group_layers.size())
+        return LMC_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int32_t i : L->object_group_layers[og]) {
+        const lmc_layer_spec &spec = L->specs[i];
+        int64_t part;
+        if (spec.kind == LMC_LAYER_KDA) {
+            const int64_t rows = spec.rec_bytes / (4 * (int64_t)sh.q8_row);
+            const int64_t record = spec.conv_bytes + 4 * rows + rows * (int64_t)sh.q8_row;
+            if (!lmc::mul_ok(sh.kda_every ? sh.nb : 1, record, &part))
+                return LMC_ERR_OVERFLOW;
+        } else if (!lmc::mul_ok(sh.nb, L->desc[i].real_bytes, &part)) {
+            return LMC_ERR_OVERFLOW;
+        }
+        if (!lmc::add_ok(total, part, &total))
+            return LMC_ERR_OVERFLOW;
+    }
+    *out = total;
     return LMC_OK;
 }
 
@@ -1302,26 +1350,31 @@ extern "C" int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t
 extern "C" int lmc_object_bytes_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems,
                                    int32_t object_group, int64_t *out) {
     Shape sh;
-    int rc = q8_shape(layout, chunk_size, row_elems, sh);
-    if (rc != LMC_OK)
-        return rc;
-    if (out == nullptr || object_group < 0 || (size_t)object_group >= layout->object_group_layers.size())
-        return LMC_ERR_INVALID_ARG;
-    int64_t total = 0;
-    for (int32_t i : layout->object_group_layers[object_group]) {
-        const lmc_layer_spec &spec = layout->specs[i];
-        int64_t part;
-        if (spec.kind == LMC_LAYER_KDA) {
-            const int64_t rows = spec.rec_bytes / (4 * row_elems);
-            part = spec.conv_bytes + 4 * rows + rows * row_elems;
-        } else if (!lmc::mul_ok(sh.nb, layout->desc[i].real_bytes, &part)) {
-            return LMC_ERR_OVERFLOW;
-        }
-        if (!lmc::add_ok(total, part, &total))
-            return LMC_ERR_OVERFLOW;
-    }
-    *out = total;
-    return LMC_OK;
+    const int rc = q8_shape(layout, chunk_size, row_elems, sh);
+    return rc != LMC_OK ? rc : object_bytes_q8(layout, sh, object_group, out);
+}
+
+extern "C" int lmc_store_blocks_q8(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                                   int64_t row_elems, const void *pool, const lmc_batch *batch, void *arena,
+                                   int64_t arena_bytes, uint32_t *status, void *stream) {
+    Shape sh;
+    const int rc = q8_block_shape(layout, blocks_per_object, kda_mode, row_elems, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kStore);
+}
+
+extern "C" int lmc_load_blocks_q8(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                                  int64_t row_elems, void *pool, const lmc_batch *batch, const void *arena,
+                                  int64_t arena_bytes, uint32_t *status, void *stream) {
+    Shape sh;
+    const int rc = q8_block_shape(layout, blocks_per_object, kda_mode, row_elems, sh);
+    return rc != LMC_OK ? rc : run_objects(layout, sh, pool, batch, arena, arena_bytes, status, stream, kLoad);
+}
+
+extern "C" int lmc_object_bytes_blocks_q8(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
+                                          int64_t row_elems, int32_t object_group, int64_t *out) {
+    Shape sh;
+    const int rc = q8_block_shape(layout, blocks_per_object, kda_mode, row_elems, sh);
+    return rc != LMC_OK ? rc : object_bytes_q8(layout, sh, object_group, out);
 }
 
 extern "C" int lmc_selftest_row_scale(const float *amax, float *scale, float *inv, float *ieee, int64_t n,

@@ -398,14 +398,19 @@ def _block_units(inp, kind):
     return [(nb, False, [u] * og_n) for nb, u in sorted(tails.items())]
 
 
-def _blocks_exact(lmc, inp, Lp, kind):
+def _blocks_exact(lmc, inp, Lp, kind, d=0):
+    """Block-granular objects (d > 0: with INT8 KDA records of rows of d)
+    stored and loaded back, compared in full with the oracle."""
     Lo = inp.layout
     shapes = _block_units(inp, kind)
     assert shapes
     for nb, every, units in shapes:
-        sizes = [Lo.object_bytes_blocks(nb, every, g) for g in range(Lo.num_object_groups)]
-        for g in range(Lo.num_object_groups):
-            assert Lp.object_bytes_blocks(nb, every, g) == sizes[g]
+        if d:
+            sizes = [Lo.object_bytes_blocks_q8(nb, every, d, g) for g in range(Lo.num_object_groups)]
+            assert [Lp.object_bytes_blocks_q8(nb, every, d, g) for g in range(Lo.num_object_groups)] == sizes
+        else:
+            sizes = [Lo.object_bytes_blocks(nb, every, g) for g in range(Lo.num_object_groups)]
+            assert [Lp.object_bytes_blocks(nb, every, g) for g in range(Lo.num_object_groups)] == sizes
         jobs, nbytes = W.pack_jobs(units, sizes)
         mode = lmc.LMC_KDA_EVERY_BLOCK if every else lmc.LMC_KDA_LAST_BLOCK
         pool_h = W.fill_normal_np(Lo.pool_bytes, 55 + nb)
@@ -414,14 +419,21 @@ def _blocks_exact(lmc, inp, Lp, kind):
         fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
         st = _status()
         dj = dev_jobs(jobs, DEV)
-        lmc.lmc_store_blocks(Lp, nb, mode, pool, dev_tables(inp.tables_src, DEV), dj, arena, st)
-        lmc.lmc_load_blocks(Lp, nb, mode, fresh, dev_tables(inp.tables_dst, DEV), dj, arena, st)
+        t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+        arena_o = np.full(nbytes, 0x3C, dtype=np.uint8)
+        fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+        if d:
+            lmc.lmc_store_blocks_q8(Lp, nb, mode, d, pool, t_src, dj, arena, st)
+            lmc.lmc_load_blocks_q8(Lp, nb, mode, d, fresh, t_dst, dj, arena, st)
+            assert oracle.store_blocks_q8(Lo, nb, every, d, pool_h, inp.tables_src, jobs, arena_o) == 0
+            assert oracle.load_blocks_q8(Lo, nb, every, d, fresh_o, inp.tables_dst, jobs, arena_o) == 0
+        else:
+            lmc.lmc_store_blocks(Lp, nb, mode, pool, t_src, dj, arena, st)
+            lmc.lmc_load_blocks(Lp, nb, mode, fresh, t_dst, dj, arena, st)
+            assert oracle.store_blocks(Lo, nb, every, pool_h, inp.tables_src, jobs, arena_o) == 0
+            assert oracle.load_blocks(Lo, nb, every, fresh_o, inp.tables_dst, jobs, arena_o) == 0
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        arena_o = np.full(nbytes, 0x3C, dtype=np.uint8)
-        assert oracle.store_blocks(Lo, nb, every, pool_h, inp.tables_src, jobs, arena_o) == 0
-        fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
-        assert oracle.load_blocks(Lo, nb, every, fresh_o, inp.tables_dst, jobs, arena_o) == 0
         assert np.array_equal(arena.cpu().numpy(), arena_o), (kind, nb)
         assert np.array_equal(fresh.cpu().numpy(), fresh_o), (kind, nb)
 
@@ -452,6 +464,71 @@ def test_block_objects_random_specs(lmc, t):
     _blocks_exact(lmc, inp, Lp, "every")
     if _block_units(inp, "tails"):
         _blocks_exact(lmc, inp, Lp, "tails")
+
+
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("kind", ["tails", "every"])
+def test_q8_block_objects_exact(lmc, packed, kind):
+    """Block-granular objects with INT8 KDA records (rows of 64): tails past
+    the last whole chunk (the last block's snapshot) and chunks with one
+    snapshot per block."""
+    inp, Lp = case_inputs(_tail_cfg(8, packed))
+    _blocks_exact(lmc, inp, Lp, kind, d=64)
+
+
+@pytest.mark.parametrize("d,rows", [(4, 2400), (12, 800), (128, 16), (512, 20)])
+def test_q8_block_objects_row_lengths_exact(lmc, d, rows):
+    """Every-block INT8 records for row lengths of each encoder and decoder
+    path, single- and multi-tile states."""
+    state = {"kind": "KDA", "token_bytes": 0, "conv_bytes": 48, "rec_bytes": 4 * d * rows, "window": 0}
+    spec = [state, W.mla(32), dict(state, conv_bytes=64), W.mla(32)]
+    cfg = W.Config(450 + d, "q8b", spec, N=8, requested_chunk=16, packed=bool(d % 8), num_requests=3,
+                   lengths="fixed", fixed_lengths=(40, 77, 23), seed=d)
+    inp, Lp = case_inputs(cfg)
+    _blocks_exact(lmc, inp, Lp, "every", d=d)
+
+
+def test_q8_block_objects_full_size_every_block(lmc):
+    """The lognormal Kimi-Linear batch (packed, chunk 2N) as block objects of
+    2 blocks with every snapshot an INT8 record (d = 128): sampled objects
+    and decoded pages against the oracle."""
+    cfg = W.CONFIGS[2]
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    m, d = C // Lo.N, W.state_row_elems(cfg)
+    units = [[(int(j["request"]), int(j["chunk"]) * m) for j in J] for J in inp.jobs]
+    sizes = [Lo.object_bytes_blocks_q8(m, True, d, g) for g in range(Lo.num_object_groups)]
+    jobs, nbytes = W.pack_jobs(units, sizes)
+    pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, 64)
+    arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    dj = dev_jobs(jobs, DEV)
+    lmc.lmc_store_blocks_q8(Lp, m, lmc.LMC_KDA_EVERY_BLOCK, d, pool, dev_tables(inp.tables_src, DEV), dj, arena, st)
+    lmc.lmc_load_blocks_q8(Lp, m, lmc.LMC_KDA_EVERY_BLOCK, d, fresh, dev_tables(inp.tables_dst, DEV), dj, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(9)
+    sel = [J[np.sort(rng.choice(len(J), 5, replace=False))] for J in jobs]
+    pages, s0 = oracle.list_pages(Lo, C, inp.tables_src, sel, 1 << 62, nb=m, kda_every=True)
+    assert s0 == 0
+    host = np.zeros(Lo.pool_bytes, dtype=np.uint8)
+    for pg in pages:
+        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
+        host[lo:lo + n] = pool[lo:lo + n].cpu().numpy()
+    arena_o = np.zeros(nbytes, dtype=np.uint8)
+    assert oracle.store_blocks_q8(Lo, m, True, d, host, inp.tables_src, sel, arena_o) == 0
+    for g, J in enumerate(sel):
+        for job in J:
+            lo, hi = int(job["offset"]), int(job["offset"]) + sizes[g]
+            assert np.array_equal(arena[lo:hi].cpu().numpy(), arena_o[lo:hi])
+    back = np.zeros(Lo.pool_bytes, dtype=np.uint8)
+    assert oracle.load_blocks_q8(Lo, m, True, d, back, inp.tables_dst, sel, arena_o) == 0
+    pages_d, _ = oracle.list_pages(Lo, C, inp.tables_dst, sel, 1 << 62, nb=m, kda_every=True)
+    for pg in pages_d:
+        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
+        assert np.array_equal(fresh[lo:lo + n].cpu().numpy(), back[lo:lo + n])
 
 
 def test_block_objects_full_size_every_block(lmc):

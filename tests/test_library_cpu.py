@@ -212,6 +212,44 @@ def test_q8_object_sizes_match_oracle(lmc, cfg_index):
                     assert p.object_bytes_q8(C, d, g) == want
 
 
+@pytest.mark.parametrize("cfg_index", [0, 1, 2, 3, 4])
+def test_q8_block_object_sizes_match_oracle(lmc, cfg_index):
+    cfg = W.CONFIGS[cfg_index]
+    p = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, 1 << 36)
+    o = oracle.layout(cfg.layers, cfg.N, cfg.packed, 1 << 36)
+    for d in (4, 64, 128, 6, 1024):
+        for nb in (1, 2, 7):
+            for every in (False, True):
+                for g in range(o.num_object_groups):
+                    want = o.object_bytes_blocks_q8(nb, every, d, g)
+                    if want < 0:
+                        with pytest.raises(lmc.LmcError) as e:
+                            p.object_bytes_blocks_q8(nb, every, d, g)
+                        assert e.value.code == lmc.LMC_ERR_INVALID_ARG
+                    else:
+                        assert p.object_bytes_blocks_q8(nb, every, d, g) == want, (d, nb, every, g)
+    # nb = C / N with the last block's snapshot is the chunk form's object
+    if o.object_bytes_q8(cfg.N, 128, 0) > 0:
+        for g in range(o.num_object_groups):
+            assert p.object_bytes_blocks_q8(1, False, 128, g) == p.object_bytes_q8(cfg.N, 128, g)
+
+
+def test_q8_blocks_host_checks(lmc):
+    cfg = W.CONFIGS[1]
+    L = lmc.lmc_layout_build(cfg.layers, cfg.N, False, 1 << 34)
+    buf = (ctypes.c_uint8 * 256)()
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+    tables = (lmc.lmc_block_table * L.num_kv_groups)(*[lmc.lmc_block_table(addr, 4, 4)] * L.num_kv_groups)
+    jobs = (ctypes.c_void_p * L.num_object_groups)(*[addr] * L.num_object_groups)
+    counts = (ctypes.c_int64 * L.num_object_groups)(*[1] * L.num_object_groups)
+    b = lmc.lmc_batch(2, L.num_kv_groups, tables, L.num_object_groups, 0, jobs, counts)
+    for fn in (lmc._lib.lmc_store_blocks_q8, lmc._lib.lmc_load_blocks_q8):
+        assert fn(L.handle, 2, 1, 100, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+        assert fn(L.handle, 2, 2, 128, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+        assert fn(L.handle, 0, 1, 128, addr, ctypes.byref(b), addr, 64, addr, None) == lmc.LMC_ERR_INVALID_ARG
+        assert fn(L.handle, 2, 1, 128, addr, ctypes.byref(b), addr + 4, 64, addr, None) == lmc.LMC_ERR_ALIGN
+
+
 def test_q8_host_checks(lmc):
     cfg = W.CONFIGS[1]
     L = lmc.lmc_layout_build(cfg.layers, cfg.N, False, 1 << 34)
