@@ -320,7 +320,9 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 // shared memory per CTA): 7.10 TB/s (3 stages 7.00, 5 stages 7.03, 11 CTAs
 // 6.94, 9 CTAs 6.99; 256-thread CTAs 5.9 since a 64-row tile then runs only
 // two rounds; the next round prefetched in registers instead: 6.70 at
-// 128 x 12); decoder 256 x 6 with two rounds in flight (7.02 TB/s).
+// 128 x 12; preferring the largest shared-memory carveout cost up to 3 %, so
+// the driver's default split is kept); decoder 256 x 6 with two rounds in
+// flight (7.02 TB/s).
 #ifndef LMC_ROW_VEC
 #define LMC_ROW_VEC 2
 #endif
@@ -1145,10 +1147,6 @@ int launch_plan(const Plan &P, bool vec, void *stream) {
         // one CTA per tile, capped; the kernel strides over the rest
         const unsigned grid = (unsigned)std::min<int64_t>(P.total_tiles, (int64_t)sms * 2048);
         if (P.q8_row > 0) {
-            if (P.mode == kStore &&
-                cudaFuncSetAttribute(lmc_store_q8_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-                return LMC_ERR_CUDA;  // the staged encoder wants shared memory rather than L1 (its loads bypass L1)
             if (P.mode == kStore)
                 lmc_store_q8_kernel<<<grid, kEncThreads, 0, s>>>(P);
             else

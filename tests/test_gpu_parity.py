@@ -1012,6 +1012,57 @@ def test_store_load_captured_in_cuda_graph(lmc):
     assert np.array_equal(fresh.cpu().numpy(), fresh_o)
 
 
+def test_codec_and_block_calls_captured_in_cuda_graph(lmc):
+    """The INT8 calls and the block-granular INT8 calls enqueue only kernel
+    launches as well: captured into a CUDA graph (torch's default, global
+    capture mode) and replayed, they write the oracle's bytes."""
+    cfg = _tail_cfg(9, False)
+    inp, Lp = case_inputs(cfg)
+    Lo, C, d = inp.layout, inp.C, 64
+    m = C // Lo.N
+    og = range(Lo.num_object_groups)
+    chunk_units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
+    block_units = [[(r, c * m) for r, c in u] for u in chunk_units]
+    sizes_c = [Lo.object_bytes_q8(C, d, g) for g in og]
+    sizes_b = [Lo.object_bytes_blocks_q8(m, True, d, g) for g in og]
+    jobs_c, n_c = W.pack_jobs(chunk_units, sizes_c)
+    jobs_b, n_b = W.pack_jobs(block_units, sizes_b)
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 96)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    arena_c = torch.zeros(n_c, dtype=torch.uint8, device=DEV)
+    arena_b = torch.zeros(n_b, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+    jc, jb = dev_jobs(jobs_c, DEV), dev_jobs(jobs_b, DEV)
+    every = lmc.LMC_KDA_EVERY_BLOCK
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside capture
+        lmc.lmc_store_q8(Lp, C, d, pool, t_src, jc, arena_c, st, side)
+    torch.cuda.synchronize()
+    arena_c.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        lmc.lmc_store_q8(Lp, C, d, pool, t_src, jc, arena_c, st, side)
+        lmc.lmc_store_blocks_q8(Lp, m, every, d, pool, t_src, jb, arena_b, st, side)
+        lmc.lmc_load_blocks_q8(Lp, m, every, d, fresh, t_dst, jb, arena_b, st, side)
+    torch.cuda.synchronize()
+    assert not arena_c.any() and not arena_b.any(), "capture must not execute the kernels"
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ac = np.zeros(n_c, dtype=np.uint8)
+    assert oracle.store_q8(Lo, C, d, pool_h, inp.tables_src, jobs_c, ac) == 0
+    ab = np.zeros(n_b, dtype=np.uint8)
+    assert oracle.store_blocks_q8(Lo, m, True, d, pool_h, inp.tables_src, jobs_b, ab) == 0
+    fo = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    assert oracle.load_blocks_q8(Lo, m, True, d, fo, inp.tables_dst, jobs_b, ab) == 0
+    assert np.array_equal(arena_c.cpu().numpy(), ac)
+    assert np.array_equal(arena_b.cpu().numpy(), ab)
+    assert np.array_equal(fresh.cpu().numpy(), fo)
+
+
 def _max_spec():
     """256 layers: 62 sliding windows x 4 layers, 4 MLA, 4 KDA; one KV group
     per spec gives 64 KV groups and 64 object groups (the library's limits)."""
