@@ -1063,6 +1063,52 @@ def test_codec_and_block_calls_captured_in_cuda_graph(lmc):
     assert np.array_equal(fresh.cpu().numpy(), fo)
 
 
+def test_one_layout_shared_by_threads_and_streams(lmc):
+    """A built layout is shared by four host threads, each storing its own
+    request on its own stream into its own arena, many times over: every
+    arena equals the oracle's objects for that request (the calls keep no
+    state between them)."""
+    import threading
+    cfg = W.CONFIGS[0]
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 97)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    t_src = dev_tables(inp.tables_src, DEV)
+    work = []
+    for k in range(4):
+        r = k % len(inp.lengths)
+        units = [[(r, c) for c in range(int(inp.lengths[r]) // C)] for _ in range(Lo.num_object_groups)]
+        jobs, nbytes = W.pack_jobs(units, inp.object_bytes)
+        work.append((jobs, nbytes, torch.zeros(nbytes, dtype=torch.uint8, device=DEV), _status(),
+                     torch.cuda.Stream(DEV)))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(k):
+        try:
+            jobs, nbytes, arena, st, stream = work[k]
+            dj = dev_jobs(jobs, DEV)
+            for _ in range(25):
+                lmc.lmc_store(Lp, C, pool, t_src, dj, arena, st, stream)
+            stream.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(k,)) for k in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for jobs, nbytes, arena, st, _ in work:
+        assert int(st.item()) == 0
+        arena_o = np.zeros(nbytes, dtype=np.uint8)
+        assert oracle.store(Lo, C, pool_h, inp.tables_src, jobs, arena_o) == 0
+        assert np.array_equal(arena.cpu().numpy(), arena_o)
+
+
 def _max_spec():
     """256 layers: 62 sliding windows x 4 layers, 4 MLA, 4 KDA; one KV group
     per spec gives 64 KV groups and 64 object groups (the library's limits)."""
