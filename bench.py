@@ -703,8 +703,9 @@ def run_gpu(args):
     }
     if world == 1 and not args.no_cpu_baseline and args.op == "paging":
         threads = os.cpu_count() or 1
-        line["cpu_baseline"] = oracle_sample(args.config, requests=8, reps=20, threads=threads)
-        one = oracle_sample(args.config, requests=2, reps=2, threads=1)
+        # about 10 s of host time: ~150 passes over 8 requests on every core, then 20 on one
+        line["cpu_baseline"] = oracle_sample(args.config, requests=8, reps=150, threads=threads)
+        one = oracle_sample(args.config, requests=2, reps=20, threads=1)
         line["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
     print(json.dumps(line))
     if dist is not None:
