@@ -1109,6 +1109,42 @@ def test_one_layout_shared_by_threads_and_streams(lmc):
         assert np.array_equal(arena.cpu().numpy(), arena_o)
 
 
+def test_repeated_full_size_launches_are_deterministic(lmc):
+    """Fifty store + load rounds of the full Kimi-Linear batch, plain and
+    INT8: every round leaves the arena and the reloaded pool bit-identical
+    to the first round's (no race between tiles, CTAs or launches)."""
+    cfg = W.CONFIGS[1]
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    d = W.state_row_elems(cfg)
+    pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, 98)
+    ts, td = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+    units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
+    jobs_q, n_q = W.pack_jobs(units, [Lo.object_bytes_q8(C, d, g) for g in range(Lo.num_object_groups)])
+    for q8, jobs_np, nbytes in ((False, inp.jobs, inp.arena_bytes), (True, jobs_q, n_q)):
+        arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+        st = _status()
+        dj = dev_jobs(jobs_np, DEV)
+        first = None
+        for it in range(50):
+            if q8:
+                lmc.lmc_store_q8(Lp, C, d, pool, ts, dj, arena, st)
+                lmc.lmc_load_q8(Lp, C, d, fresh, td, dj, arena, st)
+            else:
+                lmc.lmc_store(Lp, C, pool, ts, dj, arena, st)
+                lmc.lmc_load(Lp, C, fresh, td, dj, arena, st)
+            if it == 0:
+                first = (arena.clone(), fresh.clone())
+            elif it % 7 == 0 or it == 49:
+                assert torch.equal(arena, first[0]) and torch.equal(fresh, first[1]), (q8, it)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        del arena, fresh, first
+        torch.cuda.empty_cache()
+
+
 def _max_spec():
     """256 layers: 62 sliding windows x 4 layers, 4 MLA, 4 KDA; one KV group
     per spec gives 64 KV groups and 64 object groups (the library's limits)."""
