@@ -121,6 +121,16 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def _kernel_times(nbytes, ms_list):
+    """Mean (the line's figure), median and best of one kernel's per-step
+    CUDA-event times, with the bytes-moved rates they give."""
+    if not ms_list or max(ms_list) <= 0:
+        return {"ms": None, "gbs": None}
+    mean, med, best = statistics.mean(ms_list), statistics.median(ms_list), min(ms_list)
+    return {"ms": round(mean, 4), "gbs": _gbs(nbytes, mean), "median_ms": round(med, 4),
+            "median_gbs": _gbs(nbytes, med), "best_ms": round(best, 4), "best_gbs": _gbs(nbytes, best)}
+
+
 def _gbs(nbytes, ms):
     return round(nbytes / (ms * 1e-3) / 1e9, 2) if nbytes and ms > 0 else None
 
@@ -688,8 +698,8 @@ def run_gpu(args):
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "chunks_per_s": round(S.chunks * world / (ms_per_step * 1e-3), 1),
-        "store": {"ms": round(st_avg, 4), "gbs": _gbs(S.store_bytes, st_avg)},
-        "load": {"ms": round(ld_avg, 4), "gbs": _gbs(S.load_bytes, ld_avg)},
+        "store": _kernel_times(S.store_bytes, store_ms),
+        "load": _kernel_times(S.load_bytes, load_ms),
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -104,3 +104,10 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert "workload" in d["config"]
+
+
+def test_kernel_times_mean_median_best():
+    t = bench._kernel_times(2_000_000_000, [2.0, 1.0, 4.0])
+    assert t["ms"] == round(7 / 3, 4) and t["median_ms"] == 2.0 and t["best_ms"] == 1.0
+    assert t["best_gbs"] == 2000.0 and t["median_gbs"] == 1000.0
+    assert bench._kernel_times(0, [0.002])["gbs"] is None
