@@ -135,6 +135,17 @@ def _gbs(nbytes, ms):
     return round(nbytes / (ms * 1e-3) / 1e9, 2) if nbytes and ms > 0 else None
 
 
+def _all_ranks(dist, flag: bool, device) -> bool:
+    """True when `flag` holds on every rank (a MIN over ranks; the local
+    flag when there is no process group)."""
+    if dist is None:
+        return bool(flag)
+    import torch
+    t = torch.tensor([1 if flag else 0], dtype=torch.int32, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(t.item())
+
+
 def _reduce_max(dist, values, device):
     """Max over ranks of per-rank timings (the only cross-rank step)."""
     import torch
@@ -646,23 +657,32 @@ def run_gpu(args):
     load_ms = [e[2].elapsed_time(e[3]) for e in evs]
     assert int(S.status.item()) == 0
 
-    if args.op == "copy":
-        S.setup_e2e()
-    else:
-        S.setup_e2e(args.e2e_parts)
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    for _ in range(2):
-        S.e2e_step()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(S.main)
-    for _ in range(e2e_steps):
-        S.e2e_step()
-    e1.record(S.main)
-    barrier()
-    assert int(S.h_status.item()) == 0
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # the end-to-end step needs the objects in pinned host memory; if any rank
+    # cannot pin them, every rank skips it (the ranks agree before going on)
+    e2e_err = None
+    try:
+        if args.op == "copy":
+            S.setup_e2e()
+        else:
+            S.setup_e2e(args.e2e_parts)
+    except (RuntimeError, MemoryError) as err:
+        e2e_err = f"{type(err).__name__}: {err}".splitlines()[0][:200]
+    e2e_ok = _all_ranks(dist, e2e_err is None, dev)
+    e2e_ms = 0.0
+    if e2e_ok:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            S.e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(S.main)
+        for _ in range(e2e_steps):
+            S.e2e_step()
+        e1.record(S.main)
+        barrier()
+        assert int(S.h_status.item()) == 0
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     ms_per_step = total_ms / args.steps
     if dist is not None:
@@ -705,9 +725,10 @@ def run_gpu(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": _traffic(dominant, cfg.index, args.op) if args.requests is None else None,
                      "algorithmic_bytes_per_launch": dom_bytes},
-        "e2e": {"value": round(S.bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h,
-                "parts": None if args.op == "copy" else args.e2e_parts},
+        "e2e": ({"value": round(S.bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h,
+                 "parts": None if args.op == "copy" else args.e2e_parts} if e2e_ok else
+                {"value": None, "unit": "GB/s", "unavailable": e2e_err or "a rank could not pin its host buffers"}),
         "gpu_launches": S.launches_per_step * args.steps,
         "clocks": clocks,
     }

@@ -30,6 +30,9 @@ def _worker(rank, world, port, out):
     assert (r, w, local) == (rank, world, rank) and d is dist
     dist.init_process_group("gloo", rank=rank, world_size=world)
     got = bench._reduce_max(dist, [1.0 + rank, 10.0 - rank], "cpu")
+    # the ranks agree on skipping the end-to-end step when any one cannot run it
+    agree = (bench._all_ranks(dist, True, "cpu"), bench._all_ranks(dist, rank == 0, "cpu"))
+    assert agree == (True, False), agree
     dist.barrier()
     dist.destroy_process_group()
     # the reference arm: every rank but 0 exits at once without work or output
@@ -59,3 +62,4 @@ def test_single_process_has_no_group(monkeypatch):
     sys.path.insert(0, ROOT)
     import bench
     assert bench._dist() == (None, 0, 1, 0)
+    assert bench._all_ranks(None, True, "cpu") and not bench._all_ranks(None, False, "cpu")
