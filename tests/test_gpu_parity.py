@@ -804,6 +804,35 @@ def test_q8_error_paths_match_oracle(lmc):
         assert np.array_equal(fresh.cpu().numpy(), fresh_o), what
 
 
+def test_q8_without_state_layers_is_the_plain_store(lmc):
+    """A model with no KDA layer (full and sliding-window attention only):
+    the INT8 calls have nothing to encode and move exactly the plain
+    objects."""
+    spec = [W.mla(64), W.swa(64, 16), W.mla(64), W.swa(64, 16)]
+    cfg = W.Config(470, "attn-only", spec, N=8, requested_chunk=16, packed=True, num_requests=3,
+                   lengths="fixed", fixed_lengths=(40, 77, 23), seed=47)
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    for g in range(Lo.num_object_groups):
+        assert Lp.object_bytes_q8(C, 64, g) == Lo.object_bytes(C, g)
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 48)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    arena = torch.full((inp.arena_bytes,), 0x3C, dtype=torch.uint8, device=DEV)
+    fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    dj = dev_jobs(inp.jobs, DEV)
+    lmc.lmc_store_q8(Lp, C, 64, pool, dev_tables(inp.tables_src, DEV), dj, arena, st)
+    lmc.lmc_load_q8(Lp, C, 64, fresh, dev_tables(inp.tables_dst, DEV), dj, arena, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    arena_o = np.full(inp.arena_bytes, 0x3C, dtype=np.uint8)
+    assert oracle.store(Lo, C, pool_h, inp.tables_src, inp.jobs, arena_o) == 0
+    fresh_o = np.full(Lo.pool_bytes, W.SENTINEL, dtype=np.uint8)
+    assert oracle.load(Lo, C, fresh_o, inp.tables_dst, inp.jobs, arena_o) == 0
+    assert np.array_equal(arena.cpu().numpy(), arena_o)
+    assert np.array_equal(fresh.cpu().numpy(), fresh_o)
+
+
 def test_q8_full_size_kimi_linear(lmc):
     """Kimi-Linear full size, d = 128: sampled records and decoded pages
     against the oracle; decoded values within half a step everywhere sampled."""
