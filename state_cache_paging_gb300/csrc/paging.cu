@@ -85,7 +85,7 @@ struct Entry {
     int64_t pool_base;    // pool byte offset of block 0's page
     int64_t pool_stride;  // bytes between consecutive blocks' pages
     int64_t obj_off;      // byte offset of the layer's first page in the object
-    int32_t seg_bytes;    // real bytes of one page
+    int32_t seg_bytes;    // real bytes of one page (codec: the conv bytes before the state)
     int32_t tile_bytes;   // bytes per tile of this page (last tile shorter)
     int32_t tiles_per_seg;
     int32_t tile_start;   // tiles of earlier layers in the object
@@ -269,8 +269,8 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
 
     if (kCodec && E.codec) {
         // rows [k * R, k * R + n) of the page's recurrent state, which starts
-        // after the conv bytes (seg_bytes); the record holds the scales at
-        // obj_off and the codes after all the scales
+        // after the conv bytes (seg_bytes); the entry's j-th record part, at
+        // obj_off + j * obj_stride, holds all the rows' scales, then the codes
         const int64_t row0 = (int64_t)k * E.tile_bytes;
         const int32_t n = min(E.tile_bytes, (int32_t)(E.rows - row0));
         const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + E.seg_bytes + row0 * 4 * P.q8_row;
