@@ -488,6 +488,31 @@ def test_q8_block_objects_row_lengths_exact(lmc, d, rows):
     _blocks_exact(lmc, inp, Lp, "every", d=d)
 
 
+@pytest.mark.parametrize("t", range(6))
+def test_q8_random_specs_exact(lmc, t):
+    """Random hybrid models (full attention, sliding windows, KDA states of
+    (heads, d, d) fp32 with d = 8 .. 64 and conv windows of whole 16-byte
+    units), random N and lengths, padded and packed: chunk objects and
+    every-block objects with INT8 records, exact against the oracle."""
+    rng = np.random.default_rng(7000 + t)
+    spec = P.random_spec(rng, int(rng.integers(2, 8)))
+    spec = [l for l in spec if l["kind"] != "KDA"] or [W.mla(32)]
+    d = int(rng.choice([8, 16, 32, 64]))
+    for _ in range(int(rng.integers(1, 4))):
+        spec.insert(int(rng.integers(0, len(spec) + 1)),
+                    W.kda(8 * int(rng.integers(1, 9)), 3, int(rng.choice([1, 2, 4])), d))
+    N = int(rng.choice([2, 4, 16]))
+    lengths = tuple(int(x) for x in rng.integers(N, 30 * N, size=int(rng.integers(1, 5))))
+    cfg = W.Config(480 + t, "q8-random", spec, N=N, requested_chunk=int(rng.integers(N, 4 * N)),
+                   packed=bool(t % 2), num_requests=len(lengths), lengths="fixed", fixed_lengths=lengths,
+                   snapshot="block", seed=t)
+    inp, Lp = case_inputs(cfg, split=bool((t // 2) % 2))
+    _q8_exact(lmc, inp, Lp, d, W.fill_normal_np(inp.layout.pool_bytes, 70 + t))
+    _blocks_exact(lmc, inp, Lp, "every", d=d)
+    if _block_units(inp, "tails"):
+        _blocks_exact(lmc, inp, Lp, "tails", d=d)
+
+
 def test_q8_block_objects_full_size_every_block(lmc):
     """The lognormal Kimi-Linear batch (packed, chunk 2N) as block objects of
     2 blocks with every snapshot an INT8 record (d = 128): sampled objects
