@@ -6,8 +6,9 @@
  * CPU-baseline leg load this file's library. The product library never links,
  * includes or calls it, and it shares no code with the product.
  *
- * Everything here is integer arithmetic and memcpy; there is no floating
- * point, so "correct" means byte-identical.
+ * Apart from the INT8 codec of the KDA recurrent state (IEEE binary32
+ * arithmetic, spelled out where it is defined), everything here is integer
+ * arithmetic and memcpy, so "correct" means byte-identical.
  *
  * Sources (page title, section):
  *   [KL]  "Kimi-Linear" (LMCache recipe): chunk size a multiple of N; the
@@ -20,7 +21,9 @@
  *         (path B), §4 the byte buffer and its per-layer views.
  *   [MC]  "When Prefix Cache Meets KDA" (Mooncake post), section "Flat KV":
  *         69 KDA layers split into three groups of 23, plus the
- *         full-attention group, on 24 physical slabs.
+ *         full-attention group, on 24 physical slabs; "Copy-on-Write" /
+ *         "Snapshot" (in-pool block copies); "Compressed Checkpoint Storage"
+ *         (per-channel INT8 recurrent state, conv window kept).
  *   [HM]  "Hybrid Attention Models" (LMCache docs), "Object-group
  *         separation": one object group per cross-chunk attention window.
  *
@@ -33,8 +36,9 @@
  *
  * Parity status: negotiation and layout sizes are pinned by values and
  * closed forms from the pages; store/load are pinned by invariants (identity,
- * untouched bytes) and by an independent per-token brute force. The byte
- * order inside an object is a reading, not a value from the pages.
+ * untouched bytes) and by an independent per-token brute force; the codec by
+ * worked rows and an independent float32 restatement. The byte order inside
+ * an object is a reading, not a value from the pages.
  */
 #include <math.h>
 #include <stdint.h>
