@@ -11,8 +11,9 @@
 // layer the state snapshot stored at the object's last block (or one per
 // block). A block copy moves every layer page of one KV group from a source
 // block to a destination block of the same pool. The cached pages are
-// byte-opaque, so this is pure data movement: every byte is read once from
-// HBM and written once.
+// byte-opaque, so store, load and copy are pure data movement: every byte is
+// read once from HBM and written once (the codec forms read and write each
+// byte once as well, turning the KDA state rows into INT8 records and back).
 //
 // GPU design. The work of one launch is a flat list of tiles (each at most
 // kTileBytes, 16-byte multiples, never crossing a page). Tile t resolves to
