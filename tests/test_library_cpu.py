@@ -353,3 +353,20 @@ def test_binding_refuses_memory_the_kernels_cannot_address(lmc):
         with pytest.raises(lmc.LmcError, match="CUDA tensor or pinned host memory") as e:
             call()
         assert e.value.code == lmc.LMC_ERR_INVALID_ARG
+
+
+def test_layout_too_small_for_one_block(lmc):
+    """Memory below one whole block of the layout: NO_MEMORY from the library
+    and the oracle alike (padded: S slabs of one page; packed: one stride)."""
+    cfg = W.CONFIGS[1]
+    for packed in (False, True):
+        big = oracle.layout(cfg.layers, cfg.N, packed, 1 << 40)
+        one = big.pool_bytes // big.num_blocks
+        for mem in (0, 1, one - 1):
+            with pytest.raises(lmc.LmcError) as e:
+                lmc.lmc_layout_build(cfg.layers, cfg.N, packed, mem)
+            assert e.value.code == lmc.LMC_ERR_NO_MEMORY
+            with pytest.raises(oracle.OracleError) as o:
+                oracle.layout(cfg.layers, cfg.N, packed, mem)
+            assert o.value.code == oracle.ERR_NO_MEMORY
+        assert lmc.lmc_layout_build(cfg.layers, cfg.N, packed, one).num_blocks == 1
