@@ -139,3 +139,17 @@ def test_store_load_from_c_match_oracle(tmp_path, cfg_index, ids):
     assert oracle.load(Lo, C, fresh_o, inp.tables_dst, inp.jobs, arena_o) == 0
     assert np.array_equal(np.fromfile(d / "arena.out", dtype=np.uint8), arena_o)
     assert np.array_equal(np.fromfile(d / "fresh.out", dtype=np.uint8), fresh_o)
+
+
+@pytest.mark.gpu
+def test_readme_python_example_runs():
+    """The Python example in README.md runs as written: a Kimi-Linear layout,
+    one request's two chunks stored into objects and loaded into other
+    blocks, a page checked."""
+    import re
+    text = open(os.path.join(ROOT, "README.md")).read()
+    block = re.search(r"```python\n(.*?)```", text, re.S).group(1)
+    scope = {}
+    exec(compile(block, "README.md", "exec"), scope)
+    assert scope["C"] == 944 and scope["L"].num_blocks == 64
+    assert int(scope["status"].item()) == 0
