@@ -63,7 +63,7 @@ int or_negotiate_chunk(int64_t requested, int64_t N, int strict, int64_t *out)
         *out = requested;
         return OR_OK;
     }
-    /* Smallest multiple of N that is >= requested; a minimum at or below
+    /* The least multiple of N not below `requested`; a minimum at or below
      * zero negotiates to N itself. */
     if (requested <= 0) {
         *out = N;

@@ -10,10 +10,10 @@
 // paged attention layer contributes the object's blocks, token-major, a KDA
 // layer the state snapshot stored at the object's last block (or one per
 // block). A block copy moves every layer page of one KV group from a source
-// block to a destination block of the same pool. The cached pages are
-// byte-opaque, so store, load and copy are pure data movement: every byte is
-// read once from HBM and written once (the codec forms read and write each
-// byte once as well, turning the KDA state rows into INT8 records and back).
+// block to a destination block of the same pool. Every page is handled as
+// opaque bytes: store, load and copy only move data, each byte read once from
+// HBM and written once (the codec forms also touch each byte once, turning
+// the KDA state rows into INT8 records and back).
 //
 // GPU design. The work of one launch is a flat list of tiles (each at most
 // kTileBytes, 16-byte multiples, never crossing a page). Tile t resolves to

@@ -48,7 +48,7 @@ def check_negotiation_golden(lib):
 
 
 def check_negotiation_bruteforce(lib):
-    # The smallest multiple of N that is >= the request, found by search.
+    # By search: the least multiple of N not below the request.
     for N in range(1, 41):
         for req in list(range(-3, 300)) + [997, 1000]:
             k = 1

@@ -117,8 +117,8 @@ def test_large_pages_exact(lmc):
 @pytest.mark.parametrize("packed", [False, True])
 def test_step_boundary_snapshots_exact(lmc, packed):
     """The >= 2N scheduler regime ("Kimi-Linear" recipe, Why these settings:
-    a step spans several blocks and only its last block gets a KDA
-    snapshot): with C = N and steps of 3 blocks, the KDA tables hold states
+    one scheduler step covers more than one block, and the KDA state is
+    saved only where the step ends): with C = N and steps of 3 blocks, the KDA tables hold states
     only at positions 3k + 2. With separate object groups the caller stores
     every chunk's MLA object and only the step-end chunks' KDA objects: exact
     against the oracle. A KDA object asked for at a chunk inside a step finds
