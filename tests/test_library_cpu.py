@@ -370,3 +370,16 @@ def test_layout_too_small_for_one_block(lmc):
                 oracle.layout(cfg.layers, cfg.N, packed, mem)
             assert o.value.code == oracle.ERR_NO_MEMORY
         assert lmc.lmc_layout_build(cfg.layers, cfg.N, packed, one).num_blocks == 1
+
+
+def test_every_declaration_is_documented():
+    """Each entry point of include/lmc.h comes with its comment block (the
+    passage it follows, arguments, layout, ownership, errors), alone or
+    shared with the declarations of its pair (store/load)."""
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lmc.h")).read()
+    names = []
+    for m in re.finditer(r"LMC_API [^;]*?\b(lmc_\w+)\s*\(", src):
+        before = src[:m.start()].rstrip()
+        assert before.endswith("*/") or re.search(r"LMC_API[^;]*;\s*$", before), m.group(1)
+        names.append(m.group(1))
+    assert len(names) >= 20
