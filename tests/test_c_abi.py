@@ -142,14 +142,10 @@ def test_store_load_from_c_match_oracle(tmp_path, cfg_index, ids):
 
 
 @pytest.mark.gpu
-def test_readme_python_example_runs():
-    """The Python example in README.md runs as written: a Kimi-Linear layout,
-    one request's two chunks stored into objects and loaded into other
-    blocks, a page checked."""
-    import re
-    text = open(os.path.join(ROOT, "README.md")).read()
-    block = re.search(r"```python\n(.*?)```", text, re.S).group(1)
-    scope = {}
-    exec(compile(block, "README.md", "exec"), scope)
-    assert scope["C"] == 944 and scope["L"].num_blocks == 64
-    assert int(scope["status"].item()) == 0
+def test_python_usage_example_runs():
+    """The usage example (tests/example_usage.py, also printed in the README)
+    runs as written: a Kimi-Linear layout, one request's two chunks stored
+    into objects and loaded into other blocks, a page checked."""
+    import example_usage
+    out = example_usage.run("cuda")
+    assert out == {"C": 944, "num_blocks": 64, "status": 0}

@@ -88,6 +88,22 @@ def test_layout_rejects_bad_specs_like_oracle(lmc):
     assert ep.value.code == lmc.LMC_ERR_INVALID_ARG
 
 
+def test_negotiation_golden_values(lmc):
+    """The library itself against the negotiation values of tests/golden
+    (the pages' chunk sizes, plus requests of 0 and -1: non-strict rises to
+    N, strict refuses with INVALID_ARG)."""
+    names = {lmc.LMC_ERR_NOT_MULTIPLE: "ERR_NOT_MULTIPLE", lmc.LMC_ERR_INVALID_ARG: "ERR_INVALID_ARG"}
+    n = 0
+    for req, N, strict, exp in P._rows("negotiation.txt"):
+        try:
+            got = str(lmc.lmc_negotiate_chunk(int(req), int(N), bool(int(strict))))
+        except lmc.LmcError as e:
+            got = names.get(e.code, str(e.code))
+        assert got == exp, (req, N, strict, got, exp)
+        n += 1
+    assert n >= 17
+
+
 def test_negotiation_and_budget_match_oracle(lmc):
     for N in list(range(1, 50)) + [768, 944, 1888, 12288]:
         for req in list(range(-2, 200)) + [1500, 12287, 12288, 12289, 2**62]:
