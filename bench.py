@@ -285,35 +285,6 @@ def split_parts(jobs, object_bytes, parts):
     return out
 
 
-def touched_blocks(layout, tables, jobs, m):
-    """Block ids (over all KV groups) whose pages a set of chunk jobs reads or
-    writes: for job (request r, chunk c) and each layer of its object group,
-    positions c*m .. c*m+m-1 of a paged layer's KV group, or position
-    (c+1)*m-1 of a KDA layer's (the chunk-end snapshot)."""
-    out = []
-    for og, J in enumerate(jobs):
-        if len(J) == 0:
-            continue
-        r = J["request"].astype(np.int64)[:, None]
-        c = J["chunk"].astype(np.int64)[:, None]
-        groups = {(layout.kv_group[i], layout.kinds[i] == "KDA")
-                  for i in range(len(layout.kinds)) if layout.object_group[i] == og}
-        for k, kda in sorted(groups):
-            pos = (c + 1) * m - 1 if kda else c * m + np.arange(m)[None, :]
-            out.append(np.asarray(tables[k])[r, pos].ravel())
-    blocks = np.unique(np.concatenate(out)) if out else np.zeros(0, dtype=np.int32)
-    return blocks[blocks >= 0]
-
-
-def check_disjoint(layout, tables, load_jobs, store_jobs, m):
-    """The mixed step runs its load and its store concurrently on one pool:
-    refuses a batch in which they would touch a common block."""
-    common = np.intersect1d(touched_blocks(layout, tables, load_jobs, m),
-                            touched_blocks(layout, tables, store_jobs, m))
-    if common.size:
-        raise RuntimeError(f"mixed step: load and store share {common.size} block(s), e.g. {common[:4].tolist()}")
-
-
 class PagingStep:
     """Device inputs and one step of the hot path for a workload.
 
@@ -359,7 +330,11 @@ class PagingStep:
         self.status = T.zeros(1, dtype=T.int32, device=dev)
         self.t_src = [T.from_numpy(t).to(dev) for t in inp.tables_src]
         if cfg.mixed:
-            check_disjoint(L, inp.tables_src, inp.load_jobs, inp.store_jobs, C // cfg.N)
+            # the load and the store run concurrently on one pool: refuse a
+            # batch in which they would touch a common block
+            common = lmc.lmc_check_disjoint(L, C, inp.tables_src, inp.load_jobs, inp.tables_src, inp.store_jobs)
+            if common >= 0:
+                raise RuntimeError(f"mixed step: load and store share block {common}")
             sizes = inp.object_bytes
             self.load_payload = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.load_jobs))
             self.store_payload = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.store_jobs))
@@ -590,7 +565,7 @@ class CopyStep:
     def step(self, ev=None):
         if ev is not None:
             ev[0].record(self.main)
-        self.lmc.lmc_copy_blocks(self.L, self.pool, self.pairs, self.status, self.main)
+        self.lmc.lmc_copy_blocks(self.L, self.pool, self.pairs, self.h_pairs, self.status, self.main)
         if ev is not None:
             ev[1].record(self.main)
             ev[2].record(self.main)

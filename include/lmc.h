@@ -63,6 +63,8 @@ extern "C" {
 #define LMC_ERR_CUDA (-5)         /* a CUDA runtime call failed */
 #define LMC_ERR_OVERFLOW (-6)     /* a size does not fit 64-bit arithmetic */
 #define LMC_ERR_BUDGET (-7)       /* scheduler budget outside the allowed range */
+#define LMC_ERR_OVERLAP (-8)      /* copies that would race: a block written twice, or
+                                     written by one copy and read by another */
 
 /* ---- device status bits (OR-ed into *status) ----------------------------- */
 #define LMC_ST_BLOCK_OOR 0x1u   /* block id < -1 or >= num_blocks */
@@ -307,6 +309,11 @@ typedef struct {
     const lmc_block_pair *const *pairs; /* host array [num_kv_groups] of device
                                            pointers (NULL allowed when the count is 0) */
     const int64_t *num_pairs;         /* host array [num_kv_groups] */
+    const lmc_block_pair *const *host_pairs; /* host array [num_kv_groups] of HOST
+                                           pointers to the same pairs as `pairs`
+                                           (the copy the caller built them from;
+                                           NULL allowed when the count is 0): the
+                                           call checks the pairs on them */
 } lmc_copy_batch;
 
 /* In-pool copies ([MC] "Copy-on-Write": a hit's shared KDA checkpoint is
@@ -316,11 +323,31 @@ typedef struct {
  * from block src_block to block dst_block of `pool` (padding untouched).
  * A request's whole KDA state is one pair per KDA KV group. Pairs naming -1
  * raise LMC_ST_NO_BLOCK, ids outside [0, num_blocks) LMC_ST_BLOCK_OOR; such
- * pairs are skipped. Destination blocks must be distinct and must not be the
- * source of another pair of the same call (they would race); src == dst is
- * a no-op. Asynchronous on `stream`; errors INVALID_ARG, ALIGN, CUDA. */
+ * pairs are skipped. The pairs of one call run concurrently, so the call
+ * checks, on `host_pairs` and before anything is enqueued, that among the
+ * pairs it will copy no block is the destination of two pairs or the
+ * destination of one and the source of another, across all KV groups (a
+ * block id names the same block in every group): LMC_ERR_OVERLAP otherwise,
+ * and nothing is copied. The device pairs must equal the host pairs (the
+ * kernels read the device copy). Asynchronous on `stream`; errors
+ * INVALID_ARG (host_pairs missing), OVERLAP, ALIGN, CUDA. */
 LMC_API int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy_batch *batch, uint32_t *status,
                     void *stream);
+
+/* Guard for a mixed serving step ([HM] object groups; [VB] §5.3 a hit's state
+ * becomes the initial state): a load of cached chunks and a store of new
+ * chunks issued at the same time on one pool race unless they touch disjoint
+ * blocks. Given two chunk-form batches whose block tables and jobs are in
+ * HOST memory (the copies the caller built them from), computes the blocks
+ * each one's objects read or write, exactly as lmc_store / lmc_load address
+ * them (a paged layer's m = chunk_size / N positions of the chunk, a KDA
+ * layer's chunk-end position; entries the kernels would skip touch nothing),
+ * and returns LMC_OK when no block is touched by both, else LMC_ERR_OVERLAP
+ * with *out_block (if not NULL) = the smallest shared block id (-1 when
+ * disjoint). Errors: INVALID_ARG, NOT_MULTIPLE, OVERFLOW. Host only; nothing
+ * enqueued. */
+LMC_API int lmc_check_disjoint(const lmc_layout *layout, int64_t chunk_size, const lmc_batch *a, const lmc_batch *b,
+                               int32_t *out_block);
 
 /* ---- INT8 per-channel codec of the KDA recurrent state ------------------- */
 

@@ -40,6 +40,7 @@ ERR_NOT_MULTIPLE = -3
 ERR_NO_MEMORY = -4
 ERR_OVERFLOW = -6
 ERR_BUDGET = -7
+ERR_OVERLAP = -8
 
 ST_BLOCK_OOR = 0x1
 ST_NO_BLOCK = 0x2
@@ -163,6 +164,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.or_check_backends.argtypes = [P(_Layout), ctypes.c_int, ctypes.c_int]
     lib.or_check_backends.restype = ctypes.c_uint32
     lib.or_copy_blocks.argtypes = [P(_Layout), ctypes.c_void_p, P(_CopyBatch), P(ctypes.c_uint32)]
+    lib.or_check_disjoint.argtypes = [P(_Layout), ctypes.c_int64, P(_Tables), P(_Jobs), P(_Tables), P(_Jobs),
+                                      P(ctypes.c_int32)]
     for name in ("or_store_q8", "or_load_q8"):
         getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, P(_Tables),
                                        P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
@@ -468,6 +471,21 @@ def copy_blocks(L: Layout, pool: np.ndarray, pairs) -> int:
     if rc != OK:
         raise OracleError(rc, "copy_blocks")
     return st.value
+
+
+def check_disjoint(L: Layout, C: int, tables_a, jobs_a, tables_b, jobs_b) -> int:
+    """-1 when the chunk batches (tables_a, jobs_a) and (tables_b, jobs_b)
+    touch disjoint blocks, else the smallest block both touch."""
+    Ta, Ja, keep_a = _marshal(L, tables_a, jobs_a)
+    Tb, Jb, keep_b = _marshal(L, tables_b, jobs_b)
+    out = ctypes.c_int32(0)
+    rc = L._lib.or_check_disjoint(ctypes.byref(L._c), int(C), ctypes.byref(Ta), ctypes.byref(Ja), ctypes.byref(Tb),
+                                  ctypes.byref(Jb), ctypes.byref(out))
+    if rc == ERR_OVERLAP:
+        return out.value
+    if rc != OK:
+        raise OracleError(rc, "check_disjoint")
+    return -1
 
 
 def list_pages(L: Layout, C: int, tables, jobs, arena_bytes: int, nb: int = 0, kda_every: bool = False):

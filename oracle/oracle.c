@@ -42,6 +42,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "oracle.h"
@@ -821,6 +822,41 @@ int64_t or_object_bytes_blocks_q8(const or_layout *L, int64_t nb, int kda_every,
  * spare buffer). For every pair of KV group g, each layer of g gets the real
  * bytes of block src copied to block dst. A pair naming -1 or a block outside
  * the pool is skipped and raises its bit. */
+static int block_in_pool(const or_layout *L, int64_t b)
+{
+    return b >= 0 && b < L->num_blocks;
+}
+
+/* The pairs of one copy call are applied together, not one after another
+ * ([MC] "Copy-on-Write": each hit gets its own private slot; "Snapshot":
+ * each running state its own spare buffer), so a call is well defined only
+ * if no block it writes is written again or read by another of its pairs.
+ * A block id names one block for every KV group (the groups' pages of block
+ * b share memory in both layouts), so pairs of different groups are
+ * compared too. Pairs with an id outside the pool copy nothing and take no
+ * part. Returns 1 when two pairs collide. */
+static int copies_collide(const or_layout *L, const or_copy_batch *B)
+{
+    for (int g = 0; g < L->num_kv_groups; g++) {
+        for (int64_t q = 0; q < B->num_pairs[g]; q++) {
+            const or_pair *p = &B->pairs[g][q];
+            if (!block_in_pool(L, p->src_block) || !block_in_pool(L, p->dst_block))
+                continue;
+            for (int h = 0; h < L->num_kv_groups; h++) {
+                for (int64_t t = 0; t < B->num_pairs[h]; t++) {
+                    const or_pair *o = &B->pairs[h][t];
+                    if ((h == g && t == q) || !block_in_pool(L, o->src_block) ||
+                        !block_in_pool(L, o->dst_block))
+                        continue;
+                    if (p->dst_block == o->dst_block || p->dst_block == o->src_block)
+                        return 1;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
 int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, uint32_t *status)
 {
     if (L == NULL || pool == NULL || B == NULL || status == NULL ||
@@ -830,6 +866,8 @@ int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, ui
         if (B->num_pairs[g] < 0 || (B->num_pairs[g] > 0 && B->pairs[g] == NULL))
             return OR_ERR_INVALID_ARG;
     }
+    if (copies_collide(L, B))
+        return OR_ERR_OVERLAP;
     for (int g = 0; g < L->num_kv_groups; g++) {
         for (int64_t q = 0; q < B->num_pairs[g]; q++) {
             int64_t src = B->pairs[g][q].src_block;
@@ -851,6 +889,76 @@ int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, ui
         }
     }
     return OR_OK;
+}
+
+/* Sets `bit` in map[b] for every block b whose pages the chunk objects of a
+ * batch read (store) or write (load): per job of object group og and per
+ * layer of og, the chunk's C / N positions of a paged layer's block table,
+ * or the chunk-end position of a KDA layer's ([KL] snapshots at block
+ * boundaries). A job naming no request of the batch or a negative chunk,
+ * a position past the table, and an id outside the pool mark nothing. */
+static int mark_blocks(const or_layout *L, int64_t m, const or_tables *T, const or_jobs *J,
+                       uint8_t *map, uint8_t bit)
+{
+    int rc = check_tables(L, T);
+    if (rc != OR_OK)
+        return rc;
+    if (J == NULL || J->num_object_groups != L->num_object_groups)
+        return OR_ERR_INVALID_ARG;
+    for (int og = 0; og < L->num_object_groups; og++) {
+        if (J->num_jobs[og] < 0 || (J->num_jobs[og] > 0 && J->jobs[og] == NULL))
+            return OR_ERR_INVALID_ARG;
+        for (int64_t q = 0; q < J->num_jobs[og]; q++) {
+            int64_t r = J->jobs[og][q].request;
+            int64_t c = J->jobs[og][q].chunk;
+            if (r < 0 || r >= T->num_requests || c < 0)
+                continue;
+            for (int i = 0; i < L->num_layers; i++) {
+                if (L->object_group[i] != og)
+                    continue;
+                int k = L->kv_group[i];
+                int64_t lo = c * m, hi = c * m + m; /* positions [lo, hi) */
+                if (L->layers[i].kind == OR_KDA)
+                    lo = hi - 1;
+                for (int64_t pos = lo; pos < hi && pos < T->num_cols[k]; pos++) {
+                    int64_t b = T->table[k][r * T->row_stride[k] + pos];
+                    if (block_in_pool(L, b))
+                        map[b] |= bit;
+                }
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* A load and a store issued at the same time on one pool (the mixed
+ * serving step) must touch disjoint blocks. *out_block = the smallest block
+ * both touch, or -1. */
+int or_check_disjoint(const or_layout *L, int64_t C, const or_tables *Ta, const or_jobs *Ja,
+                      const or_tables *Tb, const or_jobs *Jb, int32_t *out_block)
+{
+    if (L == NULL || out_block == NULL)
+        return OR_ERR_INVALID_ARG;
+    if (C <= 0 || C % L->N != 0)
+        return OR_ERR_NOT_MULTIPLE;
+    uint8_t *map = calloc((size_t)L->num_blocks + 1, 1);
+    if (map == NULL)
+        return OR_ERR_INVALID_ARG;
+    int rc = mark_blocks(L, C / L->N, Ta, Ja, map, 1);
+    if (rc == OR_OK)
+        rc = mark_blocks(L, C / L->N, Tb, Jb, map, 2);
+    *out_block = -1;
+    if (rc == OR_OK) {
+        for (int64_t b = 0; b < L->num_blocks; b++) {
+            if (map[b] == 3) {
+                *out_block = (int32_t)b;
+                rc = OR_ERR_OVERLAP;
+                break;
+            }
+        }
+    }
+    free(map);
+    return rc;
 }
 
 /* Smallest multiple of `align` tokens whose attention page

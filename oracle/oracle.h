@@ -17,6 +17,7 @@
 #define OR_ERR_NO_MEMORY (-4)
 #define OR_ERR_OVERFLOW (-6)
 #define OR_ERR_BUDGET (-7)
+#define OR_ERR_OVERLAP (-8)
 
 /* Status bits raised by a store or load; the offending page is skipped. */
 #define OR_ST_BLOCK_OOR 0x1u   /* block id outside [0, num_blocks), not -1 */
@@ -144,6 +145,8 @@ typedef struct {
 } or_copy_batch;
 
 int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, uint32_t *status);
+int or_check_disjoint(const or_layout *L, int64_t C, const or_tables *Ta, const or_jobs *Ja,
+                      const or_tables *Tb, const or_jobs *Jb, int32_t *out_block);
 
 int or_store_q8(const or_layout *L, int64_t C, int64_t d, const uint8_t *pool,
                 const or_tables *T, const or_jobs *J,

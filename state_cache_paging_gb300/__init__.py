@@ -33,6 +33,7 @@ LMC_ERR_NO_MEMORY = -4
 LMC_ERR_CUDA = -5
 LMC_ERR_OVERFLOW = -6
 LMC_ERR_BUDGET = -7
+LMC_ERR_OVERLAP = -8
 
 LMC_ST_BLOCK_OOR = 0x1
 LMC_ST_NO_BLOCK = 0x2
@@ -97,7 +98,8 @@ class lmc_block_table(ctypes.Structure):
 
 class lmc_copy_batch(ctypes.Structure):
     _fields_ = [("num_kv_groups", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("pairs", ctypes.POINTER(ctypes.c_void_p)), ("num_pairs", ctypes.POINTER(ctypes.c_int64))]
+                ("pairs", ctypes.POINTER(ctypes.c_void_p)), ("num_pairs", ctypes.POINTER(ctypes.c_int64)),
+                ("host_pairs", ctypes.POINTER(ctypes.c_void_p))]
 
 
 class lmc_batch(ctypes.Structure):
@@ -131,6 +133,7 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
                                       ctypes.c_void_p, _i64, ctypes.c_void_p, ctypes.c_void_p]
     so.lmc_copy_blocks.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(lmc_copy_batch), ctypes.c_void_p,
                                    ctypes.c_void_p]
+    so.lmc_check_disjoint.argtypes = [ctypes.c_void_p, _i64, _P(lmc_batch), _P(lmc_batch), _P(ctypes.c_int32)]
     for name in ("lmc_store_q8", "lmc_load_q8"):
         getattr(so, name).argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
                                       _i64, ctypes.c_void_p, ctypes.c_void_p]
@@ -470,25 +473,73 @@ def pairs_to_device(pairs: np.ndarray, device):
     return torch.from_numpy(a.view(np.uint8).copy()).to(device)
 
 
-def lmc_copy_blocks(layout: Layout, pool, pairs, status, stream=None) -> None:
+def lmc_copy_blocks(layout: Layout, pool, pairs, host_pairs, status, stream=None) -> None:
     """In-pool copies: `pairs[g]` (device tensor of 8-byte lmc_block_pair
-    records) lists (src, dst) blocks of KV group g."""
+    records) lists (src, dst) blocks of KV group g; `host_pairs[g]` is the
+    same list as a PAIR_DTYPE numpy array, on which the library checks that
+    the copies do not race (LmcError LMC_ERR_OVERLAP otherwise)."""
     _check_launch(layout, pool, None, status)
     g = layout.num_kv_groups
-    if len(pairs) != g:
-        raise LmcError(LMC_ERR_INVALID_ARG, f"{g} pair arrays expected, got {len(pairs)}")
+    if len(pairs) != g or len(host_pairs) != g:
+        raise LmcError(LMC_ERR_INVALID_ARG, f"{g} pair arrays expected, got {len(pairs)} and {len(host_pairs)}")
     parr = (ctypes.c_void_p * max(g, 1))()
+    harr = (ctypes.c_void_p * max(g, 1))()
     narr = (_i64 * max(g, 1))()
-    for k, p in enumerate(pairs):
+    keep = []
+    for k, (p, h) in enumerate(zip(pairs, host_pairs)):
         _visible("pair array", p)
         nbytes = p.numel() * p.element_size()
         if nbytes % 8 or not p.is_contiguous():
             raise LmcError(LMC_ERR_INVALID_ARG, "pair arrays hold contiguous 8-byte lmc_block_pair records")
+        h = np.ascontiguousarray(h, dtype=PAIR_DTYPE)
+        if h.nbytes != nbytes:
+            raise LmcError(LMC_ERR_INVALID_ARG, "host and device pair arrays differ in length")
+        keep.append(h)
         parr[k] = p.data_ptr() if nbytes else None
+        harr[k] = h.ctypes.data if nbytes else None
         narr[k] = nbytes // 8
-    b = lmc_copy_batch(g, 0, parr, narr)
+    b = lmc_copy_batch(g, 0, parr, narr, harr)
     _check(_lib.lmc_copy_blocks(layout.handle, pool.data_ptr(), ctypes.byref(b), status.data_ptr(),
                                 _stream_ptr(stream)), "lmc_copy_blocks")
+
+
+def _host_batch(layout: Layout, tables, jobs):
+    """An lmc_batch over HOST numpy arrays (int32 block tables, JOB_DTYPE jobs)."""
+    g = layout.num_kv_groups
+    if len(tables) != g or len(jobs) != layout.num_object_groups:
+        raise LmcError(LMC_ERR_INVALID_ARG, "one block table per KV group and one job array per object group")
+    keep = []
+    nreq = int(tables[0].shape[0]) if g else 0
+    tarr = (lmc_block_table * max(g, 1))()
+    for k, t in enumerate(tables):
+        t = np.ascontiguousarray(t, dtype=np.int32)
+        if t.ndim != 2 or t.shape[0] != nreq:
+            raise LmcError(LMC_ERR_INVALID_ARG, "block tables must be int32 [num_requests, cols]")
+        keep.append(t)
+        tarr[k] = lmc_block_table(t.ctypes.data, int(t.shape[1]), int(t.shape[1]))
+    o = layout.num_object_groups
+    jarr = (ctypes.c_void_p * max(o, 1))()
+    narr = (_i64 * max(o, 1))()
+    for q, j in enumerate(jobs):
+        j = np.ascontiguousarray(j, dtype=JOB_DTYPE)
+        keep.append(j)
+        jarr[q] = j.ctypes.data if j.size else None
+        narr[q] = j.size
+    return lmc_batch(nreq, g, tarr, o, 0, jarr, narr), (keep, tarr, jarr, narr)
+
+
+def lmc_check_disjoint(layout: Layout, chunk: int, tables_a, jobs_a, tables_b, jobs_b) -> int:
+    """Host check for two chunk batches run at the same time on one pool
+    (numpy block tables and JOB_DTYPE jobs): -1 when the blocks their
+    objects touch are disjoint, else the smallest block both touch."""
+    a, keep_a = _host_batch(layout, tables_a, jobs_a)
+    b, keep_b = _host_batch(layout, tables_b, jobs_b)
+    out = ctypes.c_int32(0)
+    rc = _lib.lmc_check_disjoint(layout.handle, int(chunk), ctypes.byref(a), ctypes.byref(b), ctypes.byref(out))
+    if rc == LMC_ERR_OVERLAP:
+        return out.value
+    _check(rc, "lmc_check_disjoint")
+    return -1
 
 
 __all__ = [n for n in dir() if n.startswith(("lmc_", "LMC_"))] + ["Layout", "LmcError", "JOB_DTYPE",

@@ -1,7 +1,7 @@
 """Builds liblmc.so in-tree for sm_103a (nvcc + g++, no cmake).
 
 Usage: ``python state_cache_paging_gb300/build.py [--force] [-v]`` (run by
-path: importing the package itself requires the built library). The two translation units
+path: importing the package itself requires the built library). The translation units
 compile in parallel; the CUDA runtime is linked statically, so the library
 loads without torch and shares the primary context with whatever else runs
 in the process.
@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(PKG, "liblmc.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
+HOST_UNITS = ("layout", "checks")  # host C++ translation units in csrc/
 CXX = os.environ.get("CXX", "g++")
 
 
@@ -51,14 +52,14 @@ def build_library(force: bool = False, extra_nvcc=(), out_path: str | None = Non
     os.makedirs(BUILD_DIR, exist_ok=True)
     work = tempfile.mkdtemp(dir=BUILD_DIR)  # private per build (builds may run concurrently)
     cu_obj = os.path.join(work, "paging.o")
-    cpp_obj = os.path.join(work, "layout.o")
+    cpp_objs = [os.path.join(work, name + ".o") for name in HOST_UNITS]
     ptxas_log = os.path.join(BUILD_DIR, "ptxas.log")
     cmds = [
         [NVCC, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xptxas", "-v", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC, *extra_nvcc, "-c", os.path.join(CSRC, "paging.cu"), "-o", cu_obj],
-        [CXX, "-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE,
-         "-I", CSRC,
-         "-c", os.path.join(CSRC, "layout.cpp"), "-o", cpp_obj],
+        *[[CXX, "-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE,
+           "-I", CSRC, "-c", os.path.join(CSRC, name + ".cpp"), "-o", obj]
+          for name, obj in zip(HOST_UNITS, cpp_objs)],
     ]
     procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True) for c in cmds]
     logs = [p.communicate()[0] for p in procs]
@@ -71,7 +72,7 @@ def build_library(force: bool = False, extra_nvcc=(), out_path: str | None = Non
         print(logs[0])
     tmp = os.path.join(work, "liblmc.so")
     link = [NVCC, "-shared", *ARCH, "-Xlinker", "--version-script=" + os.path.join(CSRC, "liblmc.map"),
-            "-o", tmp, cu_obj, cpp_obj]
+            "-o", tmp, cu_obj, *cpp_objs]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout}{r.stderr}")

@@ -341,6 +341,7 @@ extern "C" const char *lmc_strerror(int code) {
     case LMC_ERR_CUDA: return "LMC_ERR_CUDA: a CUDA runtime call failed";
     case LMC_ERR_OVERFLOW: return "LMC_ERR_OVERFLOW: size overflows 64-bit arithmetic";
     case LMC_ERR_BUDGET: return "LMC_ERR_BUDGET: scheduler budget outside [N, 2N) (>= 2N needs separate object groups)";
+    case LMC_ERR_OVERLAP: return "LMC_ERR_OVERLAP: copies would race (a block written twice, or written and read)";
     default: return "LMC_ERR_UNKNOWN: unknown status code";
     }
 }

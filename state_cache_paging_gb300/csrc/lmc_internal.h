@@ -30,4 +30,12 @@ namespace lmc {
 inline bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
 inline bool add_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_add_overflow(a, b, out); }
 
+// The rule lmc_copy_blocks checks on the host copy of its pairs before any
+// launch: among the pairs whose two block ids lie in the pool, no block is
+// the destination of two pairs, nor the destination of one pair and the
+// source of another (KV groups share block ids). LMC_OK or LMC_ERR_OVERLAP
+// (LMC_ERR_INVALID_ARG when the host pairs are missing). The batch's group
+// count and pair counts are checked by the caller.
+int check_copy_pairs(const lmc_layout *L, const lmc_copy_batch *b);
+
 }  // namespace lmc

@@ -67,7 +67,7 @@
 
 namespace {
 
-constexpr int kMaxEntries = LMC_MAX_LAYERS;  // layer entries in one launch
+constexpr int kMaxEntries = 2 * LMC_MAX_LAYERS;  // layer entries in one launch (a codec KDA layer takes two)
 constexpr int kMaxGroups = 64;               // object groups (or KV groups) in one launch
 constexpr int kMaxKv = 64;                   // KV groups (block tables)
 constexpr int kTileBytes = LMC_TILE_BYTES;
@@ -82,21 +82,26 @@ static_assert(kEngine != 1 || kBulkCtasPerSm * (kBulkStages * kTileBytes + 1024)
 enum Mode : int32_t { kStore = 0, kLoad = 1, kCopy = 2 };
 
 // One layer's run of pages inside an object (or inside a copied block).
+// A codec entry (INT8 record of a KDA recurrent state) counts rows instead
+// of bytes: seg_bytes holds the page's state rows, tile_bytes the rows per
+// tile, and pool_base points past the conv bytes, at the state itself.
 struct Entry {
     int64_t pool_base;    // pool byte offset of block 0's page
     int64_t pool_stride;  // bytes between consecutive blocks' pages
     int64_t obj_off;      // byte offset of the layer's first page in the object
-    int32_t seg_bytes;    // real bytes of one page (codec: the conv bytes before the state)
+    int32_t seg_bytes;    // real bytes of one page
     int32_t tile_bytes;   // bytes per tile of this page (last tile shorter)
     int32_t tiles_per_seg;
     int32_t tile_start;   // tiles of earlier layers in the object
-    int32_t pos_add;      // block position = first + pos_add + page index
-    int16_t kv;           // KV group (block table)
+    int32_t obj_stride;   // bytes between the object's consecutive pages of this entry
+    uint8_t kv;           // KV group (block table)
     uint8_t kda;          // 1: a KDA state page (a missing one is NO_SNAPSHOT)
     uint8_t codec;        // 1: INT8 record of the recurrent state (see below)
-    int32_t rows;         // codec: state rows of the page; tile_bytes holds rows per tile
-    int32_t obj_stride;   // bytes between the object's consecutive pages of this entry
+    uint8_t last;         // 1: only the object's last block position (block position =
+                          // first + Plan::last_pos + page index; else first + page index)
 };
+static_assert(sizeof(Entry) == 48, "launch plan entry layout");
+static_assert(kMaxKv <= 256, "KV group index held in one byte");
 
 struct Group {
     const void *items;   // lmc_job[] (store/load) or lmc_block_pair[] (copy)
@@ -126,8 +131,8 @@ struct Plan {
     int32_t num_requests;
     int32_t num_groups;
     int32_t mode;
-    int32_t q8_row;  // codec: values per recurrent-state row (0: no codec)
-    int32_t pad;
+    int32_t q8_row;    // codec: values per recurrent-state row (0: no codec)
+    int32_t last_pos;  // block positions per object - 1 (the `last` entries' position offset)
     Group groups[kMaxGroups];
     Table tables[kMaxKv];
     Entry entries[kMaxEntries];
@@ -259,7 +264,7 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
         (job.offset & 15) != 0 || job.offset > P.arena_bytes - G.obj_bytes)
         return LMC_ST_BAD_JOB;
     const Table &T = P.tables[E.kv];
-    const int64_t pos = (int64_t)job.chunk * P.pos_mul + E.pos_add + j;
+    const int64_t pos = (int64_t)job.chunk * P.pos_mul + (E.last ? P.last_pos : 0) + j;
     if (pos >= T.num_cols)
         return LMC_ST_BAD_JOB;
     const int32_t block = __ldg(T.ptr + (int64_t)job.request * T.row_stride + pos);
@@ -269,15 +274,14 @@ __device__ __forceinline__ uint32_t resolve(const Plan &P, int64_t tile, Span &s
         return LMC_ST_BLOCK_OOR;
 
     if (kCodec && E.codec) {
-        // rows [k * R, k * R + n) of the page's recurrent state, which starts
-        // after the conv bytes (seg_bytes); the entry's j-th record part, at
-        // obj_off + j * obj_stride, holds all the rows' scales, then the codes
-        const int64_t row0 = (int64_t)k * E.tile_bytes;
-        const int32_t n = min(E.tile_bytes, (int32_t)(E.rows - row0));
-        const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + E.seg_bytes + row0 * 4 * P.q8_row;
+        // rows [row0, row0 + s.bytes) of the page's recurrent state (pool_base
+        // already points past the conv bytes; seg_bytes counts the rows); the
+        // entry's j-th record part, at obj_off + j * obj_stride, holds all the
+        // rows' scales, then the codes
+        const int64_t row0 = piece;
+        const int64_t page = E.pool_base + (int64_t)block * E.pool_stride + row0 * 4 * P.q8_row;
         const int64_t rec = job.offset + E.obj_off + (int64_t)j * E.obj_stride;
-        const int64_t codes = rec + 4 * (int64_t)E.rows + row0 * P.q8_row;
-        s.bytes = n;
+        const int64_t codes = rec + 4 * (int64_t)E.seg_bytes + row0 * P.q8_row;
         if (P.mode == kStore) {
             s.codec = 1;
             s.src = P.src_base + page;
@@ -950,7 +954,7 @@ bool aligned16(int64_t x) { return (x & 15) == 0; }
 // to back from the object's current offset `obj`, which advances past them;
 // with rec_stride > 0 page j lies at obj + j * rec_stride instead (the page
 // part of interleaved records) and the caller advances obj.
-int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t pos_add, int64_t &obj,
+int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, bool last, int64_t &obj,
               int64_t &tiles, bool &vec, int64_t rec_stride = 0) {
     if (ne >= kMaxEntries)
         return LMC_ERR_INVALID_ARG;
@@ -970,8 +974,9 @@ int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t 
     E.tiles_per_seg = (seg + tb - 1) / tb;
     E.tile_start = (int32_t)tiles;
     E.kda = d.kind == LMC_LAYER_KDA;
-    E.pos_add = pos_add;
-    E.kv = (int16_t)d.kv_group;
+    E.codec = 0;
+    E.last = last;
+    E.kv = (uint8_t)d.kv_group;
     E.obj_stride = rec_stride > 0 ? (int32_t)rec_stride : seg;
     int64_t add;
     if (rec_stride > INT32_MAX || (rec_stride == 0 && (!lmc::mul_ok(pages, seg, &add) || !lmc::add_ok(obj, add, &obj))))
@@ -987,7 +992,7 @@ int add_entry(Plan &P, int &ne, const lmc_layer_desc &d, int64_t pages, int32_t 
 // object, the recurrent state after the conv bytes, encoded as the scales
 // then the codes of an INT8 record at obj_off + j * rec_stride.
 int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_spec &spec, int64_t pages,
-                    int32_t pos_add, int64_t obj_off, int64_t rec_stride, int64_t &tiles, bool &vec) {
+                    bool last, int64_t obj_off, int64_t rec_stride, int64_t &tiles, bool &vec) {
     if (ne >= kMaxEntries)
         return LMC_ERR_INVALID_ARG;
     const int64_t row = P.q8_row;
@@ -998,19 +1003,18 @@ int add_codec_entry(Plan &P, int &ne, const lmc_layer_desc &d, const lmc_layer_s
     // on a 16-byte boundary
     const int32_t per_tile = (int32_t)std::max<int64_t>(4, kQ8TileBytes / (4 * row) / 4 * 4);
     Entry &E = P.entries[ne++];
-    E.pool_base = d.base;
+    E.pool_base = d.base + spec.conv_bytes;  // the state starts after the conv bytes
     E.pool_stride = d.stride;
     E.obj_off = obj_off;
     E.obj_stride = (int32_t)rec_stride;
-    E.seg_bytes = (int32_t)spec.conv_bytes;  // the state starts after the conv bytes
+    E.seg_bytes = (int32_t)rows;  // a codec entry counts rows
     E.tile_bytes = per_tile;
-    E.rows = (int32_t)rows;
     E.tiles_per_seg = (int32_t)((rows + per_tile - 1) / per_tile);
     E.tile_start = (int32_t)tiles;
     E.kda = 1;
     E.codec = 1;
-    E.pos_add = pos_add;
-    E.kv = (int16_t)d.kv_group;
+    E.last = last;
+    E.kv = (uint8_t)d.kv_group;
     tiles += pages * E.tiles_per_seg;
     // the rows are read and written as 16-byte vectors
     vec = vec && aligned16(d.base) && aligned16(d.stride) && aligned16(spec.conv_bytes);
@@ -1065,6 +1069,7 @@ int build_object_plan(const lmc_layout *L, const Shape &sh, const void *pool, co
 
     std::memset(&P, 0, sizeof(P));
     P.pos_mul = sh.pos_mul;
+    P.last_pos = (int32_t)(sh.nb - 1);
     P.q8_row = sh.q8_row;
     P.num_requests = b->num_requests;
     P.num_blocks = L->num_blocks;
@@ -1099,20 +1104,18 @@ int build_object_plan(const lmc_layout *L, const Shape &sh, const void *pool, co
                 // window as is, then the state's scales and codes
                 const lmc_layer_spec &spec = L->specs[i];
                 const int64_t pages = last_only ? 1 : sh.nb;
-                const int32_t pos_add = last_only ? (int32_t)(sh.nb - 1) : 0;
                 const int64_t rows = spec.rec_bytes / (4 * (int64_t)sh.q8_row);
                 const int64_t record = spec.conv_bytes + 4 * rows + rows * (int64_t)sh.q8_row;
                 lmc_layer_desc conv = d;
                 conv.real_bytes = spec.conv_bytes;
                 int64_t at = obj, add = 0;
-                rc = conv.real_bytes > 0 ? add_entry(P, ne, conv, pages, pos_add, at, tiles, vec, record) : LMC_OK;
+                rc = conv.real_bytes > 0 ? add_entry(P, ne, conv, pages, last_only, at, tiles, vec, record) : LMC_OK;
                 if (rc == LMC_OK)
-                    rc = add_codec_entry(P, ne, d, spec, pages, pos_add, obj + spec.conv_bytes, record, tiles, vec);
+                    rc = add_codec_entry(P, ne, d, spec, pages, last_only, obj + spec.conv_bytes, record, tiles, vec);
                 if (rc == LMC_OK && (!lmc::mul_ok(pages, record, &add) || !lmc::add_ok(obj, add, &obj)))
                     rc = LMC_ERR_OVERFLOW;
             } else {
-                rc = add_entry(P, ne, d, last_only ? 1 : sh.nb, last_only ? (int32_t)(sh.nb - 1) : 0, obj, tiles,
-                               vec);
+                rc = add_entry(P, ne, d, last_only ? 1 : sh.nb, last_only, obj, tiles, vec);
             }
             if (rc != LMC_OK)
                 return rc;
@@ -1295,6 +1298,12 @@ extern "C" int lmc_copy_blocks(const lmc_layout *L, void *pool, const lmc_copy_b
     const int nkv = (int)L->kv_group_kind.size();
     if (b->num_kv_groups != nkv || nkv > kMaxGroups || b->pairs == nullptr || b->num_pairs == nullptr)
         return LMC_ERR_INVALID_ARG;
+    for (int g = 0; g < nkv; g++)
+        if (b->num_pairs[g] < 0 || (b->num_pairs[g] > 0 && b->pairs[g] == nullptr))
+            return LMC_ERR_INVALID_ARG;
+    // the pairs run concurrently: refuse a batch whose copies would race
+    if (const int rc = lmc::check_copy_pairs(L, b); rc != LMC_OK)
+        return rc;
     Plan P;
     std::memset(&P, 0, sizeof(P));
     P.num_blocks = L->num_blocks;
@@ -1314,7 +1323,7 @@ extern "C" int lmc_copy_blocks(const lmc_layout *L, void *pool, const lmc_copy_b
         for (size_t i = 0; i < L->desc.size(); i++) {
             if (L->desc[i].kv_group != g)
                 continue;
-            const int rc = add_entry(P, ne, L->desc[i], 1, 0, obj, tiles, vec);
+            const int rc = add_entry(P, ne, L->desc[i], 1, false, obj, tiles, vec);
             if (rc != LMC_OK)
                 return rc;
         }

@@ -775,9 +775,142 @@ def check_backends(lib):
     assert L.check_backends(False, False) == 0
 
 
+def _brute_copies(B, pool, pairs, order):
+    """The pairs applied by the brute force one after another ("forward",
+    "reverse"), or all read before any is written ("together")."""
+    out = pool.copy()
+    if order == "together":
+        for g, P in enumerate(pairs):
+            for p in P:
+                for i in B.groups[g]:
+                    B.view(out, i)[int(p["dst_block"])] = B.view(pool, i)[int(p["src_block"])]
+        return out
+    seq = [(g, p) for g, P in enumerate(pairs) for p in P]
+    for g, p in (seq if order == "forward" else seq[::-1]):
+        brute.copy_blocks(B, out, [P if k == g else P[:0] for k, P in enumerate(pairs[:g])] +
+                          [np.array([p], dtype=oracle.PAIR_DTYPE)] + [P[:0] for P in pairs[g + 1:]])
+    return out
+
+
+def check_copy_collisions(lib):
+    """The pairs of one copy call run at the same time ("When Prefix Cache
+    Meets KDA", Copy-on-Write: each hit its own private slot; Snapshot: each
+    state its own spare buffer). Against the brute force: whenever the
+    oracle accepts a batch, applying its pairs in any order (forward,
+    reverse, all reads first) gives the oracle's result; whenever two orders
+    give different pools, the oracle refuses the batch (OVERLAP) and writes
+    nothing. Batches draw ids from a few blocks so collisions are common,
+    across KV groups too (equal block ids share memory)."""
+    rng = np.random.default_rng(29)
+    refused = accepted = 0
+    for t in range(80):
+        spec = random_spec(rng, int(rng.integers(2, 7)))
+        N = int(rng.choice([2, 4]))
+        try:
+            L = oracle.layout(spec, N, bool(t % 2), int(rng.integers(4000, 20000)), split_groups=bool(t % 3),
+                              _lib=lib)
+        except oracle.OracleError:
+            continue
+        if L.num_blocks < 3:
+            continue
+        B = brute.BruteLayout(spec, N, L.packed, L.pool_bytes, bool(t % 3))
+        pool = W.fill_normal_np(L.pool_bytes, 100 + t)
+        span = int(rng.integers(3, min(L.num_blocks, 8) + 1))
+        pairs = []
+        for g in range(L.num_kv_groups):
+            k = int(rng.integers(0, 3))
+            pairs.append(np.array([(int(rng.integers(0, span)), int(rng.integers(0, span))) for _ in range(k)],
+                                  dtype=oracle.PAIR_DTYPE).reshape(-1))
+        results = [_brute_copies(B, pool, pairs, o) for o in ("forward", "reverse", "together")]
+        out = pool.copy()
+        try:
+            assert oracle.copy_blocks(L, out, pairs) == 0
+        except oracle.OracleError as e:
+            assert e.code == oracle.ERR_OVERLAP, e.code
+            assert np.array_equal(out, pool), "a refused batch must copy nothing"
+            refused += 1
+            continue
+        accepted += 1
+        for r in results:
+            assert np.array_equal(out, r), "an accepted batch depends on the order of its pairs"
+    assert refused >= 10 and accepted >= 10, (refused, accepted)
+    # order-dependent batches, planted: two pairs writing one block, a pair
+    # writing a block another reads (in another KV group)
+    L = oracle.layout(W.CONFIGS[0].layers, 64, False, 64 * 73_728, _lib=lib)
+    B = brute.BruteLayout(W.CONFIGS[0].layers, 64, False, L.pool_bytes)
+    pool = W.fill_normal_np(L.pool_bytes, 3)
+    e0 = np.zeros(0, dtype=oracle.PAIR_DTYPE)
+    for pairs in ([np.array([(1, 9), (2, 9)], dtype=oracle.PAIR_DTYPE), e0, e0, e0],
+                  [np.array([(1, 9)], dtype=oracle.PAIR_DTYPE), e0, np.array([(9, 12)], dtype=oracle.PAIR_DTYPE), e0]):
+        fw, rv = _brute_copies(B, pool, pairs, "forward"), _brute_copies(B, pool, pairs, "reverse")
+        assert not np.array_equal(fw, rv)
+        try:
+            oracle.copy_blocks(L, pool.copy(), pairs)
+            raise AssertionError("an order-dependent batch was accepted")
+        except oracle.OracleError as e:
+            assert e.code == oracle.ERR_OVERLAP
+
+
+def _tagged_pool(B):
+    """Every 4-byte word of every page of block b holds b (all layers)."""
+    pool = np.full(B.pool_bytes, 0xEE, dtype=np.uint8)
+    for i in range(len(B.spec)):
+        v = B.view(pool, i)
+        for b in range(B.num_blocks):
+            v[b] = np.full(v[b].size // 4, b, dtype=np.int32).view(np.uint8).reshape(v[b].shape)
+    return pool
+
+
+def check_disjoint(lib):
+    """The mixed step's guard against the brute force: on a pool whose pages
+    are tagged with their block id, the blocks a chunk batch touches are the
+    tags its objects pick up when the brute force stores them; the oracle's
+    smallest common block of the load and the store side must be the
+    smallest common tag (-1 when none), on the mixed workload's structure
+    (KDA x3, SWA, MLA; chunk = 2N) and with shared blocks planted."""
+    layers = []
+    for _ in range(2):
+        layers += [{"kind": "KDA", "token_bytes": 0, "conv_bytes": 16, "rec_bytes": 64, "window": 0}] * 3
+        layers += [W.swa(16, 12), W.mla(16)]
+    cfg = W.Config(600, "mixed-small", layers, N=4, requested_chunk=8, packed=True, num_requests=8,
+                   lengths="fixed", fixed_lengths=(40, 23, 57, 31, 64, 17, 12, 48), snapshot="block", seed=6,
+                   mixed=True)
+    C = oracle.negotiate_chunk(8, 4, _lib=lib)
+    inp = W.make_inputs(cfg, lambda mem: oracle.layout(layers, 4, True, mem, _lib=lib), C)
+    L = inp.layout
+    B = brute.BruteLayout(layers, 4, True, L.pool_bytes)
+    pool = _tagged_pool(B)
+
+    def tags(tables, jobs, nbytes):
+        arena = np.full(nbytes, 0xFF, dtype=np.uint8)
+        brute.store(B, C, pool, tables, jobs, arena)
+        ids = np.unique(arena.view(np.int32))
+        return set(int(x) for x in ids if x >= 0)
+
+    rng = np.random.default_rng(6)
+    store_side = sorted(tags(inp.tables_src, inp.store_jobs, inp.store_arena_bytes))
+    seen_shared = 0
+    for t in range(40):
+        tables = [x.copy() for x in inp.tables_src]
+        lj = [j.copy() for j in inp.load_jobs]
+        if t > 0:
+            # point one table entry at a block the store side reads (or at
+            # any block): shared only if the load side uses that entry
+            k = int(rng.integers(0, len(tables)))
+            r, c = np.argwhere(tables[k] >= 0)[int(rng.integers(0, int((tables[k] >= 0).sum())))]
+            pick = store_side if t % 3 else range(L.num_blocks)
+            tables[k][r, c] = int(pick[int(rng.integers(0, len(pick)))])
+        common = tags(tables, lj, inp.load_arena_bytes) & tags(tables, inp.store_jobs, inp.store_arena_bytes)
+        want = min(common) if common else -1
+        seen_shared += want >= 0
+        assert oracle.check_disjoint(L, C, tables, lj, tables, inp.store_jobs) == want, (t, want)
+    assert seen_shared >= 5
+
+
 ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",
        "check_budget", "check_page_formulas", "check_unified_block_size", "check_k3_groups", "check_closed_forms",
        "check_non_overlap", "check_store_load_cases", "check_block_objects", "check_copy_blocks",
+       "check_copy_collisions", "check_disjoint",
        "check_q8_golden", "check_q8_random", "check_q8_objects", "check_q8_block_objects", "check_backends"]
 
 

@@ -39,50 +39,22 @@ def test_split_parts_cover_jobs_once(cfg_index, ids, parts):
         assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
 
 
-def test_mixed_step_load_and_store_blocks_are_disjoint():
+def test_mixed_step_load_and_store_blocks_are_disjoint(lmc):
     """The mixed workload's load (cached chunks) and store (new chunks) touch
-    disjoint blocks, so the two streams never race; a batch whose store
-    repeats a loaded chunk is refused before any launch."""
+    disjoint blocks, so the two streams never race (the library's guard the
+    benchmark calls); a batch whose store repeats a loaded chunk shares a
+    block."""
     cfg = W.CONFIGS[4]
     C = oracle.negotiate_chunk(cfg.requested_chunk, cfg.N)
     inp = W.make_inputs(cfg, functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed), C, list(range(40)))
-    m = C // cfg.N
-    L = inp.layout
-    lb = bench.touched_blocks(L, inp.tables_src, inp.load_jobs, m)
-    sb = bench.touched_blocks(L, inp.tables_src, inp.store_jobs, m)
-    assert lb.size and sb.size and np.intersect1d(lb, sb).size == 0
-    bench.check_disjoint(L, inp.tables_src, inp.load_jobs, inp.store_jobs, m)
-    # the same chunk in both sets: refused
+    L = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, inp.layout.pool_bytes)
+    T = inp.tables_src
+    assert sum(len(j) for j in inp.load_jobs) and sum(len(j) for j in inp.store_jobs)
+    assert lmc.lmc_check_disjoint(L, C, T, inp.load_jobs, T, inp.store_jobs) == -1
     bad = [J.copy() for J in inp.store_jobs]
     g = next(g for g, J in enumerate(inp.load_jobs) if len(J))
     bad[g] = np.concatenate([bad[g], inp.load_jobs[g][:1]])
-    with pytest.raises(RuntimeError, match="share"):
-        bench.check_disjoint(L, inp.tables_src, inp.load_jobs, bad, m)
-
-
-def test_touched_blocks_by_hand():
-    """Positions read per job: a paged layer's m blocks of the chunk, a KDA
-    layer's last block of the chunk (tiny workload, chunk = 2 blocks)."""
-    cfg = W.CONFIGS[0]
-    C = oracle.negotiate_chunk(cfg.requested_chunk, cfg.N)
-    inp = W.make_inputs(cfg, functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed), C)
-    L = inp.layout
-    m = C // cfg.N
-    assert m == 2
-    one = [J[:0] for J in inp.jobs]
-    g_kda = L.object_group[L.kinds.index("KDA")]
-    g_mla = L.object_group[L.kinds.index("MLA")]
-    J = inp.jobs[g_kda][:1].copy()
-    J["request"], J["chunk"] = 1, 1
-    one[g_kda] = J
-    want = sorted(int(inp.tables_src[L.kv_group[i]][1][3]) for i in range(len(L.kinds)) if L.kinds[i] == "KDA")
-    assert bench.touched_blocks(L, inp.tables_src, one, m).tolist() == sorted(set(want))
-    one = [J[:0] for J in inp.jobs]
-    J = inp.jobs[g_mla][:1].copy()
-    J["request"], J["chunk"] = 0, 0
-    one[g_mla] = J
-    k = L.kv_group[L.kinds.index("MLA")]
-    assert bench.touched_blocks(L, inp.tables_src, one, m).tolist() == sorted(int(x) for x in inp.tables_src[k][0][:2])
+    assert lmc.lmc_check_disjoint(L, C, T, inp.load_jobs, T, bad) >= 0
 
 
 def test_reference_arm_prints_the_contract_line():

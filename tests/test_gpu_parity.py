@@ -622,7 +622,7 @@ def test_copy_blocks_exact(lmc, t):
     pool_h = W.fill_normal_np(o.pool_bytes, t)
     pool = torch.from_numpy(pool_h).to(DEV)
     st = _status()
-    lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], st)
+    lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], pairs, st)
     torch.cuda.synchronize()
     st_o = oracle.copy_blocks(o, pool_h, pairs)
     assert int(st.item()) == st_o
@@ -649,7 +649,7 @@ def test_copy_blocks_full_size_kda_states(lmc):
     W.fill_normal(pool, 91)
     before = pool.clone()
     st = _status()
-    lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], st)
+    lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], pairs, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     # every destination page holds its source page; every other byte is unchanged
@@ -958,7 +958,7 @@ def test_odd_page_sizes_blocks_and_copies_exact(lmc):
     pool_h = W.fill_normal_np(o.pool_bytes, 78)
     pool = torch.from_numpy(pool_h).to(DEV)
     st = _status()
-    lmc.lmc_copy_blocks(Lp, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], st)
+    lmc.lmc_copy_blocks(Lp, pool, [lmc.pairs_to_device(x, DEV) for x in pairs], pairs, st)
     torch.cuda.synchronize()
     assert int(st.item()) == oracle.copy_blocks(o, pool_h, pairs) == 0
     assert np.array_equal(pool.cpu().numpy(), pool_h)
@@ -1217,3 +1217,17 @@ def test_maximum_layout_exact(lmc):
     assert Lp.num_layers == 256 and Lp.num_kv_groups == 64 and Lp.num_object_groups == 64
     _full_exact(lmc, inp, Lp)
     _blocks_exact(lmc, inp, Lp, "every")
+
+
+def test_maximum_kda_layout_q8_exact(lmc):
+    """256 KDA layers (the layer limit) through the INT8 codec: every KDA
+    layer takes two launch-plan entries (its conv window and its state
+    rows), 512 in one launch. Chunk and every-block forms, exact against the
+    oracle."""
+    kda = {"kind": "KDA", "token_bytes": 0, "conv_bytes": 32, "rec_bytes": 8 * 16 * 4, "window": 0}
+    cfg = W.Config(501, "max-kda", [dict(kda) for _ in range(256)], N=4, requested_chunk=8, packed=True,
+                   num_requests=3, lengths="fixed", fixed_lengths=(40, 23, 57), seed=12)
+    inp, Lp = case_inputs(cfg, split=False)
+    assert Lp.num_layers == 256 and Lp.num_object_groups == 1
+    _q8_exact(lmc, inp, Lp, 16, W.fill_normal_np(inp.layout.pool_bytes, 12))
+    _blocks_exact(lmc, inp, Lp, "every", d=16)

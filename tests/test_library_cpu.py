@@ -201,14 +201,127 @@ def test_copy_blocks_host_checks(lmc):
     pairs = (ctypes.c_void_p * g)(*[None] * g)
     counts = (ctypes.c_int64 * g)(*[0] * g)
     f = lmc._lib.lmc_copy_blocks
-    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts)), addr, None) == lmc.LMC_OK
-    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g - 1, 0, pairs, counts)), addr, None) \
+    B = lambda n=g: ctypes.byref(lmc.lmc_copy_batch(n, 0, pairs, counts, pairs))
+    assert f(L.handle, addr, B(), addr, None) == lmc.LMC_OK
+    assert f(L.handle, addr, B(g - 1), addr, None) == lmc.LMC_ERR_INVALID_ARG
+    assert f(L.handle, addr, B(), addr + 2, None) == lmc.LMC_ERR_ALIGN
+    # the host copy of the pairs is required
+    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts, None)), addr, None) \
         == lmc.LMC_ERR_INVALID_ARG
-    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts)), addr + 2, None) \
-        == lmc.LMC_ERR_ALIGN
     counts[1] = 3  # pairs given as NULL with a non-zero count
-    assert f(L.handle, addr, ctypes.byref(lmc.lmc_copy_batch(g, 0, pairs, counts)), addr, None) \
-        == lmc.LMC_ERR_INVALID_ARG
+    assert f(L.handle, addr, B(), addr, None) == lmc.LMC_ERR_INVALID_ARG
+
+
+def _copy_batch_code(lmc, L, host_pairs):
+    """The library's return code for copies given only on the host. The pool
+    pointer is NULL, so a batch that passes the overlap rule is refused with
+    INVALID_ARG just before the launch: nothing is ever launched."""
+    g = L.num_kv_groups
+    keep = [np.ascontiguousarray(p, dtype=lmc.PAIR_DTYPE) for p in host_pairs]
+    harr = (ctypes.c_void_p * g)(*[p.ctypes.data if p.size else None for p in keep])
+    counts = (ctypes.c_int64 * g)(*[p.size for p in keep])
+    buf = (ctypes.c_uint8 * 64)()
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+    return lmc._lib.lmc_copy_blocks(L.handle, None, ctypes.byref(lmc.lmc_copy_batch(g, 0, harr, counts, harr)),
+                                    addr, None)
+
+
+def _racing_pairs(rng, L):
+    """A random batch of pairs with one planted collision: a destination
+    repeated, or a destination that is another pair's source (possibly in
+    another KV group)."""
+    nb, g = L.num_blocks, L.num_kv_groups
+    ids = rng.permutation(nb)
+    n = int(rng.integers(2, max(3, min(12, nb // 2))))
+    src, dst = ids[:n], ids[n:2 * n]
+    pairs = [np.array([(s, d)], dtype=oracle.PAIR_DTYPE) for s, d in zip(src, dst)]
+    i, j = rng.choice(n, 2, replace=False)
+    if rng.random() < 0.5:
+        pairs[j]["dst_block"] = pairs[i]["dst_block"]
+    else:
+        pairs[j]["dst_block"] = pairs[i]["src_block"]
+    groups = [[] for _ in range(g)]
+    for p in pairs:
+        groups[int(rng.integers(0, g))].append(p)
+    return [np.concatenate(x) if x else np.zeros(0, dtype=oracle.PAIR_DTYPE) for x in groups]
+
+
+def test_copy_blocks_refuse_racing_pairs_like_the_oracle(lmc):
+    """Copies of one call run concurrently: a destination named twice, or a
+    destination that another pair reads, is refused before launch by the
+    library and by the oracle alike, with nothing copied by the oracle."""
+    rng = np.random.default_rng(23)
+    for t in range(60):
+        spec = P.random_spec(rng, int(rng.integers(1, 9)))
+        N = int(rng.integers(1, 40))
+        packed = bool(t % 2)
+        o = oracle.layout(spec, N, packed, int(rng.integers(1, 4)) << 20)
+        p = lmc.lmc_layout_build(spec, N, packed, int(o.pool_bytes))
+        if o.num_blocks < 4:
+            continue
+        pairs = _racing_pairs(rng, o)
+        pool = np.zeros(o.pool_bytes, dtype=np.uint8)
+        with pytest.raises(oracle.OracleError) as e:
+            oracle.copy_blocks(o, pool, pairs)
+        assert e.value.code == oracle.ERR_OVERLAP
+        assert not pool.any()
+        assert _copy_batch_code(lmc, p, pairs) == lmc.LMC_ERR_OVERLAP
+    # src == dst alone is allowed; a pair writing what a no-op pair reads is not
+    o = oracle.layout(W.CONFIGS[0].layers, 64, False, 1 << 22)
+    p = lmc.lmc_layout_build(W.CONFIGS[0].layers, 64, False, 1 << 22)
+    g = o.num_kv_groups
+    same = [np.array([(3, 3)], dtype=oracle.PAIR_DTYPE)] + [np.zeros(0, dtype=oracle.PAIR_DTYPE)] * (g - 1)
+    assert oracle.copy_blocks(o, np.zeros(o.pool_bytes, np.uint8), same) == 0
+    assert _copy_batch_code(lmc, p, same) == lmc.LMC_ERR_INVALID_ARG  # passed the rule; NULL pool refused
+    clash = [np.array([(3, 3), (5, 3)], dtype=oracle.PAIR_DTYPE)] + [np.zeros(0, dtype=oracle.PAIR_DTYPE)] * (g - 1)
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(o, np.zeros(o.pool_bytes, np.uint8), clash)
+    assert _copy_batch_code(lmc, p, clash) == lmc.LMC_ERR_OVERLAP
+    # ids outside the pool copy nothing and take no part in the rule
+    skipped = [np.array([(-1, 7), (7, o.num_blocks), (2, 7)], dtype=oracle.PAIR_DTYPE)] + \
+        [np.zeros(0, dtype=oracle.PAIR_DTYPE)] * (g - 1)
+    assert oracle.copy_blocks(o, np.zeros(o.pool_bytes, np.uint8), skipped) == \
+        oracle.ST_NO_BLOCK | oracle.ST_BLOCK_OOR
+
+
+def test_check_disjoint_matches_oracle(lmc):
+    """The mixed step's guard: the block sets two chunk batches touch, by the
+    library and by the oracle, on the mixed workload (disjoint by
+    construction) and on batches with planted shared blocks."""
+    cfg = W.CONFIGS[4]
+    C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
+    import functools
+    inp = W.make_inputs(cfg, functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed), C, list(range(40)))
+    o = inp.layout
+    p = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, o.pool_bytes)
+    T = inp.tables_src
+    assert oracle.check_disjoint(o, C, T, inp.load_jobs, T, inp.store_jobs) == -1
+    assert lmc.lmc_check_disjoint(p, C, T, inp.load_jobs, T, inp.store_jobs) == -1
+    # a batch against itself shares its smallest block
+    both = oracle.check_disjoint(o, C, T, inp.store_jobs, T, inp.store_jobs)
+    assert both >= 0 and lmc.lmc_check_disjoint(p, C, T, inp.store_jobs, T, inp.store_jobs) == both
+    rng = np.random.default_rng(31)
+    for t in range(30):
+        # plant: one load job moved onto a store job's (request, chunk), or a
+        # table entry of the load side pointed at a block the store reads
+        lj = [j.copy() for j in inp.load_jobs]
+        tables = [x.copy() for x in T]
+        og = int(rng.integers(0, len(lj)))
+        sj = inp.store_jobs[og]
+        if len(lj[og]) and len(sj) and rng.random() < 0.5:
+            k = int(rng.integers(0, len(lj[og])))
+            s = sj[int(rng.integers(0, len(sj)))]
+            lj[og][k]["request"], lj[og][k]["chunk"] = s["request"], s["chunk"]
+        else:
+            k = int(rng.integers(0, len(tables)))
+            used = tables[k][tables[k] >= 0]
+            r, c = np.argwhere(tables[k] >= 0)[int(rng.integers(0, used.size))]
+            tables[k][r, c] = int(rng.integers(0, o.num_blocks))
+        a = oracle.check_disjoint(o, C, tables, lj, tables, inp.store_jobs)
+        assert lmc.lmc_check_disjoint(p, C, tables, lj, tables, inp.store_jobs) == a, t
+    with pytest.raises(lmc.LmcError) as e:
+        lmc.lmc_check_disjoint(p, C + 1, T, inp.load_jobs, T, inp.store_jobs)
+    assert e.value.code == lmc.LMC_ERR_NOT_MULTIPLE
 
 
 @pytest.mark.parametrize("cfg_index", [0, 1, 3])
@@ -365,7 +478,7 @@ def test_binding_refuses_memory_the_kernels_cannot_address(lmc):
                  lambda: lmc.lmc_load(L, C, pool, tables, jobs, arena, status),
                  lambda: lmc.lmc_store_q8(L, C, 64, pool, tables, jobs, arena, status),
                  lambda: lmc.lmc_copy_blocks(L, pool, [torch.zeros(0, dtype=torch.uint8)] * L.num_kv_groups,
-                                             status)):
+                                             [np.zeros(0, dtype=lmc.PAIR_DTYPE)] * L.num_kv_groups, status)):
         with pytest.raises(lmc.LmcError, match="CUDA tensor or pinned host memory") as e:
             call()
         assert e.value.code == lmc.LMC_ERR_INVALID_ARG

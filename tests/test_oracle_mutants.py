@@ -57,6 +57,14 @@ MUTANTS = [
     ("every-block INT8 records advance by the raw page",
      "cursor += sh->q8_row > 0 ? q8_record_bytes(&L->layers[i], sh->q8_row)\n                                                 : L->real_bytes[i];",
      "cursor += L->real_bytes[i];"),
+    ("copies may write a block another pair reads",
+     "p->dst_block == o->dst_block || p->dst_block == o->src_block", "p->dst_block == o->dst_block"),
+    ("copies may write one block twice",
+     "p->dst_block == o->dst_block || p->dst_block == o->src_block", "p->dst_block == o->src_block"),
+    ("copy collisions looked for only inside a KV group", "if ((h == g && t == q) ||", "if (h != g || t == q ||"),
+    ("disjoint check marks a KDA layer's first position", "lo = hi - 1;", "lo = lo + 0;"),
+    ("disjoint check drops a chunk's last paged position", "pos < hi && pos < T->num_cols[k]",
+     "pos < hi - 1 + (L->layers[i].kind == OR_KDA) && pos < T->num_cols[k]"),
 ]
 
 
