@@ -1,5 +1,6 @@
 """Helpers for the GPU parity tests: device inputs for a workload, calls
-through the C ABI, and oracle checks that scale to full-size workloads.
+through the C ABI, and oracle checks that scale to full-size workloads
+(every object and every loaded page compared, streamed in slices).
 
 Inputs come from the seeded generators (workloads/) using the ORACLE's
 layout; the library's layout is asserted equal before anything runs, so the
@@ -9,6 +10,7 @@ the oracle.
 from __future__ import annotations
 
 import functools
+import mmap
 
 import numpy as np
 import torch
@@ -56,61 +58,119 @@ def object_span(inp, og, job):
     return off, off + int(inp.object_bytes[og])
 
 
-def pick_jobs(jobs, per_group, rng):
-    out = []
-    for J in jobs:
-        k = min(per_group, len(J))
-        idx = np.sort(rng.choice(len(J), size=k, replace=False)) if k else np.zeros(0, dtype=np.int64)
-        out.append(J[idx])
+# ---------------------------------------------------------------------------
+# Full-size comparison with the oracle, streamed in arena-ordered slices so
+# the host holds a few GB whatever the pool's size
+# ---------------------------------------------------------------------------
+
+SLICE_BYTES = 2 << 30
+ARENA_FILL = 0x3C  # arenas start filled with this byte on both sides
+
+
+class LazyHost:
+    """n bytes of private anonymous host memory standing for a pool on the
+    oracle's side: a page costs memory only once written, and release()
+    hands every page back (all bytes read as zero again)."""
+
+    def __init__(self, n):
+        self.n = int(n)
+        self._map = mmap.mmap(-1, max(self.n, 1), flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        self.a = np.frombuffer(self._map, dtype=np.uint8, count=self.n)
+
+    def release(self):
+        self._map.madvise(mmap.MADV_DONTNEED)
+
+
+def fetch(dev_buf, lo, hi, out=None):
+    """Device bytes [lo, hi) copied into `out` (a numpy view) or a new array."""
+    if out is None:
+        out = np.empty(hi - lo, dtype=np.uint8)
+    torch.from_numpy(out).copy_(dev_buf[lo:hi])
     return out
 
 
-def _fetch(dev_buf, lo, hi):
-    return dev_buf[lo:hi].cpu().numpy()
+def job_slices(jobs, sizes, limit=None):
+    """Every job of every object group in arena order, cut into runs whose
+    objects span at most ~limit bytes (default SLICE_BYTES): yields
+    (per-group job subsets, lo, hi) where [lo, hi) is the run's arena range."""
+    limit = SLICE_BYTES if limit is None else limit
+    order = sorted((int(j["offset"]), g, k) for g, J in enumerate(jobs) for k, j in enumerate(J))
+    start = 0
+    while start < len(order):
+        lo = order[start][0]
+        end = start
+        hi = lo
+        while end < len(order):
+            off, g, _ = order[end]
+            stop = off + int(sizes[g])
+            if end > start and stop - lo > limit:
+                break
+            hi = max(hi, stop)
+            end += 1
+        picks = [[] for _ in jobs]
+        for _, g, k in order[start:end]:
+            picks[g].append(k)
+        yield [J[np.array(p, dtype=np.int64)] for J, p in zip(jobs, picks)], lo, hi
+        start = end
 
 
-def check_store_sampled(inp, pool_dev, arena_dev, jobs, tables, arena_bytes, per_group, rng):
-    """The oracle recomputes a sample of objects from the pages it names and
-    the bytes are compared with the library's objects."""
-    Lo, C = inp.layout, inp.C
-    sel = pick_jobs(jobs, per_group, rng)
-    pages, st = oracle.list_pages(Lo, C, tables, sel, arena_bytes)
-    assert st == 0
-    host_pool = np.zeros(Lo.pool_bytes, dtype=np.uint8)  # pages mapped lazily
-    for pg in pages:
-        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
-        host_pool[lo:lo + n] = _fetch(pool_dev, lo, lo + n)
-    arena_o = np.zeros(arena_bytes, dtype=np.uint8)
-    assert oracle.store(Lo, C, host_pool, tables, sel, arena_o) == 0
-    n_checked = 0
-    for og, J in enumerate(sel):
-        for job in J:
-            lo, hi = object_span(inp, og, job)
-            assert np.array_equal(_fetch(arena_dev, lo, hi), arena_o[lo:hi]), (og, job)
-            n_checked += hi - lo
-    return n_checked
+def _rebased(sel, lo):
+    out = []
+    for J in sel:
+        J = J.copy()
+        J["offset"] -= lo
+        out.append(J)
+    return out
 
 
-def check_load_sampled(inp, pool_dev, arena_dev, jobs, tables, arena_bytes, per_group, rng):
-    """The oracle scatters a sample of objects; every page it writes is
-    compared with the library's pool."""
-    Lo, C = inp.layout, inp.C
-    sel = pick_jobs(jobs, per_group, rng)
-    host_arena = np.zeros(arena_bytes, dtype=np.uint8)
-    for og, J in enumerate(sel):
-        for job in J:
-            lo, hi = object_span(inp, og, job)
-            host_arena[lo:hi] = _fetch(arena_dev, lo, hi)
-    host_pool = np.zeros(Lo.pool_bytes, dtype=np.uint8)
-    assert oracle.load(Lo, C, host_pool, tables, sel, host_arena) == 0
-    pages, st = oracle.list_pages(Lo, C, tables, sel, arena_bytes)
-    assert st == 0
-    n_checked = 0
-    for pg in pages:
-        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
-        assert np.array_equal(_fetch(pool_dev, lo, lo + n), host_pool[lo:lo + n]), pg
-        n_checked += n
-    return n_checked
+def _first_diff(got, want, base):
+    bad = np.flatnonzero(got != want)
+    return f"{bad.size} bytes differ, first at {base + int(bad[0])}"
+
+
+def check_store_streamed(Lo, C, pool_dev, arena_dev, jobs, sizes, tables, oracle_store, nb=0, kda_every=False,
+                         fill=ARENA_FILL):
+    """Every object of `jobs` is recomputed by the oracle (oracle_store(pool,
+    tables, jobs, arena) -> status) from the pool pages it reads, fetched from
+    the device, and compared byte for byte with the device arena (filled with
+    `fill` before the store, like the oracle's). Returns the object bytes
+    compared, which a test sets against the full payload."""
+    host = LazyHost(Lo.pool_bytes)
+    checked = 0
+    for sel, lo, hi in job_slices(jobs, sizes):
+        pages, st = oracle.list_pages(Lo, C, tables, sel, 1 << 62, nb=nb, kda_every=kda_every)
+        assert st == 0
+        for po, n in zip(pages["pool_offset"].tolist(), pages["bytes"].tolist()):
+            fetch(pool_dev, po, po + n, host.a[po:po + n])
+        want = np.full(hi - lo, fill, dtype=np.uint8)
+        assert oracle_store(host.a, tables, _rebased(sel, lo), want) == 0
+        got = fetch(arena_dev, lo, hi)
+        if not np.array_equal(got, want):
+            raise AssertionError("store: " + _first_diff(got, want, lo))
+        checked += sum(int(sizes[g]) * len(J) for g, J in enumerate(sel))
+        host.release()
+    return checked
+
+
+def check_load_streamed(Lo, C, dest_dev, arena_dev, jobs, sizes, tables, oracle_load, nb=0, kda_every=False):
+    """The oracle (oracle_load(pool, tables, jobs, arena) -> status) scatters
+    every object of `jobs`, read from the device arena, and every page it
+    writes is compared byte for byte with the device pool. Returns the page
+    bytes compared."""
+    host = LazyHost(Lo.pool_bytes)
+    checked = 0
+    for sel, lo, hi in job_slices(jobs, sizes):
+        src = fetch(arena_dev, lo, hi)
+        assert oracle_load(host.a, tables, _rebased(sel, lo), src) == 0
+        pages, st = oracle.list_pages(Lo, C, tables, sel, 1 << 62, nb=nb, kda_every=kda_every)
+        assert st == 0
+        for po, n in zip(pages["pool_offset"].tolist(), pages["bytes"].tolist()):
+            got = fetch(dest_dev, po, po + n)
+            if not np.array_equal(got, host.a[po:po + n]):
+                raise AssertionError("load: " + _first_diff(got, host.a[po:po + n], po))
+            checked += n
+        host.release()
+    return checked
 
 
 def check_untouched(inp, pool_dev, jobs, tables, arena_bytes, fill_value):

@@ -2,9 +2,10 @@
 
 Small cases (the tiny workload, random specs, every error path) are compared
 in full. The full-size workloads run in the launch configuration the
-benchmark times and are checked on oracle-recomputed samples plus properties
-that hold at any size (store after load reproduces the objects; pool bytes
-outside the addressed pages stay untouched).
+benchmark times, and every object and every loaded page is compared with the
+oracle too, streamed through host memory in slices (each test asserts that
+the bytes compared equal the full payload of each direction); pool bytes
+outside the addressed pages are checked untouched on the device.
 """
 import ctypes
 
@@ -15,8 +16,8 @@ import torch
 import oracle
 import oracle_pins as P
 import workloads as W
-from gpu_harness import (case_inputs, check_load_sampled, check_store_sampled, check_untouched,
-                         dev_jobs, dev_tables)
+from gpu_harness import (ARENA_FILL, LazyHost, case_inputs, check_load_streamed, check_store_streamed,
+                         check_untouched, dev_jobs, dev_tables, fetch)
 
 pytestmark = pytest.mark.gpu
 
@@ -263,14 +264,18 @@ def test_object_at_arena_end(lmc):
     assert int(st.item()) == 0 and np.array_equal(arena.cpu().numpy(), arena_o)
 
 
-def _full_size(lmc, cfg, request_ids=None, per_group=12):
-    """Full-size store + load in the benchmark's launch configuration."""
+def _oracle_calls(Lo, C):
+    return (lambda p, t, j, a: oracle.store(Lo, C, p, t, j, a)), (lambda p, t, j, a: oracle.load(Lo, C, p, t, j, a))
+
+
+def _full_size(lmc, cfg, request_ids=None):
+    """Full-size store + load in the benchmark's launch configuration, every
+    byte of both directions compared with the oracle."""
     inp, Lp = case_inputs(cfg, request_ids)
     Lo, C = inp.layout, inp.C
-    rng = np.random.default_rng(cfg.seed)
     pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
     W.fill_normal(pool, cfg.seed)
-    arena = torch.empty(inp.arena_bytes, dtype=torch.uint8, device=DEV)
+    arena = torch.full((inp.arena_bytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
     fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
     st = _status()
     t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
@@ -279,15 +284,14 @@ def _full_size(lmc, cfg, request_ids=None, per_group=12):
     lmc.lmc_load(Lp, C, fresh, t_dst, jobs, arena, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert check_store_sampled(inp, pool, arena, inp.jobs, inp.tables_src, inp.arena_bytes, per_group, rng) > 0
-    assert check_load_sampled(inp, fresh, arena, inp.jobs, inp.tables_dst, inp.arena_bytes, per_group, rng) > 0
+    store_o, load_o = _oracle_calls(Lo, C)
+    assert check_store_streamed(Lo, C, pool, arena, inp.jobs, inp.object_bytes, inp.tables_src,
+                                store_o) == inp.payload_bytes
     del pool
-    # store after load under the load's tables reproduces every object
-    arena2 = torch.empty_like(arena)
-    lmc.lmc_store(Lp, C, fresh, t_dst, jobs, arena2, st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0 and torch.equal(arena, arena2)
-    del arena2, arena
+    assert check_load_streamed(Lo, C, fresh, arena, inp.jobs, inp.object_bytes, inp.tables_dst,
+                               load_o) == inp.payload_bytes
+    del arena
+    torch.cuda.empty_cache()
     assert check_untouched(inp, fresh, inp.jobs, inp.tables_dst, inp.arena_bytes, W.SENTINEL)
 
 
@@ -304,13 +308,13 @@ def test_full_size_k3_waves(lmc, wave):
     """K3 (93 layers, N = 768, chunk 1536), 4 requests of 131,072 tokens in
     4 waves of one request (a wave's pool, objects and fresh pool fill
     ~116 GB)."""
-    _full_size(lmc, W.CONFIGS[3], request_ids=[wave], per_group=4)
+    _full_size(lmc, W.CONFIGS[3], request_ids=[wave])
 
 
 def _mixed_run(lmc, inp, Lp, pool, load_arena):
     """The mixed serving step: load of cached chunks on one stream, store of
     new chunks on another, both on the same pool (disjoint blocks)."""
-    store_arena = torch.empty(inp.store_arena_bytes, dtype=torch.uint8, device=DEV)
+    store_arena = torch.full((inp.store_arena_bytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
     st = _status()
     tabs = dev_tables(inp.tables_src, DEV)
     lj, sj = dev_jobs(inp.load_jobs, DEV), dev_jobs(inp.store_jobs, DEV)
@@ -348,16 +352,21 @@ def test_full_size_mixed_two_streams(lmc):
     cfg = W.CONFIGS[4]
     inp, Lp = case_inputs(cfg)
     Lo, C = inp.layout, inp.C
-    rng = np.random.default_rng(4)
     pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
     W.fill_normal(pool, 40)
     load_arena = torch.empty(inp.load_arena_bytes, dtype=torch.uint8, device=DEV)
     W.fill_normal(load_arena, 42)
     store_arena, tabs, lj = _mixed_run(lmc, inp, Lp, pool, load_arena)
-    assert check_store_sampled(inp, pool, store_arena, inp.store_jobs, inp.tables_src,
-                               inp.store_arena_bytes, 8, rng) > 0
-    assert check_load_sampled(inp, pool, load_arena, inp.load_jobs, inp.tables_src,
-                              inp.load_arena_bytes, 8, rng) > 0
+    # every stored object against the oracle, from the pool's pages (the
+    # store's blocks are not the load's: the untouched check below shows
+    # they still hold the original bytes); every loaded page against the
+    # oracle's scatter of the cached objects
+    sizes = inp.object_bytes
+    store_o, load_o = _oracle_calls(Lo, C)
+    assert check_store_streamed(Lo, C, pool, store_arena, inp.store_jobs, sizes, inp.tables_src, store_o) == \
+        sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.store_jobs))
+    assert check_load_streamed(Lo, C, pool, load_arena, inp.load_jobs, sizes, inp.tables_src, load_o) == \
+        sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.load_jobs))
     del store_arena
     # storing the loaded chunks back reproduces the loaded objects
     again = torch.empty_like(load_arena)
@@ -515,8 +524,8 @@ def test_q8_random_specs_exact(lmc, t):
 
 def test_q8_block_objects_full_size_every_block(lmc):
     """The lognormal Kimi-Linear batch (packed, chunk 2N) as block objects of
-    2 blocks with every snapshot an INT8 record (d = 128): sampled objects
-    and decoded pages against the oracle."""
+    2 blocks with every snapshot an INT8 record (d = 128): every record and
+    every decoded page against the oracle."""
     cfg = W.CONFIGS[2]
     inp, Lp = case_inputs(cfg)
     Lo, C = inp.layout, inp.C
@@ -526,7 +535,7 @@ def test_q8_block_objects_full_size_every_block(lmc):
     jobs, nbytes = W.pack_jobs(units, sizes)
     pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
     W.fill_normal(pool, 64)
-    arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    arena = torch.full((nbytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
     fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
     st = _status()
     dj = dev_jobs(jobs, DEV)
@@ -534,30 +543,20 @@ def test_q8_block_objects_full_size_every_block(lmc):
     lmc.lmc_load_blocks_q8(Lp, m, lmc.LMC_KDA_EVERY_BLOCK, d, fresh, dev_tables(inp.tables_dst, DEV), dj, arena, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    rng = np.random.default_rng(9)
-    sel = [J[np.sort(rng.choice(len(J), 5, replace=False))] for J in jobs]
-    pages, s0 = oracle.list_pages(Lo, C, inp.tables_src, sel, 1 << 62, nb=m, kda_every=True)
-    assert s0 == 0
-    host = np.zeros(Lo.pool_bytes, dtype=np.uint8)
-    for pg in pages:
-        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
-        host[lo:lo + n] = pool[lo:lo + n].cpu().numpy()
-    arena_o = np.zeros(nbytes, dtype=np.uint8)
-    assert oracle.store_blocks_q8(Lo, m, True, d, host, inp.tables_src, sel, arena_o) == 0
-    for g, J in enumerate(sel):
-        for job in J:
-            lo, hi = int(job["offset"]), int(job["offset"]) + sizes[g]
-            assert np.array_equal(arena[lo:hi].cpu().numpy(), arena_o[lo:hi])
-    back = np.zeros(Lo.pool_bytes, dtype=np.uint8)
-    assert oracle.load_blocks_q8(Lo, m, True, d, back, inp.tables_dst, sel, arena_o) == 0
-    pages_d, _ = oracle.list_pages(Lo, C, inp.tables_dst, sel, 1 << 62, nb=m, kda_every=True)
-    for pg in pages_d:
-        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
-        assert np.array_equal(fresh[lo:lo + n].cpu().numpy(), back[lo:lo + n])
+    assert check_store_streamed(
+        Lo, C, pool, arena, jobs, sizes, inp.tables_src,
+        lambda p, t, j, a: oracle.store_blocks_q8(Lo, m, True, d, p, t, j, a), nb=m, kda_every=True) == \
+        sum(sizes[g] * len(J) for g, J in enumerate(jobs))
+    del pool
+    assert check_load_streamed(
+        Lo, C, fresh, arena, jobs, sizes, inp.tables_dst,
+        lambda p, t, j, a: oracle.load_blocks_q8(Lo, m, True, d, p, t, j, a), nb=m, kda_every=True) == \
+        sum(Lo.object_bytes_blocks(m, True, g) * len(J) for g, J in enumerate(jobs))
 
 
 def test_block_objects_full_size_every_block(lmc):
-    """Kimi-Linear packed, chunk = 2N, objects with one KDA snapshot per block."""
+    """Kimi-Linear packed, chunk = 2N, objects with one KDA snapshot per block:
+    every object and every loaded page against the oracle."""
     cfg = W.CONFIGS[2]
     inp, Lp = case_inputs(cfg)
     Lo, C = inp.layout, inp.C
@@ -566,7 +565,7 @@ def test_block_objects_full_size_every_block(lmc):
     jobs, nbytes = W.pack_jobs(units, sizes)
     pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
     W.fill_normal(pool, 77)
-    arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    arena = torch.full((nbytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
     fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
     st = _status()
     dj = dev_jobs(jobs, DEV)
@@ -575,24 +574,14 @@ def test_block_objects_full_size_every_block(lmc):
     lmc.lmc_load_blocks(Lp, nb, lmc.LMC_KDA_EVERY_BLOCK, fresh, t_dst, dj, arena, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    rng = np.random.default_rng(2)
-    sel = [J[np.sort(rng.choice(len(J), 6, replace=False))] for J in jobs]
-    pages, s0 = oracle.list_pages(Lo, C, inp.tables_src, sel, nbytes, nb=nb, kda_every=True)
-    assert s0 == 0
-    host_pool = np.zeros(Lo.pool_bytes, dtype=np.uint8)
-    for pg in pages:
-        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
-        host_pool[lo:lo + n] = pool[lo:lo + n].cpu().numpy()
-    arena_o = np.zeros(nbytes, dtype=np.uint8)
-    assert oracle.store_blocks(Lo, nb, True, host_pool, inp.tables_src, sel, arena_o) == 0
-    for g, J in enumerate(sel):
-        for job in J:
-            lo, hi = int(job["offset"]), int(job["offset"]) + sizes[g]
-            assert np.array_equal(arena[lo:hi].cpu().numpy(), arena_o[lo:hi])
-    arena2 = torch.empty_like(arena)
-    lmc.lmc_store_blocks(Lp, nb, lmc.LMC_KDA_EVERY_BLOCK, fresh, t_dst, dj, arena2, st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0 and torch.equal(arena, arena2)
+    payload = sum(sizes[g] * len(J) for g, J in enumerate(jobs))
+    assert check_store_streamed(
+        Lo, C, pool, arena, jobs, sizes, inp.tables_src,
+        lambda p, t, j, a: oracle.store_blocks(Lo, nb, True, p, t, j, a), nb=nb, kda_every=True) == payload
+    del pool
+    assert check_load_streamed(
+        Lo, C, fresh, arena, jobs, sizes, inp.tables_dst,
+        lambda p, t, j, a: oracle.load_blocks(Lo, nb, True, p, t, j, a), nb=nb, kda_every=True) == payload
 
 
 def _random_pairs(L, rng, per_group, free_from):
@@ -662,23 +651,29 @@ def test_copy_blocks_full_size_kda_states(lmc):
                 d0 = o.base[i] + int(pr["dst_block"]) * o.stride[i]
                 ref[d0:d0 + o.real_bytes[i]] = before[s0:s0 + o.real_bytes[i]]
     assert torch.equal(ref, pool)
-    # and a sample matches the oracle run on host copies of the pages involved
-    rng = np.random.default_rng(5)
-    g = o.kv_group_kind.index("KDA")
-    sel = pairs[g][rng.choice(len(pairs[g]), 4, replace=False)]
-    host = np.zeros(o.pool_bytes, dtype=np.uint8)
-    layers = [i for i in range(len(o.kinds)) if o.kv_group[i] == g]
-    for pr in sel:
-        for i in layers:
-            s0 = o.base[i] + int(pr["src_block"]) * o.stride[i]
-            host[s0:s0 + o.real_bytes[i]] = ref[s0:s0 + o.real_bytes[i]].cpu().numpy()
-    only = [np.zeros(0, dtype=oracle.PAIR_DTYPE) for _ in pairs]
-    only[g] = sel
-    assert oracle.copy_blocks(o, host, only) == 0
-    for pr in sel:
-        for i in layers:
-            d0 = o.base[i] + int(pr["dst_block"]) * o.stride[i]
-            assert np.array_equal(pool[d0:d0 + o.real_bytes[i]].cpu().numpy(), host[d0:d0 + o.real_bytes[i]])
+    # every copied page against the oracle, run on host copies of the
+    # source pages, a slice of pairs at a time
+    host = LazyHost(o.pool_bytes)
+    checked = 0
+    for g, P_ in enumerate(pairs):
+        layers = [i for i in range(len(o.kinds)) if o.kv_group[i] == g]
+        for k in range(0, len(P_), 64):
+            sel = P_[k:k + 64]
+            for pr in sel:
+                for i in layers:
+                    s0 = o.base[i] + int(pr["src_block"]) * o.stride[i]
+                    fetch(pool, s0, s0 + o.real_bytes[i], host.a[s0:s0 + o.real_bytes[i]])
+            only = [np.zeros(0, dtype=oracle.PAIR_DTYPE) for _ in pairs]
+            only[g] = sel
+            assert oracle.copy_blocks(o, host.a, only) == 0
+            for pr in sel:
+                for i in layers:
+                    d0 = o.base[i] + int(pr["dst_block"]) * o.stride[i]
+                    assert np.array_equal(fetch(pool, d0, d0 + o.real_bytes[i]), host.a[d0:d0 + o.real_bytes[i]])
+                    checked += o.real_bytes[i]
+            host.release()
+    assert checked == sum(len(P_) * sum(o.real_bytes[i] for i in range(len(o.kinds)) if o.kv_group[i] == g)
+                          for g, P_ in enumerate(pairs))
 
 
 # ---------------------------------------------------------------------------
@@ -858,19 +853,19 @@ def test_q8_without_state_layers_is_the_plain_store(lmc):
     assert np.array_equal(fresh.cpu().numpy(), fresh_o)
 
 
-def test_q8_full_size_kimi_linear(lmc):
-    """Kimi-Linear full size, d = 128: sampled records and decoded pages
-    against the oracle; decoded values within half a step everywhere sampled."""
-    cfg = W.CONFIGS[1]
-    inp, Lp = case_inputs(cfg)
+def _q8_full_size(lmc, cfg, request_ids=None, seed=63):
+    """Full-size chunk store + load with INT8 KDA records (rows of d = 128):
+    every record and every decoded page against the oracle."""
+    inp, Lp = case_inputs(cfg, request_ids)
     Lo, C = inp.layout, inp.C
     d = W.state_row_elems(cfg)
     sizes = [Lo.object_bytes_q8(C, d, g) for g in range(Lo.num_object_groups)]
+    assert [Lp.object_bytes_q8(C, d, g) for g in range(Lo.num_object_groups)] == sizes
     units = [[(int(j["request"]), int(j["chunk"])) for j in J] for J in inp.jobs]
     jobs, nbytes = W.pack_jobs(units, sizes)
     pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
-    W.fill_normal(pool, 63)
-    arena = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, seed)
+    arena = torch.full((nbytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
     fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
     st = _status()
     dj = dev_jobs(jobs, DEV)
@@ -879,26 +874,27 @@ def test_q8_full_size_kimi_linear(lmc):
     lmc.lmc_load_q8(Lp, C, d, fresh, t_dst, dj, arena, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    rng = np.random.default_rng(8)
-    sel = [J[np.sort(rng.choice(len(J), 5, replace=False))] for J in jobs]
-    pages, s0 = oracle.list_pages(Lo, C, inp.tables_src, sel, nbytes)
-    assert s0 == 0
-    host = np.zeros(Lo.pool_bytes, dtype=np.uint8)
-    for pg in pages:
-        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
-        host[lo:lo + n] = pool[lo:lo + n].cpu().numpy()
-    arena_o = np.zeros(nbytes, dtype=np.uint8)
-    assert oracle.store_q8(Lo, C, d, host, inp.tables_src, sel, arena_o) == 0
-    for g, J in enumerate(sel):
-        for job in J:
-            lo, hi = int(job["offset"]), int(job["offset"]) + sizes[g]
-            assert np.array_equal(arena[lo:hi].cpu().numpy(), arena_o[lo:hi])
-    back = np.zeros(Lo.pool_bytes, dtype=np.uint8)
-    assert oracle.load_q8(Lo, C, d, back, inp.tables_dst, sel, arena_o) == 0
-    pages_d, _ = oracle.list_pages(Lo, C, inp.tables_dst, sel, nbytes)
-    for pg in pages_d:
-        lo, n = int(pg["pool_offset"]), int(pg["bytes"])
-        assert np.array_equal(fresh[lo:lo + n].cpu().numpy(), back[lo:lo + n])
+    assert check_store_streamed(Lo, C, pool, arena, jobs, sizes, inp.tables_src,
+                                lambda p, t, j, a: oracle.store_q8(Lo, C, d, p, t, j, a)) == \
+        sum(sizes[g] * len(J) for g, J in enumerate(jobs))
+    del pool
+    assert check_load_streamed(Lo, C, fresh, arena, jobs, sizes, inp.tables_dst,
+                               lambda p, t, j, a: oracle.load_q8(Lo, C, d, p, t, j, a)) == inp.payload_bytes
+    del arena
+    torch.cuda.empty_cache()
+    assert check_untouched(inp, fresh, inp.jobs, inp.tables_dst, inp.arena_bytes, W.SENTINEL)
+
+
+def test_q8_full_size_kimi_linear(lmc):
+    """Kimi-Linear full size (32 x 8192 tokens, 18 KDA layers of 32 heads)."""
+    _q8_full_size(lmc, W.CONFIGS[1])
+
+
+def test_q8_full_size_k3_wave(lmc):
+    """Kimi K3 (69 KDA layers of 64 heads, 147,456-byte conv windows, fp8
+    MLA), one wave of one 131,072-token request: the workload whose page
+    describes the compressed checkpoints."""
+    _q8_full_size(lmc, W.CONFIGS[3], request_ids=[0], seed=73)
 
 
 def test_q8_row_scale_every_float(lmc):
