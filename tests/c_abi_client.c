@@ -89,6 +89,57 @@ int main(void) {
     printf("store_without_batch %d\n", lmc_store(L, 944, NULL, NULL, NULL, 0, NULL, NULL));
     printf("store_bad_chunk %d\n", lmc_store(L, 900, NULL, NULL, NULL, 0, NULL, NULL));
     printf("strerror_budget %s\n", lmc_strerror(LMC_ERR_BUDGET));
+
+    /* copy-on-write pairs that would race are refused on the host copy
+     * before any launch (the pool pointer is NULL, so a batch that passed
+     * the rule would be refused just before launching: nothing runs) */
+    lmc_block_pair racing[2] = {{1, 9}, {9, 12}}; /* 9 written by one pair, read by the other */
+    lmc_block_pair fine[2] = {{1, 9}, {2, 12}};
+    const lmc_block_pair *dev_pairs[4] = {NULL, NULL, NULL, NULL};
+    const lmc_block_pair *host_pairs[4] = {NULL, NULL, NULL, NULL};
+    int64_t counts[4] = {0, 2, 0, 0};
+    lmc_copy_batch cb;
+    memset(&cb, 0, sizeof cb);
+    cb.num_kv_groups = info.num_kv_groups;
+    cb.pairs = dev_pairs;
+    cb.num_pairs = counts;
+    cb.host_pairs = host_pairs;
+    dev_pairs[1] = racing; /* never dereferenced on the host */
+    host_pairs[1] = racing;
+    uint32_t status_word = 0;
+    printf("copy_racing %d\n", lmc_copy_blocks(L, NULL, &cb, &status_word, NULL));
+    dev_pairs[1] = fine;
+    host_pairs[1] = fine;
+    printf("copy_fine_null_pool %d\n", lmc_copy_blocks(L, NULL, &cb, &status_word, NULL));
+    cb.host_pairs = NULL;
+    printf("copy_without_host_pairs %d\n", lmc_copy_blocks(L, NULL, &cb, &status_word, NULL));
+
+    /* mixed-step guard on host arrays (chunk = N, one request): the load
+     * side moves chunk 0, whose position 0 holds blocks 0, 10, 20, 30 in
+     * the four KV groups' tables; the store side chunk 1 of other tables
+     * (blocks 6, 16, 26, 36) */
+    int32_t tables_a[4][2], tables_b[4][2];
+    lmc_block_table ta[4], tb[4];
+    for (int k = 0; k < 4; k++) {
+        tables_a[k][0] = 10 * k;
+        tables_a[k][1] = 10 * k + 1;
+        tables_b[k][0] = 10 * k + 5;
+        tables_b[k][1] = 10 * k + 6;
+        ta[k].table = tables_a[k];
+        tb[k].table = tables_b[k];
+        ta[k].row_stride = tb[k].row_stride = 2;
+        ta[k].num_cols = tb[k].num_cols = 2;
+    }
+    lmc_job ja = {0, 0, 0}, jb = {0, 1, 0};
+    const lmc_job *jobs_a[2] = {&ja, &ja}, *jobs_b[2] = {&jb, &jb};
+    int64_t njobs[2] = {1, 1};
+    lmc_batch ba = {1, 4, ta, 2, 0, jobs_a, njobs}, bb = {1, 4, tb, 2, 0, jobs_b, njobs};
+    int32_t common = 0;
+    rc = lmc_check_disjoint(L, 944, &ba, &bb, &common);
+    printf("disjoint %d %d\n", rc, common);
+    tables_b[2][1] = 20; /* the store side now reads block 20, which the load side writes */
+    rc = lmc_check_disjoint(L, 944, &ba, &bb, &common);
+    printf("shared %d %d\n", rc, common);
     lmc_layout_free(L);
     printf("done\n");
     return 0;

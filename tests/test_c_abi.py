@@ -49,6 +49,12 @@ def test_host_rules_from_c(client_output):
     assert int(_value(L, "store_without_batch")) == lmc.LMC_ERR_INVALID_ARG
     assert int(_value(L, "store_bad_chunk")) == lmc.LMC_ERR_NOT_MULTIPLE
     assert _value(L, "strerror_budget") == lmc.lmc_strerror(lmc.LMC_ERR_BUDGET)
+    # racing copies and the mixed-step guard, from C
+    assert int(_value(L, "copy_racing")) == lmc.LMC_ERR_OVERLAP
+    assert int(_value(L, "copy_fine_null_pool")) == lmc.LMC_ERR_INVALID_ARG
+    assert int(_value(L, "copy_without_host_pairs")) == lmc.LMC_ERR_INVALID_ARG
+    assert _value(L, "disjoint") == f"{lmc.LMC_OK} -1"
+    assert _value(L, "shared") == f"{lmc.LMC_ERR_OVERLAP} 20"
 
 
 def test_layout_from_c_matches_binding(client_output):
