@@ -55,9 +55,10 @@ def _kernel_sha():
 
 
 def _traffic(kernel: str, workload_index: int, op: str):
-    """DRAM bytes per launch of `kernel` (its function name) on a workload and
-    operation from the committed ncu summary, or None when none was taken or
-    the kernel source changed since the counters were taken."""
+    """The committed small-case ncu capture of `kernel` (its function name)
+    on a workload and operation: {"case", "ratio" = DRAM bytes / algorithmic
+    bytes, ...}, or None when none was taken or the kernel source changed
+    since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
@@ -65,9 +66,9 @@ def _traffic(kernel: str, workload_index: int, op: str):
         return None
     key = f"config{workload_index}" + ("" if op == "paging" else f"/{op}")
     entry = t.get(key, {}).get(kernel)
-    if not entry or entry.get("kernel_sha") != _kernel_sha():
+    if not entry or entry.get("kernel_sha") != _kernel_sha() or not entry.get("ratio"):
         return None
-    return entry.get("dram_bytes_per_launch")
+    return entry
 
 
 class Clocks:
@@ -125,9 +126,9 @@ def _kernel_times(nbytes, ms_list):
     """Mean (the line's figure), median and best of one kernel's per-step
     CUDA-event times, with the bytes-moved rates they give."""
     if not ms_list or max(ms_list) <= 0:
-        return {"ms": None, "gbs": None}
+        return {"ms": None, "gbs": None, "bytes": nbytes}
     mean, med, best = statistics.mean(ms_list), statistics.median(ms_list), min(ms_list)
-    return {"ms": round(mean, 4), "gbs": _gbs(nbytes, mean), "median_ms": round(med, 4),
+    return {"ms": round(mean, 4), "gbs": _gbs(nbytes, mean), "bytes": nbytes, "median_ms": round(med, 4),
             "median_gbs": _gbs(nbytes, med), "best_ms": round(best, 4), "best_gbs": _gbs(nbytes, best)}
 
 
@@ -168,72 +169,122 @@ def _dist():
 # CPU oracle leg (cpu_baseline and --impl reference)
 # ----------------------------------------------------------------------------
 
-def oracle_sample(cfg_index: int, requests: int, reps: int, threads: int, warmup: int = 1,
-                  budget_bytes: int = 3 << 30):
-    """Times the CPU oracle on a bounded sample of the workload: the first
-    `requests` requests, each cut to at most the tokens that keep the sample's
-    payload near `budget_bytes`; `threads` workers over disjoint jobs. Plain
-    workloads: store then load into a fresh pool; the mixed step: load of the
-    cached chunks and store of the new chunks on one pool."""
-    import dataclasses
-    from concurrent.futures import ThreadPoolExecutor
+def _host_free_bytes() -> int:
+    """Free host memory (sysconf), the budget for the oracle's buffers."""
+    return os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
 
-    import torch
+
+def _step_requests(cfg, requests=None) -> int:
+    """Requests one step moves: all of the workload, or one wave when the
+    workload runs in waves (config 3: one 131,072-token request per wave),
+    or the first `requests`."""
+    if requests is not None:
+        return min(requests, cfg.num_requests)
+    return cfg.num_requests // cfg.waves if cfg.waves > 1 else cfg.num_requests
+
+
+def _workload_config(cfg, op, n_req, store_payload, load_payload, C, pool_bytes, world):
+    """The `config` object of a line; the GPU arm and the oracle arm print
+    the same one for the same workload."""
+    scope = (f"one wave: {n_req} of {cfg.num_requests} requests ({cfg.waves} waves of the workload)"
+             if cfg.waves > 1 and n_req * cfg.waves == cfg.num_requests else
+             f"{n_req} of {cfg.num_requests} requests")
+    return {"workload": cfg.name, "index": cfg.index, "op": op, "requests": n_req, "scope": scope,
+            "store_payload_bytes": int(store_payload), "load_payload_bytes": int(load_payload),
+            "chunk": int(C), "N": cfg.N, "layout": "packed" if cfg.packed else "padded",
+            "pool_bytes": int(pool_bytes),
+            "l2": "inputs larger than L2 (pool and objects are each many GB; no flush)",
+            "parallelism": f"{world} independent replica(s), no exchange"}
+
+
+def _oracle_footprint(inp) -> int:
+    L = inp.layout
+    if inp.cfg.mixed:
+        return L.pool_bytes + inp.load_arena_bytes + inp.store_arena_bytes
+    return 2 * L.pool_bytes + inp.arena_bytes
+
+
+def oracle_time(cfg_index: int, n_req: int, threads: int, seconds: float = 10.0, reps: int | None = None,
+                warmup: int = 1, pool_of=None):
+    """Times the CPU oracle, as written, on the first `n_req` requests of a
+    workload (the payload of one GPU step): the store of every whole chunk
+    then the load into a fresh pool under new tables (the mixed step: its
+    load of cached chunks and its store of new chunks on one pool), with
+    `threads` workers over disjoint jobs. `reps` timed passes after `warmup`
+    (or as many as fill about `seconds`). Host memory is checked first
+    (sysconf); when the buffers do not fit, the requests run in consecutive
+    waves and the times add up. Pool bytes: pool_of(inputs) when given (the
+    GPU arm's own device pool), else seeded N(0,1) draws on the host."""
+    from concurrent.futures import ThreadPoolExecutor
 
     import oracle
     cfg = W.CONFIGS[cfg_index]
     C = oracle.negotiate_chunk(cfg.requested_chunk, cfg.N)
-    ids = list(range(min(requests, cfg.num_requests)))
     build = functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed)
-    probe = oracle.layout(cfg.layers, cfg.N, cfg.packed, 1 << 60)
-    per_chunk = sum(probe.object_bytes(C, g) for g in range(probe.num_object_groups))
-    max_chunks = max(1, budget_bytes // (per_chunk * len(ids)))
-    lengths = W.request_lengths(cfg)
-    if lengths.max() // C > max_chunks:
-        capped = tuple(int(min(x, max_chunks * C + C // 2)) for x in lengths)
-        cfg = dataclasses.replace(cfg, lengths="fixed", fixed_lengths=capped)
-    inp = W.make_inputs(cfg, build, C, ids)
-    L = inp.layout
-    pool = W.fill_normal(torch.empty(L.pool_bytes, dtype=torch.uint8), cfg.seed).numpy()
-    sizes = inp.object_bytes
-    if cfg.mixed:
-        src = W.fill_normal(torch.empty(inp.load_arena_bytes, dtype=torch.uint8), cfg.seed + 7).numpy()
-        out = np.zeros(inp.store_arena_bytes, dtype=np.uint8)
-        lparts = [[J[k::threads] for J in inp.load_jobs] for k in range(threads)]
-        sparts = [[J[k::threads] for J in inp.store_jobs] for k in range(threads)]
-        payload = (sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.load_jobs)) +
-                   sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.store_jobs)))
+    ids = list(range(n_req))
+    budget = int(0.6 * _host_free_bytes())
+    full = W.make_inputs(cfg, build, C, ids)
+    n_waves = 1
+    while n_waves < len(ids) and max(
+            _oracle_footprint(W.make_inputs(cfg, build, C, list(w)))
+            for w in np.array_split(np.array(ids), n_waves)) > budget:
+        n_waves += 1
+    waves = [list(map(int, w)) for w in np.array_split(np.array(ids), n_waves) if len(w)]
+    total_s, passes, payload, chunks, store_total, load_total = 0.0, None, 0, 0, 0, 0
+    for w in waves:
+        inp = full if len(waves) == 1 else W.make_inputs(cfg, build, C, w)
+        L = inp.layout
+        pool = pool_of(inp) if (pool_of is not None and len(waves) == 1) else \
+            W.fill_normal_host(L.pool_bytes, cfg.seed, threads)
+        sizes = inp.object_bytes
+        if cfg.mixed:
+            src = W.fill_normal_host(inp.load_arena_bytes, cfg.seed + 7, threads)
+            out = np.zeros(inp.store_arena_bytes, dtype=np.uint8)
+            lparts = [[J[k::threads] for J in inp.load_jobs] for k in range(threads)]
+            sparts = [[J[k::threads] for J in inp.store_jobs] for k in range(threads)]
+            loaded = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.load_jobs))
+            stored = sum(int(sizes[g]) * len(j) for g, j in enumerate(inp.store_jobs))
 
-        def one_pass(ex):
-            a = list(ex.map(lambda p: oracle.load(L, C, pool, inp.tables_src, p, src), lparts))
-            b = list(ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, out), sparts))
-            return a + b
-        chunks = sum(len(j) for j in inp.store_jobs) // max(1, L.num_object_groups)
-    else:
-        fresh = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
-        arena = np.zeros(inp.arena_bytes, dtype=np.uint8)
-        parts = [[J[k::threads] for J in inp.jobs] for k in range(threads)]
-        payload = 2 * inp.payload_bytes
+            def one_pass(ex):
+                a = list(ex.map(lambda p: oracle.load(L, C, pool, inp.tables_src, p, src), lparts))
+                b = list(ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, out), sparts))
+                return a + b
+            units = sum(len(j) for j in inp.store_jobs) // max(1, L.num_object_groups)
+        else:
+            fresh = np.full(L.pool_bytes, W.SENTINEL, dtype=np.uint8)
+            arena = np.zeros(inp.arena_bytes, dtype=np.uint8)
+            parts = [[J[k::threads] for J in inp.jobs] for k in range(threads)]
+            loaded = stored = inp.payload_bytes
 
-        def one_pass(ex):
-            a = list(ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, arena), parts))
-            b = list(ex.map(lambda p: oracle.load(L, C, fresh, inp.tables_dst, p, arena), parts))
-            return a + b
-        chunks = sum(int(x) // C for x in inp.lengths)
-    with ThreadPoolExecutor(threads) as ex:
-        for _ in range(warmup):
-            one_pass(ex)
-        t0 = time.perf_counter()
-        for _ in range(reps):
-            assert all(st == 0 for st in one_pass(ex))
-        dt = time.perf_counter() - t0
-    gbs = 2 * payload * reps / dt / 1e9
+            def one_pass(ex):
+                a = list(ex.map(lambda p: oracle.store(L, C, pool, inp.tables_src, p, arena), parts))
+                b = list(ex.map(lambda p: oracle.load(L, C, fresh, inp.tables_dst, p, arena), parts))
+                return a + b
+            units = sum(int(x) // C for x in inp.lengths)
+        with ThreadPoolExecutor(threads) as ex:
+            t0 = time.perf_counter()
+            for _ in range(max(1, warmup)):
+                assert all(st == 0 for st in one_pass(ex))
+            per_pass = (time.perf_counter() - t0) / max(1, warmup)
+            if passes is None:
+                passes = reps if reps is not None else int(min(100, max(2, seconds / len(waves) / per_pass)))
+            t0 = time.perf_counter()
+            for _ in range(passes):
+                assert all(st == 0 for st in one_pass(ex))
+            total_s += time.perf_counter() - t0
+        payload += loaded + stored
+        store_total += stored
+        load_total += loaded
+        chunks += units
+        del pool
+    gbs = 2 * payload * passes / total_s / 1e9  # each payload byte read once and written once
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {len(ids)} of {W.CONFIGS[cfg_index].num_requests} requests"
-                      f"{' (cut to ' + str(max_chunks) + ' chunks each)' if cfg is not W.CONFIGS[cfg_index] else ''}"
-                      f", {payload} object bytes moved per pass (store + load), {reps} timed passes after "
-                      f"{warmup} warm-up, {threads} threads over disjoint jobs",
-            "chunks_per_s": round(chunks * reps / dt, 2), "seconds": round(dt, 3)}
+            "sample": f"the whole step: {n_req} of {cfg.num_requests} requests, {payload} object bytes moved per "
+                      f"pass (store + load) in {len(waves)} wave(s) of host buffers, {passes} timed passes after "
+                      f"{max(1, warmup)} warm-up, {threads} thread(s) over disjoint jobs",
+            "chunks_per_s": round(chunks * passes / total_s, 2), "seconds": round(total_s, 3),
+            "passes": passes, "waves": len(waves), "payload_bytes_per_pass": payload,
+            "config": _workload_config(cfg, "paging", n_req, store_total, load_total, C, full.layout.pool_bytes, 1)}
 
 
 def run_reference(args):
@@ -242,14 +293,16 @@ def run_reference(args):
         return
     threads = os.cpu_count() or 1
     cfg = W.CONFIGS[args.config]
-    # each step is one store + load pass over a bounded sample (8 of the 32
-    # requests); warm-up passes run inside the same call before timing starts
-    res = oracle_sample(args.config, requests=8, reps=args.steps, threads=threads, warmup=args.warmup)
+    n_req = _step_requests(cfg, args.requests)
+    # each step is one store + load pass over the GPU step's whole payload;
+    # the warm-up passes run inside the same call before timing starts
+    res = oracle_time(args.config, n_req, threads, reps=args.steps, warmup=args.warmup)
+    config = dict(res["config"], parallelism=f"{world} independent replica(s), no exchange")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["seconds"] * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": cfg.name, "index": cfg.index, "sample": res["sample"]},
+        "config": config,
         "cpu_baseline": {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "chunks_per_s": res["chunks_per_s"]}))
@@ -585,6 +638,118 @@ class CopyStep:
         self.h_status.copy_(self.status, non_blocking=True)
 
 
+def _capped(cfg, max_chunks, negotiate):
+    """The workload with every request cut to at most `max_chunks` whole
+    chunks (small cases for profiler captures), or unchanged."""
+    if not max_chunks:
+        return cfg
+    import dataclasses
+    C = negotiate(cfg.requested_chunk, cfg.N)
+    lengths = tuple(int(min(x, max_chunks * C)) for x in W.request_lengths(cfg))
+    return dataclasses.replace(cfg, lengths="fixed", fixed_lengths=lengths)
+
+
+def _make_step(lmc, torch, cfg, dev, rank, op, n_req):
+    ids = list(range(n_req))
+    if op == "copy":
+        return CopyStep(lmc, torch, cfg, dev, rank, ids)
+    return PagingStep(lmc, torch, cfg, dev, rank, ids, op)
+
+
+def _time_steps(S, torch, dev, dist, local, steps, warmup):
+    """W untimed steps, then K steps timed with CUDA events on the launching
+    streams, bracketed by a barrier and a device synchronise on both sides;
+    SM clocks and throttle reasons sampled during the timed region."""
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(warmup, 3)):
+        S.step()
+    barrier()
+    assert int(S.status.item()) == 0, f"device status {int(S.status.item()):#x}"
+    evs = [S.new_events() for _ in range(steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        t_start.record(S.main)
+        for k in range(steps):
+            S.step(evs[k])
+        t_end.record(S.main)
+        barrier()
+    assert int(S.status.item()) == 0
+    ms = t_start.elapsed_time(t_end) / steps
+    if dist is not None:
+        ms = _reduce_max(dist, [ms], dev)[0]
+    return {"ms_per_step": ms, "steps": steps, "warmup": max(warmup, 3), "clocks": clk.summary(),
+            "store_ms": [e[0].elapsed_time(e[1]) for e in evs], "load_ms": [e[2].elapsed_time(e[3]) for e in evs]}
+
+
+def _traffic_for(kernels, cfg_index, op):
+    """DRAM bytes per launch for the dominant kernel(s), from the committed
+    small-case ncu captures scaled to this launch by algorithmic bytes (a
+    copy's traffic grows in proportion to the bytes it moves): kernels =
+    [(kernel name, algorithmic bytes of this launch)]. None when a capture
+    is missing or the kernel source changed since it was taken."""
+    total, cases = 0, set()
+    for name, nbytes in kernels:
+        t = _traffic(name, cfg_index, op)
+        if t is None:
+            return None, None
+        total += t["ratio"] * nbytes
+        cases.add(t["case"])
+    return int(round(total)), "; ".join(sorted(cases))
+
+
+def _figures(S, cfg, op, world, t, peak, peak_src):
+    """Throughput, per-kernel times and the roofline of the dominant kernel
+    for one timed workload."""
+    ms = t["ms_per_step"]
+    value = S.bytes_per_step * world / (ms * 1e-3) / 1e9
+    st_avg, ld_avg = statistics.mean(t["store_ms"]), statistics.mean(t["load_ms"])
+    suffix = "_q8_kernel" if op in ("q8", "blocks_q8") else "_kernel"
+    if op == "copy":
+        dominant, dom_bytes, dom_ms = "lmc_copy_kernel", S.bytes_per_step, st_avg
+        parts = [("lmc_copy_kernel", dom_bytes)]
+    elif cfg.mixed:
+        # the two kernels share HBM concurrently: the roofline is the step's
+        dominant, dom_bytes, dom_ms = "lmc_store_kernel+lmc_load_kernel (concurrent)", S.bytes_per_step, ms
+        parts = [("lmc_store_kernel", S.store_bytes), ("lmc_load_kernel", S.load_bytes)]
+    elif st_avg >= ld_avg:
+        dominant, dom_bytes, dom_ms = "lmc_store" + suffix, S.store_bytes, st_avg
+        parts = [(dominant, dom_bytes)]
+    else:
+        dominant, dom_bytes, dom_ms = "lmc_load" + suffix, S.load_bytes, ld_avg
+        parts = [(dominant, dom_bytes)]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic, source = _traffic_for(parts, cfg.index, op)
+    return {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": t["steps"],
+        "warmup": t["warmup"],
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "chunks_per_s": round(S.chunks * world / (ms * 1e-3), 1),
+        "store": _kernel_times(S.store_bytes, t["store_ms"]),
+        "load": _kernel_times(S.load_bytes, t["load_ms"]),
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_source": (f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch on a small case "
+                                        f"({source}), scaled to this launch by algorithmic bytes") if source else None,
+                     "algorithmic_bytes_per_launch": dom_bytes},
+        "clocks": t["clocks"],
+    }
+
+
+# Further lines of the default run: the other workloads and operations, each
+# timed on its own in the same process (K capped to keep the run short).
+EXTRA_LINES = [("per_config", 2, "paging", 50), ("per_config", 3, "paging", 10), ("per_config", 4, "paging", 10),
+               ("per_op", 1, "q8", 50), ("per_op", 3, "q8", 10), ("per_op", 2, "blocks", 50),
+               ("per_op", 2, "blocks_q8", 50), ("per_op", 1, "copy", 50)]
+
+
 def run_gpu(args):
     import torch
 
@@ -595,42 +760,13 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = W.CONFIGS[args.config]
-    n_req = cfg.num_requests if args.requests is None else min(args.requests, cfg.num_requests)
-    if cfg.waves > 1 and args.requests is None:
-        n_req = cfg.num_requests // cfg.waves  # one wave fits the device; the step is one wave
+    cfg = _capped(W.CONFIGS[args.config], args.max_chunks, lmc.lmc_negotiate_chunk)
+    n_req = _step_requests(cfg, args.requests)
+    peak, peak_src = _peaks()
     # each rank runs its own independent copy of the batch (weak scaling)
-    if args.op == "copy":
-        S = CopyStep(lmc, torch, cfg, dev, rank, list(range(n_req)))
-    else:
-        S = PagingStep(lmc, torch, cfg, dev, rank, list(range(n_req)), args.op)
+    S = _make_step(lmc, torch, cfg, dev, rank, args.op, n_req)
     L = S.L
-
-    def barrier():
-        torch.cuda.synchronize(dev)
-        if dist is not None:
-            dist.barrier()
-
-    for _ in range(max(args.warmup, 3)):
-        S.step()
-    barrier()
-    assert int(S.status.item()) == 0, f"device status {int(S.status.item()):#x}"
-
-    evs = [S.new_events() for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
-        barrier()
-        t_start.record(S.main)
-        for k in range(args.steps):
-            S.step(evs[k])
-        t_end.record(S.main)
-        barrier()
-    clocks = clk.summary()
-    total_ms = t_start.elapsed_time(t_end)
-    store_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    load_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    assert int(S.status.item()) == 0
+    t = _time_steps(S, torch, dev, dist, local, args.steps, args.warmup)
 
     # the end-to-end step needs the objects in pinned host memory; if any rank
     # cannot pin them, every rank skips it (the ranks agree before going on)
@@ -648,72 +784,74 @@ def run_gpu(args):
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         for _ in range(2):
             S.e2e_step()
-        barrier()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(S.main)
         for _ in range(e2e_steps):
             S.e2e_step()
         e1.record(S.main)
-        barrier()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
         assert int(S.h_status.item()) == 0
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if dist is not None:
+            e2e_ms = _reduce_max(dist, [e2e_ms], dev)[0]
 
-    ms_per_step = total_ms / args.steps
-    if dist is not None:
-        ms_per_step, e2e_ms = _reduce_max(dist, [ms_per_step, e2e_ms], dev)
-    if rank != 0:
-        dist.destroy_process_group()
-        return
-
-    value = S.bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
-    peak, peak_src = _peaks()
-    st_avg, ld_avg = statistics.mean(store_ms), statistics.mean(load_ms)
-    suffix = "_q8_kernel" if args.op in ("q8", "blocks_q8") else "_kernel"
-    if args.op == "copy":
-        dominant, dom_bytes, dom_ms = "lmc_copy_kernel", S.bytes_per_step, st_avg
-    elif cfg.mixed:
-        # the two kernels share HBM concurrently: the roofline is the step's
-        dominant, dom_bytes, dom_ms = "lmc_store_kernel+lmc_load_kernel (concurrent)", S.bytes_per_step, ms_per_step
-    elif st_avg >= ld_avg:
-        dominant, dom_bytes, dom_ms = "lmc_store" + suffix, S.store_bytes, st_avg
-    else:
-        dominant, dom_bytes, dom_ms = "lmc_load" + suffix, S.load_bytes, ld_avg
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    fig = _figures(S, cfg, args.op, world, t, peak, peak_src)
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "metric": METRIC, "value": fig["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": fig["warmup"], "ms_per_step": fig["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": cfg.name, "index": cfg.index, "op": args.op, "requests": n_req,
-                   "store_payload_bytes": S.store_payload, "load_payload_bytes": S.load_payload,
-                   "chunk": S.C, "N": cfg.N, "layout": "packed" if cfg.packed else "padded",
-                   "pool_bytes": L.pool_bytes,
-                   "l2": "inputs larger than L2 (pool and objects are each many GB; no flush)",
-                   "parallelism": f"{world} independent replica(s), no exchange"},
-        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
-        "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "chunks_per_s": round(S.chunks * world / (ms_per_step * 1e-3), 1),
-        "store": _kernel_times(S.store_bytes, store_ms),
-        "load": _kernel_times(S.load_bytes, load_ms),
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic(dominant, cfg.index, args.op) if args.requests is None else None,
-                     "algorithmic_bytes_per_launch": dom_bytes},
+        "config": dict(_workload_config(cfg, args.op, n_req, S.store_payload, S.load_payload, S.C, L.pool_bytes,
+                                        world), **({"max_chunks": args.max_chunks} if args.max_chunks else {})),
+        **{k: fig[k] for k in ("pct_of_hbm_peak", "pct_of_nominal_hbm", "chunks_per_s", "store", "load", "roofline")},
         "e2e": ({"value": round(S.bytes_per_step * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                  "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": S.h2d, "d2h_bytes_per_step": S.d2h,
                  "parts": None if args.op == "copy" else args.e2e_parts} if e2e_ok else
                 {"value": None, "unit": "GB/s", "unavailable": e2e_err or "a rank could not pin its host buffers"}),
         "gpu_launches": S.launches_per_step * args.steps,
-        "clocks": clocks,
+        "clocks": fig["clocks"],
     }
     if world == 1 and not args.no_cpu_baseline and args.op == "paging":
         threads = os.cpu_count() or 1
-        # about 10 s of host time: ~150 passes over 8 requests on every core, then 20 on one
-        line["cpu_baseline"] = oracle_sample(args.config, requests=8, reps=150, threads=threads)
-        one = oracle_sample(args.config, requests=2, reps=20, threads=1)
+        # the oracle on the same payload as the step, on every host core
+        # (about 10-15 s of passes), then on one core (two passes); the pool is
+        # this step's own device pool, copied to the host
+        pool_of = lambda inp: S.pool.cpu().numpy()  # noqa: E731
+        res = oracle_time(args.config, n_req, threads, seconds=15.0, pool_of=pool_of)
+        one = oracle_time(args.config, n_req, 1, reps=2, pool_of=pool_of)
+        line["cpu_baseline"] = {k: res[k] for k in ("value", "unit", "cores", "kind", "sample", "chunks_per_s",
+                                                   "seconds", "waves")}
+        line["cpu_baseline"]["same_payload_as_step"] = res["payload_bytes_per_pass"] == \
+            S.store_payload + S.load_payload
         line["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
-    print(json.dumps(line))
+    del S
+    torch.cuda.empty_cache()
+
+    if args.extra_lines:
+        # the other workloads and operations, so that one default run covers
+        # every line; each is built, timed and freed in turn
+        for key, idx, op, k_cap in EXTRA_LINES:
+            if (idx, op) == (args.config, args.op):
+                continue
+            c = W.CONFIGS[idx]
+            nr = _step_requests(c)
+            S = _make_step(lmc, torch, c, dev, rank, op, nr)
+            tt = _time_steps(S, torch, dev, dist, local, min(args.steps, k_cap), args.warmup)
+            f = _figures(S, c, op, world, tt, peak, peak_src)
+            entry = {"config": _workload_config(c, op, nr, S.store_payload, S.load_payload, S.C, S.L.pool_bytes,
+                                                world), **f, "gpu_launches": S.launches_per_step * tt["steps"]}
+            line.setdefault(key, {})[f"config{idx}" + ("" if op == "paging" else f"/{op}")] = entry
+            del S
+            torch.cuda.empty_cache()
+        line["gpu_launches"] += sum(e["gpu_launches"] for key in ("per_config", "per_op")
+                                    for e in line.get(key, {}).values())
+    if rank == 0:
+        print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
 
@@ -725,11 +863,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--requests", type=int, default=None, help="use only the first R requests")
+    ap.add_argument("--max-chunks", type=int, default=None,
+                    help="cut every request to at most K whole chunks (small cases for profiler captures)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-parts", type=int, default=64,
                     help="ranges of (request, chunk) units the end-to-end step is pipelined over")
     ap.add_argument("--impl", choices=["lmc", "reference"], default="lmc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-lines", dest="extra_lines", action="store_false",
+                    help="time only the selected workload (the default run also times configs 2-4 and the "
+                         "codec, block and copy operations, each as its own entry)")
     ap.add_argument("--op", choices=["paging", "blocks", "copy", "q8", "blocks_q8"], default="paging",
                     help="paging: store + load by chunk; blocks: block-granular objects with one KDA "
                          "snapshot per block; copy: in-pool copy of every KDA snapshot; q8: store + load "

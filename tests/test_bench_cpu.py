@@ -82,4 +82,38 @@ def test_kernel_times_mean_median_best():
     t = bench._kernel_times(2_000_000_000, [2.0, 1.0, 4.0])
     assert t["ms"] == round(7 / 3, 4) and t["median_ms"] == 2.0 and t["best_ms"] == 1.0
     assert t["best_gbs"] == 2000.0 and t["median_gbs"] == 1000.0
-    assert bench._kernel_times(0, [0.002])["gbs"] is None
+    assert bench._kernel_times(0, [0.002])["gbs"] is None and t["bytes"] == 2_000_000_000
+
+
+def test_reference_arm_times_the_whole_step_payload():
+    """The oracle arm moves the GPU step's whole payload (both directions of
+    config 0: 2,147,328 object bytes each), and its `config` carries the
+    same workload keys as the GPU line."""
+    res = bench.oracle_time(0, 2, threads=2, reps=1, warmup=1)
+    c = res["config"]
+    assert res["payload_bytes_per_pass"] == 2 * 2_147_328
+    assert c["store_payload_bytes"] == c["load_payload_bytes"] == 2_147_328
+    assert c["requests"] == 2 and c["chunk"] == 128 and c["N"] == 64 and c["layout"] == "padded"
+    assert c["pool_bytes"] == 64 * 73_728 and res["waves"] == 1
+    assert set(c) == {"workload", "index", "op", "requests", "scope", "store_payload_bytes", "load_payload_bytes",
+                      "chunk", "N", "layout", "pool_bytes", "l2", "parallelism"}
+
+
+def test_reference_arm_runs_in_waves_when_host_memory_is_short(monkeypatch):
+    """With too little host memory for one pass, the requests run in waves
+    and the payload moved is unchanged."""
+    monkeypatch.setattr(bench, "_host_free_bytes", lambda: 16 << 20)
+    res = bench.oracle_time(0, 2, threads=1, reps=1, warmup=1)
+    assert res["waves"] == 2 and res["payload_bytes_per_pass"] == 2 * 2_147_328
+
+
+def test_step_requests_one_wave_of_k3():
+    assert bench._step_requests(W.CONFIGS[3]) == 1
+    assert bench._step_requests(W.CONFIGS[1]) == 32 and bench._step_requests(W.CONFIGS[1], 4) == 4
+
+
+def test_capped_requests_for_small_captures():
+    import state_cache_paging_gb300 as lmc
+    c = bench._capped(W.CONFIGS[3], 4, lmc.lmc_negotiate_chunk)
+    assert c.fixed_lengths == (4 * 1536,) * 4 and c.index == 3
+    assert bench._capped(W.CONFIGS[1], None, lmc.lmc_negotiate_chunk) is W.CONFIGS[1]

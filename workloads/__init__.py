@@ -261,6 +261,28 @@ def fill_normal_np(n: int, seed: int) -> np.ndarray:
     return buf
 
 
+def fill_normal_host(n: int, seed: int, threads: int = 1) -> np.ndarray:
+    """N(0,1) float32 draws as a uint8 numpy buffer of n bytes, drawn by
+    `threads` workers, each filling one contiguous part from its own stream
+    of one seed sequence (for host-side runs over many GB)."""
+    from concurrent.futures import ThreadPoolExecutor
+    buf = np.empty(n, dtype=np.uint8)
+    n4 = (n // 4) * 4
+    f = buf[:n4].view(np.float32)
+    k = max(1, int(threads))
+    bounds = [f.size * i // k for i in range(k + 1)]
+    streams = np.random.SeedSequence(int(seed)).spawn(k)
+
+    def fill(i):
+        lo, hi = bounds[i], bounds[i + 1]
+        if hi > lo:
+            np.random.default_rng(streams[i]).standard_normal(hi - lo, dtype=np.float32, out=f[lo:hi])
+    with ThreadPoolExecutor(k) as ex:
+        list(ex.map(fill, range(k)))
+    buf[n4:] = np.random.default_rng(int(seed)).integers(0, 256, n - n4, dtype=np.uint8)
+    return buf
+
+
 # ----------------------------------------------------------------------------
 # A whole batch of inputs for one workload
 # ----------------------------------------------------------------------------
