@@ -132,6 +132,13 @@ def _kernel_times(nbytes, ms_list):
             "median_gbs": _gbs(nbytes, med), "best_ms": round(best, 4), "best_gbs": _gbs(nbytes, best)}
 
 
+def _with_frac(times, peak):
+    """A kernel's mean rate as a fraction of the HBM peak (each kernel of a
+    line, beside the roofline of the slower one)."""
+    times["frac_of_peak"] = round(times["gbs"] / peak, 4) if times.get("gbs") else None
+    return times
+
+
 def _gbs(nbytes, ms):
     return round(nbytes / (ms * 1e-3) / 1e9, 2) if nbytes and ms > 0 else None
 
@@ -731,8 +738,8 @@ def _figures(S, cfg, op, world, t, peak, peak_src):
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "chunks_per_s": round(S.chunks * world / (ms * 1e-3), 1),
-        "store": _kernel_times(S.store_bytes, t["store_ms"]),
-        "load": _kernel_times(S.load_bytes, t["load_ms"]),
+        "store": _with_frac(_kernel_times(S.store_bytes, t["store_ms"]), peak),
+        "load": _with_frac(_kernel_times(S.load_bytes, t["load_ms"]), peak),
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy read+write)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,

@@ -117,3 +117,9 @@ def test_capped_requests_for_small_captures():
     c = bench._capped(W.CONFIGS[3], 4, lmc.lmc_negotiate_chunk)
     assert c.fixed_lengths == (4 * 1536,) * 4 and c.index == 3
     assert bench._capped(W.CONFIGS[1], None, lmc.lmc_negotiate_chunk) is W.CONFIGS[1]
+
+
+def test_each_kernel_reports_its_fraction_of_peak():
+    t = bench._with_frac(bench._kernel_times(7_000_000_000, [1.0]), 7000.0)
+    assert t["gbs"] == 7000.0 and t["frac_of_peak"] == 1.0
+    assert bench._with_frac(bench._kernel_times(0, [1.0]), 7000.0)["frac_of_peak"] is None
