@@ -313,7 +313,9 @@ def test_full_size_k3_waves(lmc, wave):
 
 def _mixed_run(lmc, inp, Lp, pool, load_arena):
     """The mixed serving step: load of cached chunks on one stream, store of
-    new chunks on another, both on the same pool (disjoint blocks)."""
+    new chunks on another, both on the same pool (disjoint blocks, checked
+    by the library's guard first, as a caller would)."""
+    assert lmc.lmc_check_disjoint(Lp, inp.C, inp.tables_src, inp.load_jobs, inp.tables_src, inp.store_jobs) == -1
     store_arena = torch.full((inp.store_arena_bytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
     st = _status()
     tabs = dev_tables(inp.tables_src, DEV)
@@ -616,6 +618,32 @@ def test_copy_blocks_exact(lmc, t):
     st_o = oracle.copy_blocks(o, pool_h, pairs)
     assert int(st.item()) == st_o
     assert np.array_equal(pool.cpu().numpy(), pool_h)
+
+
+def test_copy_blocks_racing_pairs_refused_nothing_launched(lmc):
+    """A batch whose pairs would race (a destination another pair reads, in
+    another KV group) is refused before any launch: the pool and the status
+    word stay as they were. Split into two calls, the same copies run and
+    match the oracle applying them in that order."""
+    o = oracle.layout(W.CONFIGS[0].layers, 64, False, 1 << 24)
+    p = lmc.lmc_layout_build(W.CONFIGS[0].layers, 64, False, 1 << 24)
+    e0 = np.zeros(0, dtype=oracle.PAIR_DTYPE)
+    first = [np.array([(1, 9)], dtype=oracle.PAIR_DTYPE), e0, e0, e0]
+    second = [e0, e0, np.array([(9, 12)], dtype=oracle.PAIR_DTYPE), e0]
+    racing = [first[0], e0, second[2], e0]
+    pool_h = W.fill_normal_np(o.pool_bytes, 19)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    st = torch.full((1,), 0x40, dtype=torch.int32, device=DEV)
+    with pytest.raises(lmc.LmcError) as e:
+        lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in racing], racing, st)
+    assert e.value.code == lmc.LMC_ERR_OVERLAP
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0x40 and np.array_equal(pool.cpu().numpy(), pool_h)
+    for part in (first, second):
+        lmc.lmc_copy_blocks(p, pool, [lmc.pairs_to_device(x, DEV) for x in part], part, st)
+        assert oracle.copy_blocks(o, pool_h, part) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0x40 and np.array_equal(pool.cpu().numpy(), pool_h)
 
 
 def test_copy_blocks_full_size_kda_states(lmc):

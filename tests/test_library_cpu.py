@@ -512,3 +512,49 @@ def test_every_declaration_is_documented():
         assert before.endswith("*/") or re.search(r"LMC_API[^;]*;\s*$", before), m.group(1)
         names.append(m.group(1))
     assert len(names) >= 20
+
+
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except ImportError:
+        return True
+
+
+@pytest.mark.skipif(not _no_gpu(), reason="passes dummy host pointers to launch-capable calls")
+def test_store_size_limits_refused_before_launch(lmc):
+    """Sizes the launch plan cannot hold are refused on the host: a page of
+    2 GiB or more (INVALID_ARG), an object of more than 2^31 tiles, a chunk of
+    more than 2^31 blocks (OVERFLOW). Without a GPU, a call that passed the
+    checks would fail only at the launch, with LMC_ERR_CUDA."""
+    buf = (ctypes.c_uint8 * 256)()
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+
+    def batch(L):
+        tables = (lmc.lmc_block_table * L.num_kv_groups)(*[lmc.lmc_block_table(addr, 4, 4)] * L.num_kv_groups)
+        jobs = (ctypes.c_void_p * L.num_object_groups)(*[addr] * L.num_object_groups)
+        counts = (ctypes.c_int64 * L.num_object_groups)(*[1] * L.num_object_groups)
+        return lmc.lmc_batch(1, L.num_kv_groups, tables, L.num_object_groups, 0, jobs, counts), (tables, jobs, counts)
+
+    store = lmc._lib.lmc_store
+    # a 3 GiB KDA state page
+    big = [{"kind": "KDA", "token_bytes": 0, "conv_bytes": 0, "rec_bytes": 3 << 30, "window": 0}]
+    L = lmc.lmc_layout_build(big, 16, True, 4 << 30)
+    b, keep = batch(L)
+    assert store(L.handle, 16, addr, ctypes.byref(b), addr, 1 << 40, addr, None) == lmc.LMC_ERR_INVALID_ARG
+    # 2 GiB - 1 MiB attention pages (65,504 tiles each), 40,000 of them per object
+    page = (2 << 30) - (1 << 20)
+    L = lmc.lmc_layout_build([W.mla(page)], 1, True, 4 << 30)
+    b, keep = batch(L)
+    assert store(L.handle, 40_000, addr, ctypes.byref(b), addr, 1 << 62, addr, None) == lmc.LMC_ERR_OVERFLOW
+    # one block more than 2^31 per chunk
+    L = lmc.lmc_layout_build([W.mla(16)], 1, True, 1 << 20)
+    b, keep = batch(L)
+    assert store(L.handle, (1 << 31) + 1, addr, ctypes.byref(b), addr, 1 << 62, addr, None) == lmc.LMC_ERR_OVERFLOW
+    # the largest page the plan holds passes every host check and fails only at the launch
+    ok = (2 << 30) - (1 << 16)
+    L = lmc.lmc_layout_build([{"kind": "KDA", "token_bytes": 0, "conv_bytes": 0, "rec_bytes": ok, "window": 0}],
+                             16, True, 4 << 30)
+    b, keep = batch(L)
+    assert store(L.handle, 16, addr, ctypes.byref(b), addr, 1 << 40, addr, None) == lmc.LMC_ERR_CUDA
