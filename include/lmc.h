@@ -340,12 +340,14 @@ LMC_API int lmc_copy_blocks(const lmc_layout *layout, void *pool, const lmc_copy
  * blocks. Given two chunk-form batches whose block tables and jobs are in
  * HOST memory (the copies the caller built them from), computes the blocks
  * each one's objects read or write, exactly as lmc_store / lmc_load address
- * them (a paged layer's m = chunk_size / N positions of the chunk, a KDA
- * layer's chunk-end position; entries the kernels would skip touch nothing),
- * and returns LMC_OK when no block is touched by both, else LMC_ERR_OVERLAP
- * with *out_block (if not NULL) = the smallest shared block id (-1 when
- * disjoint). Errors: INVALID_ARG, NOT_MULTIPLE, OVERFLOW. Host only; nothing
- * enqueued. */
+ * them: a paged layer's m = chunk_size / N positions of the chunk, a KDA
+ * layer's chunk-end position. A job naming no request of its batch or a
+ * negative chunk, a position past its table and an id outside the pool
+ * touch nothing. Arena offsets are not looked at (there is no arena), so a
+ * job the kernels would refuse for its offset still counts. Returns LMC_OK
+ * when no block is touched by both, else LMC_ERR_OVERLAP with *out_block
+ * (if not NULL) = the smallest shared block id (-1 when disjoint).
+ * Errors: INVALID_ARG, NOT_MULTIPLE, OVERFLOW. Host only; nothing enqueued. */
 LMC_API int lmc_check_disjoint(const lmc_layout *layout, int64_t chunk_size, const lmc_batch *a, const lmc_batch *b,
                                int32_t *out_block);
 
