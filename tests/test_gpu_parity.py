@@ -290,7 +290,13 @@ def _full_size(lmc, cfg, request_ids=None):
     del pool
     assert check_load_streamed(Lo, C, fresh, arena, inp.jobs, inp.object_bytes, inp.tables_dst,
                                load_o) == inp.payload_bytes
-    del arena
+    torch.cuda.empty_cache()
+    # store after load, under the load's tables, reproduces every object
+    again = torch.full_like(arena, ARENA_FILL)
+    lmc.lmc_store(Lp, C, fresh, t_dst, jobs, again, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(arena, again)
+    del arena, again
     torch.cuda.empty_cache()
     assert check_untouched(inp, fresh, inp.jobs, inp.tables_dst, inp.arena_bytes, W.SENTINEL)
 
