@@ -37,8 +37,11 @@
  * Parity status: negotiation and layout sizes are pinned by values and
  * closed forms from the pages; store/load are pinned by invariants (identity,
  * untouched bytes) and by an independent per-token brute force; the codec by
- * worked rows and an independent float32 restatement. The byte order inside
- * an object is a reading, not a value from the pages.
+ * worked rows and an independent float32 restatement; the rule refusing
+ * racing block copies by the brute force applying each batch in several
+ * orders; the mixed step's disjointness check by the brute force storing
+ * each batch from a pool whose pages hold their block id. The byte order
+ * inside an object is a reading, not a value from the pages.
  */
 #include <math.h>
 #include <stdint.h>
