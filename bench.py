@@ -576,7 +576,7 @@ class PagingStep:
             self.s_in = T.cuda.Stream(self.dev)
             self.s_load = T.cuda.Stream(self.dev)
         self.h_status = T.zeros(1, dtype=T.int32, pin_memory=True)
-        self.host_memory = self._host[0].kind
+        self.host_memory = "; ".join(h.kind for h in self._host)
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_tables) + \
             sum(j.numel() for j in self.h_jobs) + objs_in
         self.d2h = objs_out + 4
