@@ -370,7 +370,9 @@ LMC_API int lmc_check_disjoint(const lmc_layout *layout, int64_t chunk_size, con
  * recurrent state a whole number of rows and a multiple of 4 rows, and
  * conv_bytes a multiple of 16, so records stay multiples of 16 bytes
  * (INVALID_ARG otherwise), and 16-byte aligned pool and arena (ALIGN).
- * Other arguments, status bits and errors as lmc_store / lmc_load. */
+ * Every layout of up to LMC_MAX_LAYERS layers fits one launch, KDA layers
+ * included (their records take two launch-plan entries each). Other
+ * arguments, status bits and errors as lmc_store / lmc_load. */
 LMC_API int lmc_store_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, const void *pool,
                  const lmc_batch *batch, void *arena, int64_t arena_bytes, uint32_t *status, void *stream);
 LMC_API int lmc_load_q8(const lmc_layout *layout, int64_t chunk_size, int64_t row_elems, void *pool,
