@@ -530,6 +530,42 @@ def test_q8_random_specs_exact(lmc, t):
         _blocks_exact(lmc, inp, Lp, "tails", d=d)
 
 
+def test_block_objects_full_size_tails(lmc):
+    """The lognormal Kimi-Linear batch's tail objects at full size: for each
+    request, the whole blocks past its last whole chunk (one to N - 1 of
+    them, last-block snapshot), grouped by block count; every object and
+    every loaded page against the oracle."""
+    cfg = W.CONFIGS[2]
+    inp, Lp = case_inputs(cfg)
+    Lo, C = inp.layout, inp.C
+    pool = torch.empty(Lo.pool_bytes, dtype=torch.uint8, device=DEV)
+    W.fill_normal(pool, 78)
+    t_src, t_dst = dev_tables(inp.tables_src, DEV), dev_tables(inp.tables_dst, DEV)
+    shapes = _block_units(inp, "tails")
+    assert shapes
+    for nb, every, units in shapes:
+        sizes = [Lo.object_bytes_blocks(nb, every, g) for g in range(Lo.num_object_groups)]
+        assert [Lp.object_bytes_blocks(nb, every, g) for g in range(Lo.num_object_groups)] == sizes
+        jobs, nbytes = W.pack_jobs(units, sizes)
+        arena = torch.full((nbytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
+        fresh = torch.full((Lo.pool_bytes,), W.SENTINEL, dtype=torch.uint8, device=DEV)
+        st = _status()
+        dj = dev_jobs(jobs, DEV)
+        lmc.lmc_store_blocks(Lp, nb, lmc.LMC_KDA_LAST_BLOCK, pool, t_src, dj, arena, st)
+        lmc.lmc_load_blocks(Lp, nb, lmc.LMC_KDA_LAST_BLOCK, fresh, t_dst, dj, arena, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        payload = sum(sizes[g] * len(J) for g, J in enumerate(jobs))
+        assert check_store_streamed(
+            Lo, C, pool, arena, jobs, sizes, inp.tables_src,
+            lambda p, t, j, a: oracle.store_blocks(Lo, nb, False, p, t, j, a), nb=nb) == payload
+        assert check_load_streamed(
+            Lo, C, fresh, arena, jobs, sizes, inp.tables_dst,
+            lambda p, t, j, a: oracle.load_blocks(Lo, nb, False, p, t, j, a), nb=nb) == payload
+        del arena, fresh
+        torch.cuda.empty_cache()
+
+
 def test_q8_block_objects_full_size_every_block(lmc):
     """The lognormal Kimi-Linear batch (packed, chunk 2N) as block objects of
     2 blocks with every snapshot an INT8 record (d = 128): every record and

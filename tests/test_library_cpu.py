@@ -291,6 +291,12 @@ def test_check_disjoint_matches_oracle(lmc):
     cfg = W.CONFIGS[4]
     C = lmc.lmc_negotiate_chunk(cfg.requested_chunk, cfg.N)
     import functools
+    full = W.make_inputs(cfg, functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed), C)
+    pf = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, full.layout.pool_bytes)
+    Tf = full.tables_src
+    # the whole mixed workload (256 requests) is disjoint on both sides
+    assert oracle.check_disjoint(full.layout, C, Tf, full.load_jobs, Tf, full.store_jobs) == -1
+    assert lmc.lmc_check_disjoint(pf, C, Tf, full.load_jobs, Tf, full.store_jobs) == -1
     inp = W.make_inputs(cfg, functools.partial(oracle.layout, cfg.layers, cfg.N, cfg.packed), C, list(range(40)))
     o = inp.layout
     p = lmc.lmc_layout_build(cfg.layers, cfg.N, cfg.packed, o.pool_bytes)
