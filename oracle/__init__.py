@@ -166,6 +166,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.or_copy_blocks.argtypes = [P(_Layout), ctypes.c_void_p, P(_CopyBatch), P(ctypes.c_uint32)]
     lib.or_check_disjoint.argtypes = [P(_Layout), ctypes.c_int64, P(_Tables), P(_Jobs), P(_Tables), P(_Jobs),
                                       P(ctypes.c_int32)]
+    lib.or_check_disjoint_blocks.argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int, P(_Tables), P(_Jobs),
+                                             P(_Tables), P(_Jobs), P(ctypes.c_int32)]
     for name in ("or_store_q8", "or_load_q8"):
         getattr(lib, name).argtypes = [P(_Layout), ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, P(_Tables),
                                        P(_Jobs), ctypes.c_void_p, ctypes.c_int64, P(ctypes.c_uint32)]
@@ -473,14 +475,20 @@ def copy_blocks(L: Layout, pool: np.ndarray, pairs) -> int:
     return st.value
 
 
-def check_disjoint(L: Layout, C: int, tables_a, jobs_a, tables_b, jobs_b) -> int:
+def check_disjoint(L: Layout, C: int, tables_a, jobs_a, tables_b, jobs_b, nb: int = 0,
+                   kda_every: bool = False) -> int:
     """-1 when the chunk batches (tables_a, jobs_a) and (tables_b, jobs_b)
-    touch disjoint blocks, else the smallest block both touch."""
+    touch disjoint blocks, else the smallest block both touch. nb > 0
+    selects the block-granular form (C is then ignored)."""
     Ta, Ja, keep_a = _marshal(L, tables_a, jobs_a)
     Tb, Jb, keep_b = _marshal(L, tables_b, jobs_b)
     out = ctypes.c_int32(0)
-    rc = L._lib.or_check_disjoint(ctypes.byref(L._c), int(C), ctypes.byref(Ta), ctypes.byref(Ja), ctypes.byref(Tb),
-                                  ctypes.byref(Jb), ctypes.byref(out))
+    if nb:
+        rc = L._lib.or_check_disjoint_blocks(ctypes.byref(L._c), int(nb), int(bool(kda_every)), ctypes.byref(Ta),
+                                             ctypes.byref(Ja), ctypes.byref(Tb), ctypes.byref(Jb), ctypes.byref(out))
+    else:
+        rc = L._lib.or_check_disjoint(ctypes.byref(L._c), int(C), ctypes.byref(Ta), ctypes.byref(Ja),
+                                      ctypes.byref(Tb), ctypes.byref(Jb), ctypes.byref(out))
     if rc == ERR_OVERLAP:
         return out.value
     if rc != OK:

@@ -894,13 +894,14 @@ int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, ui
     return OR_OK;
 }
 
-/* Sets `bit` in map[b] for every block b whose pages the chunk objects of a
- * batch read (store) or write (load): per job of object group og and per
- * layer of og, the chunk's C / N positions of a paged layer's block table,
- * or the chunk-end position of a KDA layer's ([KL] snapshots at block
- * boundaries). A job naming no request of the batch or a negative chunk,
+/* Sets `bit` in map[b] for every block b whose pages the objects of a
+ * batch read (store) or write (load). An object covers nb block positions
+ * from `first` (chunk jobs: chunk * nb; block jobs: the job's own value):
+ * all of them for a paged layer; for a KDA layer the last one, the state at
+ * the object's end ([KL] snapshots at block boundaries), or all of them
+ * with kda_every. A job naming no request of the batch or a negative chunk,
  * a position past the table, and an id outside the pool mark nothing. */
-static int mark_blocks(const or_layout *L, int64_t m, const or_tables *T, const or_jobs *J,
+static int mark_blocks(const or_layout *L, const obj_shape *sh, const or_tables *T, const or_jobs *J,
                        uint8_t *map, uint8_t bit)
 {
     int rc = check_tables(L, T);
@@ -920,8 +921,9 @@ static int mark_blocks(const or_layout *L, int64_t m, const or_tables *T, const 
                 if (L->object_group[i] != og)
                     continue;
                 int k = L->kv_group[i];
-                int64_t lo = c * m, hi = c * m + m; /* positions [lo, hi) */
-                if (L->layers[i].kind == OR_KDA)
+                int64_t first = sh->first_is_block ? c : c * sh->nb;
+                int64_t lo = first, hi = first + sh->nb; /* positions [lo, hi) */
+                if (L->layers[i].kind == OR_KDA && !sh->kda_every)
                     lo = hi - 1;
                 for (int64_t pos = lo; pos < hi && pos < T->num_cols[k]; pos++) {
                     int64_t b = T->table[k][r * T->row_stride[k] + pos];
@@ -937,19 +939,15 @@ static int mark_blocks(const or_layout *L, int64_t m, const or_tables *T, const 
 /* A load and a store issued at the same time on one pool (the mixed
  * serving step) must touch disjoint blocks. *out_block = the smallest block
  * both touch, or -1. */
-int or_check_disjoint(const or_layout *L, int64_t C, const or_tables *Ta, const or_jobs *Ja,
-                      const or_tables *Tb, const or_jobs *Jb, int32_t *out_block)
+static int disjoint(const or_layout *L, const obj_shape *sh, const or_tables *Ta, const or_jobs *Ja,
+                    const or_tables *Tb, const or_jobs *Jb, int32_t *out_block)
 {
-    if (L == NULL || out_block == NULL)
-        return OR_ERR_INVALID_ARG;
-    if (C <= 0 || C % L->N != 0)
-        return OR_ERR_NOT_MULTIPLE;
     uint8_t *map = calloc((size_t)L->num_blocks + 1, 1);
     if (map == NULL)
         return OR_ERR_INVALID_ARG;
-    int rc = mark_blocks(L, C / L->N, Ta, Ja, map, 1);
+    int rc = mark_blocks(L, sh, Ta, Ja, map, 1);
     if (rc == OR_OK)
-        rc = mark_blocks(L, C / L->N, Tb, Jb, map, 2);
+        rc = mark_blocks(L, sh, Tb, Jb, map, 2);
     *out_block = -1;
     if (rc == OR_OK) {
         for (int64_t b = 0; b < L->num_blocks; b++) {
@@ -962,6 +960,26 @@ int or_check_disjoint(const or_layout *L, int64_t C, const or_tables *Ta, const 
     }
     free(map);
     return rc;
+}
+
+int or_check_disjoint(const or_layout *L, int64_t C, const or_tables *Ta, const or_jobs *Ja,
+                      const or_tables *Tb, const or_jobs *Jb, int32_t *out_block)
+{
+    if (L == NULL || out_block == NULL)
+        return OR_ERR_INVALID_ARG;
+    obj_shape sh;
+    int rc = chunk_shape(L, C, &sh);
+    return rc != OR_OK ? rc : disjoint(L, &sh, Ta, Ja, Tb, Jb, out_block);
+}
+
+int or_check_disjoint_blocks(const or_layout *L, int64_t nb, int kda_every, const or_tables *Ta,
+                             const or_jobs *Ja, const or_tables *Tb, const or_jobs *Jb, int32_t *out_block)
+{
+    if (L == NULL || out_block == NULL)
+        return OR_ERR_INVALID_ARG;
+    obj_shape sh;
+    int rc = block_shape(nb, kda_every, &sh);
+    return rc != OR_OK ? rc : disjoint(L, &sh, Ta, Ja, Tb, Jb, out_block);
 }
 
 /* Smallest multiple of `align` tokens whose attention page

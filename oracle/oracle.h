@@ -147,6 +147,8 @@ typedef struct {
 int or_copy_blocks(const or_layout *L, uint8_t *pool, const or_copy_batch *B, uint32_t *status);
 int or_check_disjoint(const or_layout *L, int64_t C, const or_tables *Ta, const or_jobs *Ja,
                       const or_tables *Tb, const or_jobs *Jb, int32_t *out_block);
+int or_check_disjoint_blocks(const or_layout *L, int64_t nb, int kda_every, const or_tables *Ta,
+                             const or_jobs *Ja, const or_tables *Tb, const or_jobs *Jb, int32_t *out_block);
 
 int or_store_q8(const or_layout *L, int64_t C, int64_t d, const uint8_t *pool,
                 const or_tables *T, const or_jobs *J,

@@ -134,6 +134,8 @@ def _bind(so: ctypes.CDLL) -> ctypes.CDLL:
     so.lmc_copy_blocks.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(lmc_copy_batch), ctypes.c_void_p,
                                    ctypes.c_void_p]
     so.lmc_check_disjoint.argtypes = [ctypes.c_void_p, _i64, _P(lmc_batch), _P(lmc_batch), _P(ctypes.c_int32)]
+    so.lmc_check_disjoint_blocks.argtypes = [ctypes.c_void_p, _i64, ctypes.c_int32, _P(lmc_batch), _P(lmc_batch),
+                                             _P(ctypes.c_int32)]
     for name in ("lmc_store_q8", "lmc_load_q8"):
         getattr(so, name).argtypes = [ctypes.c_void_p, _i64, _i64, ctypes.c_void_p, _P(lmc_batch), ctypes.c_void_p,
                                       _i64, ctypes.c_void_p, ctypes.c_void_p]
@@ -539,6 +541,21 @@ def lmc_check_disjoint(layout: Layout, chunk: int, tables_a, jobs_a, tables_b, j
     if rc == LMC_ERR_OVERLAP:
         return out.value
     _check(rc, "lmc_check_disjoint")
+    return -1
+
+
+def lmc_check_disjoint_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, tables_a, jobs_a, tables_b,
+                              jobs_b) -> int:
+    """lmc_check_disjoint for block-granular batches (jobs name their first
+    block position): -1 when disjoint, else the smallest shared block."""
+    a, keep_a = _host_batch(layout, tables_a, jobs_a)
+    b, keep_b = _host_batch(layout, tables_b, jobs_b)
+    out = ctypes.c_int32(0)
+    rc = _lib.lmc_check_disjoint_blocks(layout.handle, int(blocks_per_object), int(kda_mode), ctypes.byref(a),
+                                        ctypes.byref(b), ctypes.byref(out))
+    if rc == LMC_ERR_OVERLAP:
+        return out.value
+    _check(rc, "lmc_check_disjoint_blocks")
     return -1
 
 

@@ -19,13 +19,15 @@ namespace {
 
 bool valid_block(int64_t b, int64_t num_blocks) { return b >= 0 && b < num_blocks; }
 
-// Blocks whose pages the objects of `b` read (store) or write (load), in
-// chunk form: for each job of object group og and each layer of og, the
-// chunk's m positions of a paged layer's block table, or the chunk-end
-// position of a KDA layer's. Entries the kernels would skip (a request or
-// chunk out of range, a position past the table, -1 or an id outside the
-// pool) touch nothing. Appends the ids to `out`.
-int touched_blocks(const lmc_layout *L, int64_t m, const lmc_batch *b, std::vector<int32_t> &out) {
+// Blocks whose pages the objects of `b` read (store) or write (load). An
+// object covers nb block positions from job.chunk * pos_mul (chunk form:
+// pos_mul = nb = C / N; block form: pos_mul = 1): all nb positions of a
+// paged layer's block table, and of a KDA layer's either the last one or,
+// with kda_every, all nb. Entries the kernels would skip (a request or chunk
+// out of range, a position past the table, -1 or an id outside the pool)
+// touch nothing. Appends the ids to `out`.
+int touched_blocks(const lmc_layout *L, int64_t nb, int64_t pos_mul, bool kda_every, const lmc_batch *b,
+                   std::vector<int32_t> &out) {
     const int nkv = (int)L->kv_group_kind.size();
     const int nog = (int)L->object_group_layers.size();
     if (b == nullptr || b->num_requests < 0 || b->num_kv_groups != nkv || b->num_object_groups != nog ||
@@ -53,9 +55,9 @@ int touched_blocks(const lmc_layout *L, int64_t m, const lmc_batch *b, std::vect
                 continue;
             for (const auto &r : reads) {
                 const lmc_block_table &t = b->tables[r.first];
-                const int64_t first = (int64_t)job.chunk * m;
-                const int64_t lo = r.second ? first + m - 1 : first;
-                for (int64_t p = lo; p < first + m && p < t.num_cols; p++) {
+                const int64_t first = (int64_t)job.chunk * pos_mul;
+                const int64_t lo = r.second && !kda_every ? first + nb - 1 : first;
+                for (int64_t p = lo; p < first + nb && p < t.num_cols; p++) {
                     const int32_t id = t.table[(int64_t)job.request * t.row_stride + p];
                     if (valid_block(id, L->num_blocks))
                         out.push_back(id);
@@ -104,19 +106,14 @@ int check_copy_pairs(const lmc_layout *L, const lmc_copy_batch *b) {
 
 }  // namespace lmc
 
-extern "C" int lmc_check_disjoint(const lmc_layout *L, int64_t chunk_size, const lmc_batch *a, const lmc_batch *b,
-                                  int32_t *out_block) {
-    if (L == nullptr || a == nullptr || b == nullptr)
-        return LMC_ERR_INVALID_ARG;
-    if (chunk_size <= 0 || chunk_size % L->block_size != 0)
-        return LMC_ERR_NOT_MULTIPLE;
-    const int64_t m = chunk_size / L->block_size;
-    if (m > INT32_MAX)
-        return LMC_ERR_OVERFLOW;
+namespace {
+
+int disjoint(const lmc_layout *L, int64_t nb, int64_t pos_mul, bool kda_every, const lmc_batch *a,
+             const lmc_batch *b, int32_t *out_block) {
     std::vector<int32_t> ta, tb;
-    int rc = touched_blocks(L, m, a, ta);
+    int rc = touched_blocks(L, nb, pos_mul, kda_every, a, ta);
     if (rc == LMC_OK)
-        rc = touched_blocks(L, m, b, tb);
+        rc = touched_blocks(L, nb, pos_mul, kda_every, b, tb);
     if (rc != LMC_OK)
         return rc;
     std::sort(ta.begin(), ta.end());
@@ -126,4 +123,26 @@ extern "C" int lmc_check_disjoint(const lmc_layout *L, int64_t chunk_size, const
     if (out_block != nullptr)
         *out_block = common.empty() ? -1 : common.front();
     return common.empty() ? LMC_OK : LMC_ERR_OVERLAP;
+}
+
+}  // namespace
+
+extern "C" int lmc_check_disjoint(const lmc_layout *L, int64_t chunk_size, const lmc_batch *a, const lmc_batch *b,
+                                  int32_t *out_block) {
+    if (L == nullptr || a == nullptr || b == nullptr)
+        return LMC_ERR_INVALID_ARG;
+    if (chunk_size <= 0 || chunk_size % L->block_size != 0)
+        return LMC_ERR_NOT_MULTIPLE;
+    const int64_t m = chunk_size / L->block_size;
+    if (m > INT32_MAX)
+        return LMC_ERR_OVERFLOW;
+    return disjoint(L, m, m, false, a, b, out_block);
+}
+
+extern "C" int lmc_check_disjoint_blocks(const lmc_layout *L, int64_t blocks_per_object, int32_t kda_mode,
+                                         const lmc_batch *a, const lmc_batch *b, int32_t *out_block) {
+    if (L == nullptr || a == nullptr || b == nullptr || blocks_per_object <= 0 || blocks_per_object > INT32_MAX ||
+        (kda_mode != LMC_KDA_LAST_BLOCK && kda_mode != LMC_KDA_EVERY_BLOCK))
+        return LMC_ERR_INVALID_ARG;
+    return disjoint(L, blocks_per_object, 1, kda_mode == LMC_KDA_EVERY_BLOCK, a, b, out_block);
 }

@@ -905,6 +905,47 @@ def check_disjoint(lib):
         seen_shared += want >= 0
         assert oracle.check_disjoint(L, C, tables, lj, tables, inp.store_jobs) == want, (t, want)
     assert seen_shared >= 5
+    # block-granular batches: the stored chunks as objects of m blocks from
+    # their first block, KDA layers holding the last snapshot or every one;
+    # the two sides are the even and the odd requests' stores (every block
+    # position of those objects holds a block, as the brute force needs)
+    m = C // 4
+
+    def block_jobs(jobs, every, parity):
+        units = [[(int(j["request"]), int(j["chunk"]) * m) for j in J if int(j["request"]) % 2 == parity]
+                 for J in jobs]
+        sizes = [L.object_bytes_blocks(m, every, g) for g in range(L.num_object_groups)]
+        return W.pack_jobs(units, sizes)
+
+    def block_tags(tables, jobs, nbytes, every):
+        arena = np.full(nbytes, 0xFF, dtype=np.uint8)
+        brute.store(B, C, pool, tables, jobs, arena, nb=m, kda_every=every)
+        return set(int(x) for x in np.unique(arena.view(np.int32)) if x >= 0)
+
+    kda_og = L.object_group[[l["kind"] for l in layers].index("KDA")]
+    kda_kv = sorted({L.kv_group[i] for i in range(len(layers)) if layers[i]["kind"] == "KDA"})
+    for every in (False, True):
+        (aj, an), (bj, bn) = block_jobs(inp.store_jobs, every, 0), block_jobs(inp.store_jobs, every, 1)
+        b_side = sorted(block_tags(inp.tables_src, bj, bn, every))
+        hits = 0
+        for t in range(16):
+            tables = [x.copy() for x in inp.tables_src]
+            if t % 2:
+                # the first (not the last) KDA position of one even-request
+                # object now holds a block the odd requests read
+                job = aj[kda_og][int(rng.integers(0, len(aj[kda_og])))]
+                k = kda_kv[int(rng.integers(0, len(kda_kv)))]
+                tables[k][int(job["request"]), int(job["chunk"])] = b_side[int(rng.integers(0, len(b_side)))]
+            elif t:
+                k = int(rng.integers(0, len(tables)))
+                r, c = np.argwhere(tables[k] >= 0)[int(rng.integers(0, int((tables[k] >= 0).sum())))]
+                tables[k][r, c] = b_side[int(rng.integers(0, len(b_side)))]
+            common = block_tags(tables, aj, an, every) & block_tags(tables, bj, bn, every)
+            want = min(common) if common else -1
+            hits += want >= 0
+            got = oracle.check_disjoint(L, C, tables, aj, tables, bj, nb=m, kda_every=every)
+            assert got == want, (every, t, got, want)
+        assert hits >= (8 if every else 1), (every, hits)
 
 
 ALL = ["check_negotiation_golden", "check_negotiation_bruteforce", "check_negotiation_edges",

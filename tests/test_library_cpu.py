@@ -328,6 +328,20 @@ def test_check_disjoint_matches_oracle(lmc):
     with pytest.raises(lmc.LmcError) as e:
         lmc.lmc_check_disjoint(p, C + 1, T, inp.load_jobs, T, inp.store_jobs)
     assert e.value.code == lmc.LMC_ERR_NOT_MULTIPLE
+    # block-granular batches (first block position, nb blocks per object), both KDA modes
+    for nb in (1, 2, 3):
+        for every in (False, True):
+            mode = lmc.LMC_KDA_EVERY_BLOCK if every else lmc.LMC_KDA_LAST_BLOCK
+            for t in range(8):
+                bj = [J.copy() for J in inp.load_jobs]
+                sj = [J.copy() for J in inp.store_jobs]
+                for J in bj + sj:
+                    J["chunk"] = J["chunk"] * int(C // cfg.N) + int(rng.integers(0, 2))
+                a = oracle.check_disjoint(o, C, T, bj, T, sj, nb=nb, kda_every=every)
+                assert lmc.lmc_check_disjoint_blocks(p, nb, mode, T, bj, T, sj) == a, (nb, every, t)
+    with pytest.raises(lmc.LmcError) as e:
+        lmc.lmc_check_disjoint_blocks(p, 0, lmc.LMC_KDA_LAST_BLOCK, T, inp.load_jobs, T, inp.store_jobs)
+    assert e.value.code == lmc.LMC_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("cfg_index", [0, 1, 3])

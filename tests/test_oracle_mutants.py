@@ -65,6 +65,9 @@ MUTANTS = [
     ("disjoint check marks a KDA layer's first position", "lo = hi - 1;", "lo = lo + 0;"),
     ("disjoint check drops a chunk's last paged position", "pos < hi && pos < T->num_cols[k]",
      "pos < hi - 1 + (L->layers[i].kind == OR_KDA) && pos < T->num_cols[k]"),
+    ("block-form disjoint check ignores every-block snapshots",
+     "if (L->layers[i].kind == OR_KDA && !sh->kda_every)\n                    lo = hi - 1;",
+     "if (L->layers[i].kind == OR_KDA)\n                    lo = hi - 1;"),
 ]
 
 
