@@ -355,8 +355,10 @@ LMC_API int lmc_check_disjoint(const lmc_layout *layout, int64_t chunk_size, con
  * lmc_load_blocks address them): each job's object covers blocks_per_object
  * positions from its first block position, all of them for a paged layer,
  * and for a KDA layer the last one (LMC_KDA_LAST_BLOCK) or all of them
- * (LMC_KDA_EVERY_BLOCK). The INT8 forms address the same blocks. Results
- * as lmc_check_disjoint; errors INVALID_ARG. Host only; nothing enqueued. */
+ * (LMC_KDA_EVERY_BLOCK). The INT8 forms address the same blocks. When the
+ * two batches use different KDA modes, pass LMC_KDA_EVERY_BLOCK: it counts
+ * a superset of the blocks either form touches. Results as
+ * lmc_check_disjoint; errors INVALID_ARG. Host only; nothing enqueued. */
 LMC_API int lmc_check_disjoint_blocks(const lmc_layout *layout, int64_t blocks_per_object, int32_t kda_mode,
                                       const lmc_batch *a, const lmc_batch *b, int32_t *out_block);
 

@@ -335,10 +335,23 @@ def _batch(layout: Layout, tables, jobs):
     return b, (tarr, jarr, narr)
 
 
-def _stream_ptr(stream):
+def _stream_ptr(stream, *buffers):
+    """The stream's handle. When the call runs on a stream other than the
+    current one, every device tensor among `buffers` (nested lists
+    included) is marked as used by that stream, so that torch's caching
+    allocator does not hand its memory to a later allocation before the
+    call's kernels have read or written it."""
     import torch
     if stream is None:
         stream = torch.cuda.current_stream()
+    elif stream != torch.cuda.current_stream(stream.device):
+        todo = list(buffers)
+        while todo:
+            t = todo.pop()
+            if isinstance(t, (list, tuple)):
+                todo.extend(t)
+            elif isinstance(t, torch.Tensor) and t.is_cuda:
+                t.record_stream(stream)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -364,8 +377,9 @@ def lmc_store(layout: Layout, chunk: int, pool, tables, jobs, arena, status, str
     the 4-byte `status` tensor."""
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_store(layout.handle, int(chunk), pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
-                          arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+                          arena.numel() * arena.element_size(), status.data_ptr(), strm),
            "lmc_store")
 
 
@@ -373,8 +387,9 @@ def lmc_load(layout: Layout, chunk: int, pool, tables, jobs, arena, status, stre
     """Scatters the jobs' objects from `arena` into `pool` (device tensors)."""
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_load(layout.handle, int(chunk), pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
-                         arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+                         arena.numel() * arena.element_size(), status.data_ptr(), strm),
            "lmc_load")
 
 
@@ -383,18 +398,20 @@ def lmc_store_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool
     """Block-granular store: each job's `chunk` field is its first block position."""
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_store_blocks(layout.handle, int(blocks_per_object), int(kda_mode), pool.data_ptr(),
                                  ctypes.byref(b), arena.data_ptr(), arena.numel() * arena.element_size(),
-                                 status.data_ptr(), _stream_ptr(stream)), "lmc_store_blocks")
+                                 status.data_ptr(), strm), "lmc_store_blocks")
 
 
 def lmc_load_blocks(layout: Layout, blocks_per_object: int, kda_mode: int, pool, tables, jobs, arena, status,
                     stream=None) -> None:
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_load_blocks(layout.handle, int(blocks_per_object), int(kda_mode), pool.data_ptr(),
                                 ctypes.byref(b), arena.data_ptr(), arena.numel() * arena.element_size(),
-                                status.data_ptr(), _stream_ptr(stream)), "lmc_load_blocks")
+                                status.data_ptr(), strm), "lmc_load_blocks")
 
 
 def lmc_object_bytes_q8(layout: Layout, chunk: int, row_elems: int, object_group: int) -> int:
@@ -409,18 +426,20 @@ def lmc_store_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs,
     """Chunk store with KDA snapshots as INT8 records (rows of `row_elems`)."""
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_store_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
-                             arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
-                             _stream_ptr(stream)), "lmc_store_q8")
+                             arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(), strm),
+           "lmc_store_q8")
 
 
 def lmc_load_q8(layout: Layout, chunk: int, row_elems: int, pool, tables, jobs, arena, status,
                 stream=None) -> None:
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_load_q8(layout.handle, int(chunk), int(row_elems), pool.data_ptr(), ctypes.byref(b),
-                            arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(),
-                            _stream_ptr(stream)), "lmc_load_q8")
+                            arena.data_ptr(), arena.numel() * arena.element_size(), status.data_ptr(), strm),
+           "lmc_load_q8")
 
 
 def lmc_object_bytes_blocks_q8(layout: Layout, blocks_per_object: int, kda_mode: int, row_elems: int,
@@ -436,9 +455,10 @@ def lmc_store_blocks_q8(layout: Layout, blocks_per_object: int, kda_mode: int, r
     """Block-granular store with the stored KDA snapshots as INT8 records."""
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_store_blocks_q8(layout.handle, int(blocks_per_object), int(kda_mode), int(row_elems),
                                     pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
-                                    arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+                                    arena.numel() * arena.element_size(), status.data_ptr(), strm),
            "lmc_store_blocks_q8")
 
 
@@ -446,15 +466,17 @@ def lmc_load_blocks_q8(layout: Layout, blocks_per_object: int, kda_mode: int, ro
                        arena, status, stream=None) -> None:
     _check_launch(layout, pool, arena, status)
     b, keep = _batch(layout, tables, jobs)
+    strm = _stream_ptr(stream, pool, tables, jobs, arena, status)
     _check(_lib.lmc_load_blocks_q8(layout.handle, int(blocks_per_object), int(kda_mode), int(row_elems),
                                    pool.data_ptr(), ctypes.byref(b), arena.data_ptr(),
-                                   arena.numel() * arena.element_size(), status.data_ptr(), _stream_ptr(stream)),
+                                   arena.numel() * arena.element_size(), status.data_ptr(), strm),
            "lmc_load_blocks_q8")
 
 
 def lmc_selftest_wait(status, rounds: int, stream=None) -> None:
     """Runs the bounded-wait self-test: LMC_ST_TIMEOUT lands in `status`."""
-    _check(_lib.lmc_selftest_wait(status.data_ptr(), int(rounds), _stream_ptr(stream)), "lmc_selftest_wait")
+    strm = _stream_ptr(stream, status)
+    _check(_lib.lmc_selftest_wait(status.data_ptr(), int(rounds), strm), "lmc_selftest_wait")
 
 
 def lmc_selftest_row_scale(amax, scale, inv, ieee, stream=None) -> None:
@@ -464,8 +486,9 @@ def lmc_selftest_row_scale(amax, scale, inv, ieee, stream=None) -> None:
     for t in (scale, inv, ieee):
         if t.numel() != n:
             raise ValueError("lmc_selftest_row_scale: output sizes differ from amax")
-    _check(_lib.lmc_selftest_row_scale(amax.data_ptr(), scale.data_ptr(), inv.data_ptr(), ieee.data_ptr(), n,
-                                       _stream_ptr(stream)), "lmc_selftest_row_scale")
+    strm = _stream_ptr(stream, amax, scale, inv, ieee)
+    _check(_lib.lmc_selftest_row_scale(amax.data_ptr(), scale.data_ptr(), inv.data_ptr(), ieee.data_ptr(), n, strm),
+           "lmc_selftest_row_scale")
 
 
 def pairs_to_device(pairs: np.ndarray, device):
@@ -501,8 +524,9 @@ def lmc_copy_blocks(layout: Layout, pool, pairs, host_pairs, status, stream=None
         harr[k] = h.ctypes.data if nbytes else None
         narr[k] = nbytes // 8
     b = lmc_copy_batch(g, 0, parr, narr, harr)
-    _check(_lib.lmc_copy_blocks(layout.handle, pool.data_ptr(), ctypes.byref(b), status.data_ptr(),
-                                _stream_ptr(stream)), "lmc_copy_blocks")
+    strm = _stream_ptr(stream, pool, pairs, status)
+    _check(_lib.lmc_copy_blocks(layout.handle, pool.data_ptr(), ctypes.byref(b), status.data_ptr(), strm),
+           "lmc_copy_blocks")
 
 
 def _host_batch(layout: Layout, tables, jobs):

@@ -354,6 +354,86 @@ def test_mixed_step_exact_first_requests(lmc):
     assert np.array_equal(store_arena.cpu().numpy(), store_o)
 
 
+def test_mixed_step_block_objects_exact(lmc):
+    """The mixed step with block-granular objects: the cached chunks' load
+    and the new chunks' store as objects of C / N blocks from their first
+    block, then the same with one KDA snapshot per block (last-block and
+    every-block forms), issued together on two streams after the library's
+    block-form guard; compared in full with the oracle."""
+    inp, Lp = case_inputs(W.CONFIGS[4], request_ids=list(range(24)))
+    Lo, C = inp.layout, inp.C
+    m = C // Lo.N
+    for every in (False, True):
+        mode = lmc.LMC_KDA_EVERY_BLOCK if every else lmc.LMC_KDA_LAST_BLOCK
+        sizes = [Lo.object_bytes_blocks(m, every, g) for g in range(Lo.num_object_groups)]
+        units = lambda jobs: [[(int(j["request"]), int(j["chunk"]) * m) for j in J] for J in jobs]
+        # the load side holds only the hit boundary's KDA snapshot, so its
+        # KDA objects keep the last-block form
+        lj, ln = W.pack_jobs(units(inp.load_jobs), [Lo.object_bytes_blocks(m, False, g)
+                                                    for g in range(Lo.num_object_groups)])
+        sj, sn = W.pack_jobs(units(inp.store_jobs), sizes)
+        assert lmc.lmc_check_disjoint_blocks(Lp, m, lmc.LMC_KDA_LAST_BLOCK, inp.tables_src, lj,
+                                             inp.tables_src, sj) == -1
+        assert lmc.lmc_check_disjoint_blocks(Lp, m, mode, inp.tables_src, sj, inp.tables_src, lj) == -1
+        pool_h = W.fill_normal_np(Lo.pool_bytes, 43 + every)
+        load_h = W.fill_normal_np(ln, 44 + every)
+        pool = torch.from_numpy(pool_h).to(DEV)
+        load_arena = torch.from_numpy(load_h).to(DEV)
+        store_arena = torch.full((sn,), ARENA_FILL, dtype=torch.uint8, device=DEV)
+        st = _status()
+        tabs = dev_tables(inp.tables_src, DEV)
+        # the job arrays stay referenced until the synchronize: the kernels
+        # read them on other streams
+        d_lj, d_sj = dev_jobs(lj, DEV), dev_jobs(sj, DEV)
+        sa, sb = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+        fork = torch.cuda.Event()
+        fork.record()
+        sa.wait_event(fork)
+        sb.wait_event(fork)
+        lmc.lmc_load_blocks(Lp, m, lmc.LMC_KDA_LAST_BLOCK, pool, tabs, d_lj, load_arena, st, sa)
+        lmc.lmc_store_blocks(Lp, m, mode, pool, tabs, d_sj, store_arena, st, sb)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert oracle.load_blocks(Lo, m, False, pool_h, inp.tables_src, lj, load_h) == 0
+        store_o = np.full(sn, ARENA_FILL, dtype=np.uint8)
+        assert oracle.store_blocks(Lo, m, every, pool_h, inp.tables_src, sj, store_o) == 0
+        assert np.array_equal(pool.cpu().numpy(), pool_h)
+        assert np.array_equal(store_arena.cpu().numpy(), store_o)
+
+
+def test_temporaries_passed_to_side_streams_stay_valid(lmc):
+    """Job arrays built inline for calls on side streams are freed by Python
+    as soon as the calls return; the binding marks every tensor it hands to
+    a non-current stream as used by that stream, so torch's allocator cannot
+    give their memory to the next allocation while the kernels still read
+    it. The mixed step written that way (load of cached chunks and store of
+    new chunks, temporaries everywhere) is exact against the oracle."""
+    inp, Lp = case_inputs(W.CONFIGS[4], request_ids=list(range(24)))
+    Lo, C = inp.layout, inp.C
+    pool_h = W.fill_normal_np(Lo.pool_bytes, 45)
+    load_h = W.fill_normal_np(inp.load_arena_bytes, 46)
+    pool = torch.from_numpy(pool_h).to(DEV)
+    load_arena = torch.from_numpy(load_h).to(DEV)
+    store_arena = torch.full((inp.store_arena_bytes,), ARENA_FILL, dtype=torch.uint8, device=DEV)
+    st = _status()
+    sa, sb = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    for _ in range(3):
+        fork = torch.cuda.Event()
+        fork.record()
+        sa.wait_event(fork)
+        sb.wait_event(fork)
+        lmc.lmc_load(Lp, C, pool, dev_tables(inp.tables_src, DEV), dev_jobs(inp.load_jobs, DEV), load_arena, st, sa)
+        lmc.lmc_store(Lp, C, pool, dev_tables(inp.tables_src, DEV), dev_jobs(inp.store_jobs, DEV), store_arena, st,
+                      sb)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert oracle.load(Lo, C, pool_h, inp.tables_src, inp.load_jobs, load_h) == 0
+    store_o = np.full(inp.store_arena_bytes, ARENA_FILL, dtype=np.uint8)
+    assert oracle.store(Lo, C, pool_h, inp.tables_src, inp.store_jobs, store_o) == 0
+    assert np.array_equal(pool.cpu().numpy(), pool_h)
+    assert np.array_equal(store_arena.cpu().numpy(), store_o)
+
+
 def test_full_size_mixed_two_streams(lmc):
     """The full mixed step: 256 requests, 3 object groups (KDA, SWA-4096,
     MLA), load of hits concurrent with the store of new chunks."""
