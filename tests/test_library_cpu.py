@@ -578,3 +578,33 @@ def test_store_size_limits_refused_before_launch(lmc):
                              16, True, 4 << 30)
     b, keep = batch(L)
     assert store(L.handle, 16, addr, ctypes.byref(b), addr, 1 << 40, addr, None) == lmc.LMC_ERR_CUDA
+
+
+def test_check_disjoint_two_blocks_per_chunk_matches_oracle(lmc):
+    """The chunk-form guard with two blocks per chunk (KDA, SWA, MLA layers,
+    N = 4, chunk 8), on random planted table entries: library and oracle
+    name the same smallest shared block."""
+    import functools
+    layers = []
+    for _ in range(2):
+        layers += [{"kind": "KDA", "token_bytes": 0, "conv_bytes": 16, "rec_bytes": 64, "window": 0}] * 3
+        layers += [W.swa(16, 12), W.mla(16)]
+    cfg = W.Config(601, "mixed-small", layers, N=4, requested_chunk=8, packed=True, num_requests=8,
+                   lengths="fixed", fixed_lengths=(40, 23, 57, 31, 64, 17, 12, 48), snapshot="block", seed=7,
+                   mixed=True)
+    C = oracle.negotiate_chunk(8, 4)
+    inp = W.make_inputs(cfg, functools.partial(oracle.layout, layers, 4, True), C)
+    o = inp.layout
+    p = lmc.lmc_layout_build(layers, 4, True, o.pool_bytes)
+    rng = np.random.default_rng(8)
+    shared = 0
+    for t in range(60):
+        tables = [x.copy() for x in inp.tables_src]
+        if t:
+            k = int(rng.integers(0, len(tables)))
+            r, c = np.argwhere(tables[k] >= 0)[int(rng.integers(0, int((tables[k] >= 0).sum())))]
+            tables[k][r, c] = int(rng.integers(-1, o.num_blocks + 2))  # -1 and ids past the pool too
+        want = oracle.check_disjoint(o, C, tables, inp.load_jobs, tables, inp.store_jobs)
+        assert lmc.lmc_check_disjoint(p, C, tables, inp.load_jobs, tables, inp.store_jobs) == want, t
+        shared += want >= 0
+    assert shared >= 5
