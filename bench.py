@@ -377,6 +377,10 @@ class HostArena:
         import mmap
         self.torch, self.nbytes, self._map, self._ptr = torch, int(nbytes), None, None
         self.kind = "pinned (cudaHostAlloc)"
+        if self.nbytes > 0.85 * _host_free_bytes():
+            # faulting the pages in must not run the host out of memory
+            raise MemoryError(f"{self.nbytes} bytes of host memory requested, "
+                              f"{_host_free_bytes()} free")
         try:
             m = mmap.mmap(-1, max(self.nbytes, 1), flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
             m.madvise(mmap.MADV_HUGEPAGE)

@@ -123,3 +123,13 @@ def test_each_kernel_reports_its_fraction_of_peak():
     t = bench._with_frac(bench._kernel_times(7_000_000_000, [1.0]), 7000.0)
     assert t["gbs"] == 7000.0 and t["frac_of_peak"] == 1.0
     assert bench._with_frac(bench._kernel_times(0, [1.0]), 7000.0)["frac_of_peak"] is None
+
+
+def test_host_arena_refuses_more_than_free_memory(monkeypatch):
+    """The end-to-end step's host arena checks free host memory before it
+    faults pages in, and raises MemoryError (the step then reports itself
+    unavailable) rather than risk running the host out of memory."""
+    import torch
+    monkeypatch.setattr(bench, "_host_free_bytes", lambda: 1 << 20)
+    with pytest.raises(MemoryError):
+        bench.HostArena(torch, 1 << 30)
