@@ -11,6 +11,14 @@ written once (2 x payload per store, 2 x payload per load).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--impl reference]
 
+The line's headline is that workload. The default run then times the other
+workloads (configs 2-4) and operations (the INT8 codec, block-granular
+objects, in-pool copies) one after another in the same process, each as its
+own entry with CUDA-event times, clocks and roofline (`--no-extra-lines`
+times the selected one alone). The headline also carries the end-to-end
+step (objects through page-locked host memory and back) and the CPU oracle
+timed on the same payload.
+
 Under torchrun each rank runs its own copy of the workload on its own GPU
 (independent requests, no exchange between ranks); rank 0 prints one JSON line.
 """
